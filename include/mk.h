@@ -1,0 +1,226 @@
+/*
+ * mk.h — C ABI of the persistent MoE decode megakernel for GB300 (sm_103a).
+ *
+ * The library runs the token-generation decode step of a Flint-shaped
+ * mixture-of-experts transformer as ONE cooperative CUDA launch per step
+ * (one block per SM, grid-wide barriers only where data crosses blocks),
+ * as described for Apple's Metal in "rec Megakernel and Tempo9 Compared",
+ * §2 "Where Does rec's Single-Stream Advantage Come From?": input RMSNorm,
+ * QKV projection fused with RoPE and the KV write, split attention with a
+ * merge, output projection + residual, post-attention RMSNorm, router and
+ * top-k, expert gate/up -> SiLU -> down (dense MLP in the first layers), and
+ * after the last layer final norm, lm_head and argmax — all in one launch.
+ *
+ * Conventions shared by every call:
+ *  - Every function returns an int status (MK_OK == 0, else an MK_ERR_*
+ *    code) and never aborts the process.  mk_last_error() gives a message
+ *    for the calling thread's last failure.
+ *  - "device pointer" means memory on the context's CUDA device; "host
+ *    pointer" means ordinary (pageable or pinned) host memory.  No call
+ *    takes ownership of caller memory.
+ *  - Streams are passed as `void*` holding a cudaStream_t (NULL = legacy
+ *    default stream).  Launching calls are asynchronous on that stream and
+ *    return before the GPU work finishes; device-side failures (a grid
+ *    barrier that timed out, an index out of range) are reported by the next
+ *    mk_sync().
+ *  - A context is not thread-safe: calls on one context must be serialised
+ *    by the caller, and all launches of one context must be ordered on the
+ *    GPU (one stream, or explicit events between streams).
+ */
+#ifndef MK_H_
+#define MK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MK_API __attribute__((visibility("default")))
+#else
+#define MK_API
+#endif
+
+/* ---- status codes ---- */
+#define MK_OK 0
+#define MK_ERR_INVALID_ARG 1      /* a null pointer, bad size or index, misaligned weight */
+#define MK_ERR_NO_PAGES 2         /* the KV page pool has no free page */
+#define MK_ERR_STATE 3            /* call out of order (e.g. no KV pool, position mismatch) */
+#define MK_ERR_CUDA 4             /* a CUDA runtime call failed (message has the CUDA error) */
+#define MK_ERR_UNSUPPORTED 5      /* shape / dtype not compiled in, device not sm_103, no co-residency */
+#define MK_ERR_BARRIER_TIMEOUT 6  /* a grid barrier gave up waiting (reported by mk_sync) */
+#define MK_ERR_DEVICE_INDEX 7     /* the kernel's own bounds check refused an index (mk_sync) */
+
+/* ---- weight storage formats ---- */
+#define MK_F32 0        /* float32, row-major [rows, K] */
+#define MK_BF16 1       /* bfloat16, row-major [rows, K] */
+#define MK_INT4_G64 2   /* symmetric int4: codes [rows, K/2] uint8, two's-complement
+                           nibbles with the even k in the low nibble; scales
+                           [rows, K/64] bfloat16; w[r,k] = q[r,k] * s[r,k/64] */
+
+/* Model description.  The library compiles the decode step for fixed layer
+ * shapes; mk_create() answers MK_ERR_UNSUPPORTED for others.  Compiled shapes:
+ *   Flint: hidden 2048, 16 q / 4 kv heads of 128, 64 experts top-6 of FFN 768,
+ *          dense FFN 6144;
+ *   tiny:  hidden 256, 4 q / 2 kv heads of 64, 8 experts top-2 of FFN 128,
+ *          dense FFN 512.
+ * n_layers, n_dense, vocab, rope_theta and rms_eps are free.  page_tokens
+ * must be 128 and max_batch at most 16. */
+typedef struct mk_model_desc {
+  int32_t n_layers;
+  int32_t hidden;
+  int32_t n_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t vocab;
+  int32_t n_dense;      /* layers [0, n_dense) use the dense SwiGLU MLP */
+  int32_t dense_ffn;
+  int32_t n_experts;
+  int32_t top_k;
+  int32_t expert_ffn;
+  float rope_theta;
+  float rms_eps;
+  int32_t wdtype;       /* MK_F32 | MK_BF16 | MK_INT4_G64: the linear layers */
+  int32_t page_tokens;  /* must be 128 */
+  int32_t max_batch;    /* rows per launch, 1..16 */
+  int32_t max_ctx;      /* largest position + 1 any sequence may reach */
+  int32_t max_seqs;     /* sequence ids are 0 .. max_seqs-1 */
+} mk_model_desc;
+
+/* A linear weight: `w` points at the codes / values; `scales` only for int4. */
+typedef struct mk_linear {
+  const void* w;
+  const void* scales;
+} mk_linear;
+
+/* One layer's weights (device pointers, logical layouts above).  The
+ * "aux" tensors (norms, router, embedding) are float32 when wdtype is MK_F32
+ * and bfloat16 otherwise.
+ *   attn_norm, ffn_norm [hidden]
+ *   wq [n_heads*head_dim, hidden], wk / wv [n_kv_heads*head_dim, hidden],
+ *   wo [hidden, n_heads*head_dim]
+ *   dense layers (index < n_dense): gate, up [dense_ffn, hidden], down [hidden, dense_ffn]
+ *   MoE layers: router [n_experts, hidden]; exp_gate, exp_up
+ *   [n_experts, expert_ffn, hidden]; exp_down [n_experts, hidden, expert_ffn]
+ *   (int4 scales stacked the same way).  Unused fields may be NULL. */
+typedef struct mk_layer_weights {
+  const void* attn_norm;
+  mk_linear wq, wk, wv, wo;
+  const void* ffn_norm;
+  mk_linear gate, up, down;
+  const void* router;
+  mk_linear exp_gate, exp_up, exp_down;
+} mk_layer_weights;
+
+typedef struct mk_weights {
+  const void* embed;              /* [vocab, hidden] aux dtype */
+  const void* final_norm;         /* [hidden] aux dtype */
+  mk_linear lm_head;              /* [vocab, hidden] wdtype */
+  const mk_layer_weights* layers; /* HOST array of n_layers entries */
+} mk_weights;
+
+typedef struct mk_ctx mk_ctx;
+
+/* Information about a context (filled by mk_get_info). */
+typedef struct mk_info {
+  int32_t device;
+  int32_t num_sms;
+  int32_t grid;              /* blocks per launch (one per SM) */
+  int32_t block_threads;
+  int32_t smem_bytes;        /* dynamic shared memory per block */
+  int32_t n_pages;           /* KV pages in the pool (0 before mk_kv_alloc) */
+  int32_t free_pages;
+  int64_t scratch_bytes;     /* library-owned device scratch */
+  int64_t kv_bytes;          /* KV pool bytes */
+  int32_t last_chunk;        /* attention split size (tokens) of the last launch */
+  int32_t last_units;        /* attention work units of the last launch */
+} mk_info;
+
+/* Create a context on the current CUDA device.
+ * d: model description (copied).  w: weight pointers in the logical layouts
+ * above; every pointer must be 16-byte aligned.  The weights are BORROWED:
+ * the library reads them in place and they must stay valid and unchanged
+ * until mk_destroy.  The host array w->layers is copied and may be freed
+ * after the call.  Allocates library-owned scratch and the RoPE table
+ * (computed on the host in double precision).  *out receives the context.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+MK_API int mk_create(const mk_model_desc* d, const mk_weights* w, mk_ctx** out);
+
+/* Allocate the KV cache: a pool of n_pages pages of page_tokens (128)
+ * positions for every layer, bf16, laid out
+ * [layer][page][K|V][kv_head][slot][head_dim], owned by the library.
+ * Call once per context; a second call returns MK_ERR_STATE.
+ * Errors: INVALID_ARG, STATE, CUDA. */
+MK_API int mk_kv_alloc(mk_ctx* ctx, int32_t n_pages);
+
+/* Prefill: run n (1..4096) prompt tokens of sequence seq_id at positions
+ * start_pos .. start_pos+n-1 through the model, writing their K/V into
+ * pages taken from the pool ("rec prefills in 4096-token chunks",
+ * "rec Megakernel and Tempo9 Compared", §1 "Prefill").  start_pos must
+ * equal the sequence's current length (0 starts a new sequence).
+ * tokens_dev: device int32[n].  out_token_dev: device int32[1] that receives
+ * the greedy next token after the last position (may be NULL).
+ * The chunk runs as launches of up to max_batch positions each.
+ * Errors: INVALID_ARG, STATE, NO_PAGES (nothing is launched then), CUDA. */
+MK_API int mk_prefill_chunk(mk_ctx* ctx, int32_t seq_id, const int32_t* tokens_dev,
+                            int32_t n, int32_t start_pos, int32_t* out_token_dev,
+                            void* stream);
+
+/* One decode step for n (1..max_batch) sequences in ONE launch (continuous
+ * batching: any set of open sequences, each at its own position).
+ * seq_ids_host, positions_host: host int32[n]; positions[i] must equal the
+ * length of sequence seq_ids[i] (ids distinct).  tokens_dev: device int32[n]
+ * input tokens; out_tokens_dev: device int32[n] greedy next tokens.
+ * tokens_dev may alias out_tokens_dev, so steps chain on the GPU with no host
+ * synchronisation.  On success every sequence's length grows by one.
+ * Errors: INVALID_ARG, STATE, NO_PAGES (nothing is launched then), CUDA. */
+MK_API int mk_decode_step(mk_ctx* ctx, const int32_t* seq_ids_host, const int32_t* tokens_dev,
+                          const int32_t* positions_host, int32_t n, int32_t* out_tokens_dev,
+                          void* stream);
+
+/* Close a sequence and return its pages to the pool.  Pages become reusable
+ * by launches enqueued after this call on the context's stream.
+ * Errors: INVALID_ARG (bad id), STATE (sequence not open). */
+MK_API int mk_seq_release(mk_ctx* ctx, int32_t seq_id);
+
+/* Current length (positions written) of a sequence; -1 if it is not open. */
+MK_API int32_t mk_seq_length(mk_ctx* ctx, int32_t seq_id);
+
+/* Wait for the stream, then read and clear the device error word.
+ * Returns MK_OK, MK_ERR_BARRIER_TIMEOUT, MK_ERR_DEVICE_INDEX or MK_ERR_CUDA. */
+MK_API int mk_sync(mk_ctx* ctx, void* stream);
+
+/* Debugging.  flags: MK_DBG_TRACE makes every launch write its trace into
+ * trace_dev (device float buffer of trace_bytes, laid out as documented for
+ * mk_trace_bytes).  MK_DBG_SKIP_ARRIVAL makes block `arg & 0xffff` skip its
+ * arrival at grid barrier number `arg >> 16` of the next launch, so that the
+ * other blocks' bounded waits run out (a test of the timeout path).
+ * spin_limit_us bounds every grid-barrier wait (0 keeps the default, 1 s).
+ * Errors: INVALID_ARG. */
+#define MK_DBG_TRACE 1u
+#define MK_DBG_SKIP_ARRIVAL 2u
+MK_API int mk_set_debug(mk_ctx* ctx, uint32_t flags, uint32_t arg, void* trace_dev,
+                        size_t trace_bytes, uint32_t spin_limit_us);
+
+/* Size of the trace for one launch of `rows` rows.  Layout (float32):
+ *   x      [n_layers][rows][hidden]     residual after each layer
+ *   attn   [n_layers][rows][n_heads*head_dim]  attention output (merged)
+ *   logits [n_layers][rows][n_experts]  router logits (0 for dense layers)
+ *   topk   [n_layers][rows][2*top_k]    expert ids (as float) then weights
+ *   final  [rows][vocab]                lm_head logits (rows with an output) */
+MK_API size_t mk_trace_bytes(const mk_model_desc* d, int32_t rows);
+
+MK_API int mk_get_info(mk_ctx* ctx, mk_info* info);
+
+/* Release every resource of the context (waits for its device work). */
+MK_API int mk_destroy(mk_ctx* ctx);
+
+/* Message of the calling thread's last failure ("" if none). */
+MK_API const char* mk_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H_ */

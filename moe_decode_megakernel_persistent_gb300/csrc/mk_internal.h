@@ -1,0 +1,103 @@
+// Internal types shared by the host library (mk_host.cpp) and the decode
+// kernel (mk_kernel.cu).  Not part of the public ABI.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include "mk.h"
+
+namespace mk {
+
+constexpr int kMaxBatch = 16;        // rows per launch
+constexpr int kPageTokens = 128;     // KV positions per page
+constexpr int kThreads = 512;        // threads per block (16 warps)
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxUpd = 64;          // block-table updates carried by one launch
+constexpr int kMaxRowsPerBlock = 32; // hidden rows owned by one block (hidden / grid)
+constexpr int kSmemBytes = 200 * 1024;  // dynamic shared memory per block
+
+// Linear-weight slots of a layer.
+enum Lin { WQ = 0, WK, WV, WO, GATE, UP, DOWN, EGATE, EUP, EDOWN, NLIN };
+
+// Device-side copy of one layer's weight pointers.
+struct LayerW {
+  const void* attn_norm;
+  const void* ffn_norm;
+  const void* router;
+  const void* w[NLIN];
+  const void* s[NLIN];   // int4 scales (null otherwise)
+};
+
+struct PageUpd {
+  int32_t slot;   // sequence id
+  int32_t index;  // page index within the sequence
+  int32_t page;   // pool page
+};
+
+// Library-owned device scratch (one allocation, carved on the host).
+struct Scratch {
+  float* x;          // [kMaxBatch][H] residual stream
+  float* h;          // [kMaxBatch][H] residual after attention
+  float* q;          // [kMaxBatch][n_heads*hd] roped queries
+  float* attn;       // [kMaxBatch][n_heads*hd] merged attention output
+  float* part;       // [max_units][gqa][hd + 2] attention partials (m, l, o[hd])
+  float* rpart;      // [grid][kMaxBatch][E] router partial logits
+  float* rlogit;     // [kMaxBatch][E] reduced (un-normalised) router logits
+  float* act;        // [kMaxBatch][top_k][Fe] expert activations
+  float* dact;       // [kMaxBatch][Fd] dense-MLP activations
+  float* amax_v;     // [grid][kMaxBatch] per-block best logit
+  int32_t* amax_i;   // [grid][kMaxBatch] per-block best token
+  int32_t* merge_cnt;   // [kMaxBatch][n_kv] attention merge arrivals
+  uint32_t* sync;       // counters, one per 128-byte line: [0] barrier, [32] exit,
+                        // [64] router reduce, [96] argmax reduce
+  int32_t* err;         // [0] status, [1] site, [2] detail
+};
+
+struct StepArgs {
+  const LayerW* layers;
+  const void* embed;
+  const void* final_norm;
+  const void* lm_head;
+  const void* lm_head_s;
+  const float2* rope;        // [max_ctx][hd/2] (cos, sin)
+  uint16_t* kv;              // bf16 pool
+  int32_t* block_table;      // [max_seqs][max_pages_per_seq]
+  Scratch sc;
+  const int32_t* tokens;     // [n] (device)
+  int32_t* out_tokens;       // written for rows >= out_first at out_tokens[row - out_first]
+  float* trace;              // debug trace or null
+  int32_t n_pages;
+  int32_t max_pages_per_seq;
+  int32_t n;                 // rows in this launch
+  int32_t n_layers;
+  int32_t n_dense;
+  int32_t vocab;
+  float eps;
+  int32_t chunk;             // attention split size (tokens)
+  int32_t n_units;           // attention work units
+  int32_t out_first;         // first row that gets an lm_head output (n = none)
+  int32_t max_units;         // capacity of sc.part
+  int32_t n_upd;
+  uint32_t dbg_flags;
+  uint32_t dbg_arg;
+  uint64_t spin_limit_ns;
+  int32_t slot[kMaxBatch];
+  int32_t pos[kMaxBatch];
+  int32_t cur_page[kMaxBatch];
+  PageUpd upd[kMaxUpd];
+};
+
+// Error sites recorded in err[1].
+enum ErrSite { SITE_BARRIER = 1, SITE_PAGE = 2, SITE_UNIT = 3, SITE_TOKEN = 4 };
+
+// Kernel variants compiled into the library.
+enum ShapeId { SHAPE_FLINT = 0, SHAPE_TINY = 1, NSHAPE };
+
+struct KernelInfo {
+  const void* fn;
+  int smem_bytes;
+};
+
+// Returns the kernel for (shape, wdtype) or fn == nullptr if not compiled.
+KernelInfo get_kernel(int shape, int wdtype);
+
+}  // namespace mk

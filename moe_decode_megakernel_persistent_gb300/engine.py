@@ -1,0 +1,214 @@
+"""Python-side driver over the C ABI: an Engine that owns one library context
+(weights borrowed from torch tensors, KV pool, trace buffer) and a Batcher
+that runs continuous batching over it.  PyTorch supplies device memory and
+streams only; every step of the decode path runs in the library's kernel.
+
+Weight dict format (what `Engine` expects), torch tensors on the GPU in the
+logical layouts of include/mk.h:
+    ("embed",) [V, H]   ("final_norm",) [H]   ("lm_head",) W or (codes, scales)
+    ("attn_norm", l) ("ffn_norm", l) [H]
+    ("wq"|"wk"|"wv"|"wo", l)                   W or (codes, scales)
+    dense layers: ("gate"|"up"|"down", l)      W or (codes, scales)
+    MoE layers:   ("router", l) [E, H]
+                  ("exp_gate"|"exp_up"|"exp_down", l)  stacked over experts
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import torch
+
+from . import _lib as L
+
+MAX_PREFILL = 4096
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _lin(x) -> L.mk_linear:
+    if isinstance(x, tuple):
+        return L.mk_linear(_ptr(x[0]), _ptr(x[1]))
+    return L.mk_linear(_ptr(x), None)
+
+
+def make_desc(shape, max_batch: int = 16, max_ctx: int = 16384, max_seqs: int = 64) -> L.mk_model_desc:
+    """mk_model_desc from an object with the model fields (n_layers, hidden, ...)."""
+    return L.mk_model_desc(
+        n_layers=shape.n_layers, hidden=shape.hidden, n_heads=shape.n_heads,
+        n_kv_heads=shape.n_kv_heads, head_dim=shape.head_dim, vocab=shape.vocab,
+        n_dense=shape.n_dense, dense_ffn=shape.dense_ffn, n_experts=shape.n_experts,
+        top_k=shape.top_k, expert_ffn=shape.expert_ffn, rope_theta=shape.rope_theta,
+        rms_eps=shape.rms_eps, wdtype=L.WDTYPES[shape.wdtype], page_tokens=128,
+        max_batch=max_batch, max_ctx=max_ctx, max_seqs=max_seqs)
+
+
+class Engine:
+    """One library context: weights, KV pool, sequences."""
+
+    def __init__(self, shape, weights: dict, n_pages: int, max_batch: int = 16,
+                 max_ctx: int = 16384, max_seqs: int = 64, device: Optional[int] = None):
+        L.load()
+        if device is not None:
+            torch.cuda.set_device(device)
+        self.shape = shape
+        self.desc = make_desc(shape, max_batch, max_ctx, max_seqs)
+        self._weights = weights  # keep the borrowed tensors alive
+        layers = (L.mk_layer_weights * shape.n_layers)()
+        for l in range(shape.n_layers):
+            lw = layers[l]
+            lw.attn_norm = _ptr(weights[("attn_norm", l)])
+            lw.ffn_norm = _ptr(weights[("ffn_norm", l)])
+            for name in ("wq", "wk", "wv", "wo"):
+                setattr(lw, name, _lin(weights[(name, l)]))
+            if l < shape.n_dense:
+                for name in ("gate", "up", "down"):
+                    setattr(lw, name, _lin(weights[(name, l)]))
+            else:
+                lw.router = _ptr(weights[("router", l)])
+                for name in ("exp_gate", "exp_up", "exp_down"):
+                    setattr(lw, name, _lin(weights[(name, l)]))
+        self._layers = layers
+        w = L.mk_weights(embed=_ptr(weights[("embed",)]), final_norm=_ptr(weights[("final_norm",)]),
+                         lm_head=_lin(weights[("lm_head",)]), layers=layers)
+        self.ctx = L.mk_create(self.desc, w)
+        L.mk_kv_alloc(self.ctx, n_pages)
+        self.trace = None
+        self.max_batch = max_batch
+
+    @property
+    def stream(self) -> int:
+        return torch.cuda.current_stream().cuda_stream
+
+    # ---- decode path
+    def prefill(self, seq_id: int, tokens: torch.Tensor, start_pos: int = 0,
+                out: Optional[torch.Tensor] = None) -> Optional[torch.Tensor]:
+        """Run prompt tokens (int32 CUDA tensor) in chunks of at most 4096;
+        returns the device int32[1] next token after the last position."""
+        n = tokens.numel()
+        if out is None:
+            out = torch.empty(1, dtype=torch.int32, device=tokens.device)
+        for off in range(0, n, MAX_PREFILL):
+            m = min(MAX_PREFILL, n - off)
+            last = off + m == n
+            L.mk_prefill_chunk(self.ctx, seq_id, _ptr(tokens) + 4 * off, m, start_pos + off,
+                               _ptr(out) if last else None, self.stream)
+        return out
+
+    def decode_step(self, seq_ids, tokens: torch.Tensor, positions, out: torch.Tensor):
+        L.mk_decode_step(self.ctx, list(seq_ids), _ptr(tokens), list(positions), _ptr(out),
+                         self.stream)
+        return out
+
+    def release(self, seq_id: int):
+        L.mk_seq_release(self.ctx, seq_id)
+
+    def seq_length(self, seq_id: int) -> int:
+        return L.mk_seq_length(self.ctx, seq_id)
+
+    def sync(self):
+        L.mk_sync(self.ctx, self.stream)
+
+    def info(self) -> dict:
+        return L.mk_get_info(self.ctx)
+
+    # ---- debugging
+    def enable_trace(self, rows: int):
+        nbytes = L.mk_trace_bytes(self.desc, rows)
+        self.trace = torch.zeros(nbytes // 4, dtype=torch.float32, device="cuda")
+        L.mk_set_debug(self.ctx, L.MK_DBG_TRACE, 0, _ptr(self.trace), nbytes, 0)
+
+    def disable_trace(self):
+        L.mk_set_debug(self.ctx, 0, 0, 0, 0, 0)
+        self.trace = None
+
+    def split_trace(self, rows: int) -> dict:
+        """Views of the trace of the last launch of `rows` rows."""
+        s = self.shape
+        Ln, H, QD, E, K, V = s.n_layers, s.hidden, s.n_heads * s.head_dim, s.n_experts, s.top_k, s.vocab
+        t = self.trace
+        o = 0
+        out = {}
+        for name, shp in (("x", (Ln, rows, H)), ("attn", (Ln, rows, QD)),
+                          ("router_logits", (Ln, rows, E)), ("topk", (Ln, rows, 2 * K)),
+                          ("logits", (rows, V))):
+            sz = 1
+            for d in shp:
+                sz *= d
+            out[name] = t[o:o + sz].view(shp)
+            o += sz
+        return out
+
+    def close(self):
+        if self.ctx:
+            L.mk_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+@dataclasses.dataclass
+class Request:
+    seq_id: int
+    prompt: torch.Tensor         # int32 CUDA tensor
+    max_new: int
+    arrival: int = 0             # step at which it joins
+    generated: list = dataclasses.field(default_factory=list)
+    finish_step: int = -1
+
+
+class Batcher:
+    """Continuous batching: every step, requests whose arrival step has come
+    are prefilled and join; the active set (up to max_batch) runs as ONE
+    decode launch; finished requests leave and release their pages.  Tokens
+    stay on the device between steps; the host reads them back once per step
+    in one copy (needed to know the tokens; they are also the output)."""
+
+    def __init__(self, engine: Engine):
+        self.e = engine
+
+    def run(self, requests: list, read_back: bool = True) -> dict:
+        e = self.e
+        dev = torch.device("cuda")
+        pending = sorted(requests, key=lambda r: (r.arrival, r.seq_id))
+        active: list = []
+        tok_dev = {}           # seq_id -> device int32[1] with its next input token
+        step = 0
+        steps_run = 0
+        while pending or active:
+            while pending and pending[0].arrival <= step and len(active) < e.max_batch:
+                r = pending.pop(0)
+                out = e.prefill(r.seq_id, r.prompt)
+                tok_dev[r.seq_id] = out
+                r.generated.append(out)  # first generated token (device)
+                active.append(r)
+            if active:
+                ids = [r.seq_id for r in active]
+                pos = [e.seq_length(i) for i in ids]
+                toks = torch.cat([tok_dev[i] for i in ids])
+                outs = torch.empty(len(ids), dtype=torch.int32, device=dev)
+                e.decode_step(ids, toks, pos, outs)
+                steps_run += 1
+                still = []
+                for k, r in enumerate(active):
+                    o = outs[k:k + 1]
+                    tok_dev[r.seq_id] = o
+                    r.generated.append(o)
+                    if len(r.generated) >= r.max_new:
+                        r.finish_step = step
+                        e.release(r.seq_id)
+                    else:
+                        still.append(r)
+                active = still
+            step += 1
+        if read_back:
+            for r in requests:
+                r.generated = [int(t.item()) for t in r.generated]
+        return {"steps": step, "launches": steps_run,
+                "finish_step": max(r.finish_step for r in requests)}

@@ -1,0 +1,172 @@
+"""GPU-vs-oracle parity harness.
+
+Both sides get the same seeded inputs: the weights come from the generator in
+`synth` (drawn on the GPU with PyTorch, bit-identical to its NumPy path; the
+oracle reads host copies of those generator outputs), the prompt from
+`synth.prompts`.  The oracle generates its own greedy trajectory; the GPU is
+teacher-forced on the ORACLE's tokens, so every GPU step sees exactly the
+oracle's inputs.  Compared:
+  - per-layer residual, attention output: relative L2 per row <= tol
+  - router top-k ids as sets, wherever the oracle's k / k+1 logit margin > 1e-3
+  - greedy tokens wherever the oracle's top-2 logit margin > 0.05
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import Oracle
+from synth import prompts as SP
+from synth import weights as SW
+from moe_decode_megakernel_persistent_gb300.engine import Engine
+
+TOPK_MARGIN = 1e-3
+TOKEN_MARGIN = 0.05
+
+
+def tol_for(m) -> float:
+    return 2e-2 if m.wdtype == "int4" else 1e-2
+
+
+def gpu_weights(m):
+    return SW.model_torch(m, "cuda")
+
+
+def host_fetch(m, w):
+    """Oracle fetch over host copies of the generator's tensors."""
+    cache = {}
+
+    def to_np(t):
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).cpu().numpy().view(np.uint16)
+        return t.cpu().numpy()
+
+    def fetch(name, layer, expert):
+        key = (name, layer, expert)
+        if key in cache:
+            return cache[key]
+        k = (name,) if layer < 0 else (name, layer)
+        t = w[k]
+        if expert is not None:
+            t = (t[0][expert], t[1][expert]) if isinstance(t, tuple) else t[expert]
+        if isinstance(t, tuple):
+            raw = (to_np(t[0]), to_np(t[1]))
+            dt = "int4"
+        else:
+            raw = to_np(t)
+            dt = "f32" if t.dtype == torch.float32 else "bf16"
+        if expert is None and name in ("embed", "lm_head", "wq", "wk", "wv", "wo"):
+            cache[key] = (raw, dt)
+        return raw, dt
+    return fetch
+
+
+def rel_l2(a, b) -> np.ndarray:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    num = np.linalg.norm((a - b).reshape(a.shape[0], -1), axis=1)
+    den = np.linalg.norm(b.reshape(b.shape[0], -1), axis=1)
+    return num / np.maximum(den, 1e-30)
+
+
+class Report:
+    def __init__(self):
+        self.max_x = 0.0
+        self.max_attn = 0.0
+        self.tokens_checked = 0
+        self.tokens_unpinned = 0
+        self.topk_checked = 0
+        self.topk_unpinned = 0
+        self.failures = []
+
+    def __repr__(self):
+        return (f"max_x={self.max_x:.3e} max_attn={self.max_attn:.3e} tokens {self.tokens_checked} "
+                f"checked / {self.tokens_unpinned} unpinned, topk {self.topk_checked} / "
+                f"{self.topk_unpinned}, failures={self.failures[:5]}")
+
+
+def compare_trace(rep: Report, m, tr_gpu: dict, tr_orc: dict, rows_gpu, rows_orc, tol, tag):
+    """Compare rows `rows_gpu` of a GPU trace with rows `rows_orc` of an oracle trace."""
+    for l in range(m.n_layers):
+        xg = tr_gpu["x"][l][rows_gpu].double().cpu().numpy()
+        xo = tr_orc["x"][l][rows_orc]
+        e = rel_l2(xg, xo).max()
+        rep.max_x = max(rep.max_x, e)
+        if e > tol:
+            rep.failures.append(f"{tag} layer {l} x rel_l2 {e:.3e}")
+        ag = tr_gpu["attn"][l][rows_gpu].double().cpu().numpy()
+        ao = tr_orc["attn"][l][rows_orc]
+        e = rel_l2(ag, ao).max()
+        rep.max_attn = max(rep.max_attn, e)
+        if e > tol:
+            rep.failures.append(f"{tag} layer {l} attn rel_l2 {e:.3e}")
+        if l >= m.n_dense:
+            li = l - m.n_dense
+            ids_g = tr_gpu["topk"][l][rows_gpu][:, :m.top_k].cpu().numpy().astype(np.int64)
+            ids_o = tr_orc["topk_ids"][li][rows_orc]
+            mg = tr_orc["topk_margin"][li][rows_orc]
+            for r in range(len(ids_o)):
+                if mg[r] > TOPK_MARGIN:
+                    rep.topk_checked += 1
+                    if set(ids_g[r]) != set(ids_o[r]):
+                        rep.failures.append(f"{tag} layer {l} row {r} topk {sorted(ids_g[r])} != {sorted(ids_o[r])}")
+                else:
+                    rep.topk_unpinned += 1
+
+
+def check_token(rep: Report, tok_gpu: int, tok_orc: int, margin: float, tag):
+    if margin > TOKEN_MARGIN:
+        rep.tokens_checked += 1
+        if tok_gpu != tok_orc:
+            rep.failures.append(f"{tag} token {tok_gpu} != {tok_orc} (margin {margin:.3f})")
+    else:
+        rep.tokens_unpinned += 1
+
+
+def run_single(m, prompt_len: int, n_decode: int, *, seed_seq: int = 0, eng: Engine = None,
+               w=None, orc: Oracle = None, seq_id: int = 0, n_pages: int = 256) -> Report:
+    """Prefill + teacher-forced decode of one sequence, traced on both sides."""
+    rep = Report()
+    tol = tol_for(m)
+    own = eng is None
+    if w is None:
+        w = gpu_weights(m)
+    if eng is None:
+        eng = Engine(m, w, n_pages=n_pages, max_ctx=prompt_len + n_decode + 8)
+    if orc is None:
+        orc = Oracle(m, host_fetch(m, w), cache_bytes=8 << 30)
+    prompt = SP.prompt_tokens(m.seed, m.vocab, prompt_len, seq=seed_seq)
+    kv = orc.new_kv()
+    tok_o, tr_o = orc.prefill(kv, prompt)
+    # GPU prefill; the trace holds the last launch (the final <=16 prompt rows)
+    last_rows = prompt_len - ((prompt_len - 1) // 16) * 16
+    eng.enable_trace(16)
+    pt = torch.from_numpy(prompt).cuda()
+    out = eng.prefill(seq_id, pt)
+    eng.sync()
+    tg = eng.split_trace(last_rows)
+    tok_g = int(out.item())
+    compare_trace(rep, m, tg, tr_o, slice(0, last_rows), slice(prompt_len - last_rows, prompt_len), tol, "prefill")
+    check_token(rep, tok_g, tok_o, float(tr_o["top2_margin"][-1]), "prefill")
+    fin = tg["logits"][last_rows - 1].double().cpu().numpy()
+    e = rel_l2(fin[None], tr_o["logits"][-1:])[0]
+    if e > tol:
+        rep.failures.append(f"prefill final logits rel_l2 {e:.3e}")
+    # teacher-forced decode on the oracle's tokens
+    cur = tok_o
+    tin = torch.empty(1, dtype=torch.int32, device="cuda")
+    tout = torch.empty(1, dtype=torch.int32, device="cuda")
+    for i in range(n_decode):
+        pos = prompt_len + i
+        nxt_o, tr_o = orc.decode(kv, cur, pos)
+        tin.fill_(cur)
+        eng.decode_step([seq_id], tin, [pos], tout)
+        eng.sync()
+        tg = eng.split_trace(1)
+        compare_trace(rep, m, tg, tr_o, slice(0, 1), slice(0, 1), tol, f"step {i}")
+        check_token(rep, int(tout.item()), nxt_o, float(tr_o["top2_margin"][-1]), f"step {i}")
+        cur = nxt_o
+    eng.disable_trace()
+    if own:
+        eng.close()
+    return rep

@@ -1,0 +1,91 @@
+"""The C-ABI library: builds, loads without a GPU, exports every symbol the
+header declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import synth
+from moe_decode_megakernel_persistent_gb300 import _build
+from moe_decode_megakernel_persistent_gb300 import _lib as L
+from moe_decode_megakernel_persistent_gb300.engine import make_desc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return L.load()
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "mk.h")).read()
+    return set(re.findall(r"MK_API\s+[\w\s\*]+?\b(mk_\w+)\s*\(", text))
+
+
+def test_header_declares_the_four_boundary_calls():
+    syms = header_symbols()
+    assert {"mk_create", "mk_kv_alloc", "mk_decode_step", "mk_prefill_chunk"} <= syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    syms = header_symbols()
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert syms == set(L.SIGNATURES), "binding covers exactly the declared ABI"
+
+
+def _desc(cfg=1, **kw):
+    d = make_desc(synth.CONFIGS[cfg].model)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_create_rejects_bad_descriptions_without_cuda(lib):
+    out = C.c_void_p()
+    w = L.mk_weights()
+    assert lib.mk_create(None, C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_create(C.byref(_desc()), C.byref(w), None) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_create(C.byref(_desc(hidden=512)), C.byref(w), C.byref(out)) == L.MK_ERR_UNSUPPORTED
+    assert lib.mk_create(C.byref(_desc(page_tokens=64)), C.byref(w), C.byref(out)) == L.MK_ERR_UNSUPPORTED
+    assert lib.mk_create(C.byref(_desc(max_batch=17)), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_create(C.byref(_desc(wdtype=9)), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_create(C.byref(_desc(n_dense=5)), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_create(C.byref(_desc()), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    assert "NULL" in L.mk_last_error()
+    assert out.value is None
+
+
+def test_create_rejects_misaligned_weights(lib):
+    d = _desc()
+    layers = (L.mk_layer_weights * d.n_layers)()
+    w = L.mk_weights(embed=0x1000, final_norm=0x2000, lm_head=L.mk_linear(0x3008, None), layers=layers)
+    out = C.c_void_p()
+    assert lib.mk_create(C.byref(d), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    assert "lm_head" in L.mk_last_error()
+    w.lm_head = L.mk_linear(0x3000, None)
+    assert lib.mk_create(C.byref(d), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    assert "attn_norm" in L.mk_last_error()
+
+
+def test_null_context_calls_fail_cleanly(lib):
+    assert lib.mk_kv_alloc(None, 4) == L.MK_ERR_INVALID_ARG
+    ids = (C.c_int32 * 1)(0)
+    assert lib.mk_decode_step(None, ids, 16, ids, 1, 16, None) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_prefill_chunk(None, 0, 16, 1, 0, None, None) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_seq_release(None, 0) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_seq_length(None, 0) == -1
+    assert lib.mk_sync(None, None) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_get_info(None, None) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_destroy(None) == L.MK_OK
+
+
+def test_trace_bytes_layout(lib):
+    m = synth.CONFIGS[3].model
+    d = make_desc(m)
+    per_layer = m.hidden + m.n_heads * m.head_dim + m.n_experts + 2 * m.top_k
+    assert L.mk_trace_bytes(d, 3) == 4 * (m.n_layers * 3 * per_layer + 3 * m.vocab)
+    assert L.mk_trace_bytes(d, 0) == 0
