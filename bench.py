@@ -1,0 +1,456 @@
+"""Decode benchmark of the persistent MoE megakernel.
+
+Default workload: the Flint-shaped int4 model (49 layers, hidden 2048, 64
+experts top-6, layers 0-1 dense; symmetric int4 group-64 weights from seeded
+bf16 N(0, 0.02)), a 2048-token seeded prompt prefilled, then greedy decode
+at batch 1.  A step = one decode launch (the whole model, one token).
+Timed: exactly --steps steps after --warmup untimed ones (on another
+sequence), CUDA events on the launching stream, barrier + synchronize on
+both sides.  The step streams ~1.2 GB of weights, far more than L2 (129 MB),
+so no L2 flush is needed between steps.
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (the baseline arm).  Multi-GPU: independent replicas, one process
+per GPU (no collective on the data path), `value` = tokens of all ranks /
+max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+METRIC = "decode tok/s at batch 1 and 16; achieved HBM GB/s vs GB300 peak"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+# ------------------------------------------------------------------ bytes model
+
+def step_bytes(m, ctxs, distinct_experts_per_layer) -> int:
+    """Algorithmic HBM bytes of one decode step: every weight byte the step
+    needs once (norms, attention, router, the distinct selected experts,
+    dense MLPs, lm_head, the embedding rows) + the KV cache read (all cached
+    positions incl. the new one) + the KV written."""
+    H, E = m.hidden, m.n_experts
+    if m.wdtype == "int4":
+        def lin(rows, K):
+            return rows * K // 2 + rows * (K // 64) * 2
+    else:
+        bpe = 2 if m.wdtype == "bf16" else 4
+
+        def lin(rows, K):
+            return rows * K * bpe
+    aux = 2 if m.aux_dtype == "bf16" else 4
+    attn = lin(m.q_dim, H) + 2 * lin(m.kv_dim, H) + lin(H, m.q_dim) + 2 * H * aux
+    expert = 2 * lin(m.expert_ffn, H) + lin(H, m.expert_ffn)
+    dense = 2 * lin(m.dense_ffn, H) + lin(H, m.dense_ffn)
+    total = 0
+    for l in range(m.n_layers):
+        total += attn
+        if l < m.n_dense:
+            total += dense
+        else:
+            total += E * H * aux + distinct_experts_per_layer * expert
+    total += lin(m.vocab, H) + H * aux + len(ctxs) * H * aux
+    kv_tok = m.n_layers * 2 * m.kv_dim * 2
+    total += sum(ctxs) * kv_tok                 # read (includes the new position)
+    total += len(ctxs) * kv_tok                 # write
+    return int(total)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_decode_megakernel_persistent_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", f"step_kernel_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    src = None
+    traffic = None
+    for line in open(p):
+        if line.startswith("kernel_source_hash:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    if src != kernel_source_hash():
+        return None
+    return traffic
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU baseline
+
+def cpu_baseline(m, weights, n_steps: int = 2, prompt_len: int = 4):
+    """The oracle as it stands, on this host's cores: a bounded sample of the
+    workload (batch-1 decode steps at a short context; weight dequantisation
+    included; copying the generator's weights to the host excluded)."""
+    from oracle import Oracle
+    from synth import prompts as SP
+    from tests._parity import host_fetch
+    base = host_fetch(m, weights)
+    spent = [0.0]
+
+    def fetch(*k):
+        t0 = time.perf_counter()
+        r = base(*k)
+        spent[0] += time.perf_counter() - t0
+        return r
+    prompt = SP.prompt_tokens(m.seed, m.vocab, prompt_len)
+    orc = Oracle(m, fetch, cache_bytes=1 << 30)
+    kv = orc.new_kv()
+    tok, _ = orc.prefill(kv, prompt)
+    s0 = spent[0]
+    t0 = time.perf_counter()
+    for i in range(n_steps):
+        tok, _ = orc.decode(kv, tok, prompt_len + i)
+    dt = time.perf_counter() - t0 - (spent[0] - s0)
+    return {"value": round(n_steps / dt, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_steps} float64 oracle decode steps of the same model at batch 1, context "
+                      f"{prompt_len + 1}..{prompt_len + n_steps} (the workload's is 2048+), "
+                      f"dequantisation included, BLAS single-threaded"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world):
+    import torch
+    import synth
+    from synth import prompts as SP
+    from synth import weights as SW
+    from moe_decode_megakernel_persistent_gb300 import _build
+    from moe_decode_megakernel_persistent_gb300.engine import Engine
+
+    _build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = synth.CONFIGS[args.config]
+    m = w.model
+    K, W = args.steps, args.warmup
+    t0 = time.time()
+    weights = SW.model_torch(m, dev)
+    torch.cuda.synchronize()
+    gen_s = time.time() - t0
+    prompt_len = w.prompt_len
+    max_ctx = prompt_len + K + 2 * args.e2e_steps + W + 64
+    pages = 3 * ((max_ctx + 127) // 128) + 8
+    eng = Engine(m, weights, n_pages=pages, max_ctx=max_ctx, max_seqs=4)
+    stream = torch.cuda.current_stream()
+
+    # warm-up sequence: a short prompt and W decode steps
+    wtok = torch.from_numpy(SP.prompt_tokens(m.seed, m.vocab, 64, seq=1)).to(dev)
+    tok1 = eng.prefill(1, wtok)
+    for i in range(W):
+        eng.decode_step([1], tok1, [64 + i], tok1)
+    eng.sync()
+    eng.release(1)
+
+    # the measured sequence: prefill the prompt, then K timed decode steps
+    prompt = torch.from_numpy(SP.prompt_tokens(m.seed, m.vocab, prompt_len)).to(dev)
+    t0 = time.time()
+    tok = eng.prefill(0, prompt)
+    eng.sync()
+    prefill_s = time.time() - t0
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        eng.decode_step([0], tok, [prompt_len + i], tok)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    eng.sync()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / K
+
+    # end to end through the public API with host buffers: each step copies
+    # its input token from pinned host memory, runs, reads the result back
+    E = args.e2e_steps
+    h_in = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    h_out = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    d_in = torch.empty(1, dtype=torch.int32, device=dev)
+    d_out = torch.empty(1, dtype=torch.int32, device=dev)
+    tok2 = eng.prefill(2, prompt)
+    h_in.copy_(tok2.cpu())
+    eng.sync()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(E):
+        d_in.copy_(h_in, non_blocking=True)
+        eng.decode_step([2], d_in, [prompt_len + i], d_out)
+        h_out.copy_(d_out, non_blocking=True)
+        stream.synchronize()
+        h_in[0] = h_out[0]
+    e2e_s = time.perf_counter() - t0
+    eng.sync()
+
+    ctxs = [prompt_len + i + 1 for i in range(K)]
+    bytes_avg = sum(step_bytes(m, [c], m.top_k) for c in ctxs) / K
+    peaks, peak_kind = load_peaks()
+    achieved = bytes_avg / (ms_per_step * 1e-3) / 1e9
+    traffic = measured_traffic(w.name)
+    out = {
+        "metric": METRIC,
+        "value": round(world * K / (ms / 1e3), 2),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int4 weights x int16 activations (dp2a), fp32 accumulate" if m.wdtype == "int4"
+                 else f"{m.wdtype} weights, fp32 activations and accumulate",
+        "data": "synthetic: seeded N(0,0.02) weights, seeded uniform prompt tokens",
+        "config": {"workload": f"{w.name}: Flint-shaped MoE (49 layers, hidden 2048, 64 experts top-6, "
+                               f"dense layers 0-1), {m.wdtype} linear layers, {prompt_len}-token prompt, "
+                               f"greedy decode batch 1",
+                   "batch": 1, "context": [prompt_len + 1, prompt_len + K],
+                   "l2": "inputs larger than L2 (~1.2 GB of weights streamed per step); no flush",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(world * E / e2e_s, 2), "unit": "tok/s",
+                "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 4},
+        "gpu_launches": K,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "bytes_per_step": int(bytes_avg)},
+        "clocks": clk,
+        "setup_s": {"weights": round(gen_s, 1), "prefill": round(prefill_s, 3)},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(m, weights)
+    eng.close()
+    return out
+
+
+class TimedFetch:
+    """Oracle weight source over the seeded generator that keeps what it
+    produced and the time spent producing it (excluded from oracle timings).
+    The experts of a layer are drawn together in a thread pool."""
+
+    def __init__(self, m, threads: int):
+        from concurrent.futures import ThreadPoolExecutor
+        from synth import weights as SW
+        self.m, self.SW = m, SW
+        self.pool = ThreadPoolExecutor(threads)
+        self.cache = {}
+        self.seconds = 0.0
+
+    def __call__(self, name, layer, expert):
+        key = (name, layer, expert)
+        if key not in self.cache:
+            t0 = time.perf_counter()
+            m, SW = self.m, self.SW
+            if expert is not None:
+                futs = {e: self.pool.submit(SW.linear_np, m, name, layer, e) for e in range(m.n_experts)}
+                for e, f in futs.items():
+                    self.cache[(name, layer, e)] = (f.result(), m.wdtype)
+            elif name in ("embed", "attn_norm", "ffn_norm", "final_norm", "router"):
+                self.cache[key] = (SW.raw_np(m, name, layer), m.aux_dtype)
+            else:
+                shp = SW.tensor_shape(m, name)
+                step = max(1, shp[0] // 16)
+                parts = [self.pool.submit(SW.linear_np, m, name, layer, None, (r, min(shp[0], r + step)))
+                         for r in range(0, shp[0], step)]
+                res = [f.result() for f in parts]
+                if m.wdtype == "int4":
+                    val = (np.concatenate([a for a, _ in res]), np.concatenate([b for _, b in res]))
+                else:
+                    val = np.concatenate(res)
+                self.cache[key] = (val, m.wdtype)
+            self.seconds += time.perf_counter() - t0
+        return self.cache[key]
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle on a bounded sample of the same workload.  A step is a
+    fixed slice of consecutive layers of one batch-1 decode token (plus the
+    lm_head + argmax when the slice ends the token), sized so that all
+    warm-up and timed steps together cover a few tokens; tok/s counts a
+    step as (layers in slice) / (layers of the model) tokens."""
+    if rank != 0:
+        return None
+    import synth
+    from oracle import Oracle
+    from oracle import model as OM
+    from synth import prompts as SP
+    w = synth.CONFIGS[args.config]
+    m = w.model
+    threads = os.cpu_count() or 1
+    fetch = TimedFetch(m, threads)
+    orc = Oracle(m, fetch, cache_bytes=2 << 30)
+    prompt_len = 2
+    kv = orc.new_kv()
+    tok, _ = orc.prefill(kv, SP.prompt_tokens(m.seed, m.vocab, prompt_len))
+    L = m.n_layers
+    span = max(1, min(L, round(L * 6 / max(1, args.steps + args.warmup))))
+    state = {"x": None, "l": 0, "pos": prompt_len, "tok": tok}
+
+    def step():
+        for _ in range(span):
+            l = state["l"]
+            if l == 0:
+                state["x"] = orc.embed([state["tok"]])
+            tr = {"router_logits": [], "topk_ids": [], "topk_w": [], "topk_margin": []}
+            h, _ = orc._attn_block(l, state["x"], kv, state["pos"], True)
+            state["x"] = orc._ffn_block(l, h, tr)
+            state["l"] = l + 1
+            if state["l"] == L:
+                lg = OM.rmsnorm(state["x"], orc.w("final_norm"), m.rms_eps) @ orc.w("lm_head").T
+                state["tok"] = OM.argmax_lowest(lg[0])
+                state["pos"] += 1
+                state["l"] = 0
+
+    for _ in range(args.warmup):
+        step()
+    g0 = fetch.seconds
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0 - (fetch.seconds - g0)
+    toks = args.steps * span / L
+    v = toks / dt
+    sample = (f"{args.steps} steps of {span} layer(s) each = {toks:.2f} batch-1 decode tokens of the "
+              f"{w.name} model in float64 at context {prompt_len + 1}+ (the workload's context is "
+              f"{w.prompt_len}+); weight dequantisation included, weight generation excluded; "
+              f"BLAS single-threaded")
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic: seeded N(0,0.02) weights, seeded uniform prompt tokens",
+            "config": {"workload": w.name, "batch": 1},
+            "cpu_baseline": {"value": round(v, 5), "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 5), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out))
+        return
+    import torch
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    out = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

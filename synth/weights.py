@@ -261,3 +261,17 @@ def model_torch(m: ModelShape, device="cuda") -> dict:
             else:
                 out[(name, l)] = linear_torch(m, name, l, device)
     return out
+
+
+def linear_fast(m: ModelShape, name: str, layer: int = -1, expert=None):
+    """Same result as linear_np / raw_np (storage format, NumPy arrays), drawn
+    with PyTorch's multithreaded CPU kernels (bit-identical, faster)."""
+    import torch
+    if name in ("attn_norm", "ffn_norm", "final_norm", "embed", "router"):
+        t = raw_torch(m, name, layer, expert, "cpu")
+        return t.numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy().view(np.uint16)
+    t = raw_torch(m, name, layer, expert, "cpu")
+    if storage_dtype(m, name) == "int4":
+        p, s = quantize_int4_torch(t)
+        return p.numpy(), s.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy().view(np.uint16)
