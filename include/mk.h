@@ -157,8 +157,9 @@ MK_API int mk_kv_alloc(mk_ctx* ctx, int32_t n_pages);
 
 /* Prefill: run n (1..4096) prompt tokens of sequence seq_id at positions
  * start_pos .. start_pos+n-1 through the model, writing their K/V into
- * pages taken from the pool ("rec prefills in 4096-token chunks",
- * "rec Megakernel and Tempo9 Compared", §1 "Prefill").  start_pos must
+ * pages taken from the pool.  The chunk limit follows "rec Megakernel and
+ * Tempo9 Compared", §1 (Prefill), where the megakernel engine splits long
+ * prompts into pieces of 4096 tokens.  start_pos must
  * equal the sequence's current length (0 starts a new sequence).
  * tokens_dev: device int32[n].  out_token_dev: device int32[1] that receives
  * the greedy next token after the last position (may be NULL).
@@ -216,6 +217,42 @@ MK_API int mk_get_info(mk_ctx* ctx, mk_info* info);
 
 /* Release every resource of the context (waits for its device work). */
 MK_API int mk_destroy(mk_ctx* ctx);
+
+/* Decode step that allocates no device memory.  The paper has no counterpart:
+ * this entry point exists for callers that cannot call cudaMalloc — code
+ * running while a stream is being captured, hosts that hand the library a
+ * fixed memory budget carved by their own allocator, or real-time loops
+ * that must not take the implicit device synchronisation of an allocation.
+ * It launches the same kernel as mk_decode_step without a context: the
+ * per-layer pointer table, the RoPE table and the kernel's scratch live in a
+ * file-scope device array of 8 MiB that every GPU loading the library holds
+ * until the process exits.  Positions must be below 8192 (the size of that
+ * RoPE table); a model whose scratch does not fit in the array is rejected
+ * with MK_ERR_UNSUPPORTED.
+ * d, w: as for mk_create (weights borrowed for the duration of the call).
+ * kv_dev: caller-owned KV pool of n_pages pages in the layout of mk_kv_alloc.
+ * block_table_dev: caller-owned int32 [max_seqs][max_pages_per_seq]; entry
+ *   [slot][p / 128] must hold the page of every cached position p < position;
+ *   the call itself writes the entry of each row's new position.
+ * slots_host, positions_host, pages_host: host int32[n]: the block-table row
+ *   of each sequence (distinct), its position (= its current length) and the
+ *   pool page that holds that position.
+ * tokens_dev / out_tokens_dev: device int32[n] inputs / greedy next tokens.
+ * status_dev: optional device int32[1] that receives the kernel's error word
+ *   (0, MK_ERR_BARRIER_TIMEOUT or MK_ERR_DEVICE_INDEX) after the launch.
+ * The first call on a device resolves the array's address and uploads the
+ * RoPE table with a synchronous copy (again when rope_theta or head_dim
+ * changes); make that first call before any stream capture.  Every call
+ * shares the one array and it keeps the last call's contents (the call
+ * clears the counters that must start at zero): calls that overlap on the
+ * GPU, on any stream, race.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+MK_API int mk_decode_step_static(const mk_model_desc* d, const mk_weights* w, void* kv_dev,
+                                 int32_t n_pages, int32_t* block_table_dev,
+                                 int32_t max_pages_per_seq, const int32_t* slots_host,
+                                 const int32_t* positions_host, const int32_t* pages_host,
+                                 int32_t n, const int32_t* tokens_dev, int32_t* out_tokens_dev,
+                                 int32_t* status_dev, void* stream);
 
 /* Message of the calling thread's last failure ("" if none). */
 MK_API const char* mk_last_error(void);

@@ -239,6 +239,63 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
 
 }  // namespace
 
+namespace mk {
+
+int host_fail(int code, const char* msg) { return fail(code, msg); }
+void host_clear_error() { g_err.clear(); }
+
+size_t host_carve_scratch(const mk_model_desc& d, int grid, int max_units, char* base, Scratch* sc) {
+  return carve_scratch(d, grid, max_units, base, sc);
+}
+
+void host_attention_split(int n_kv_heads, int grid, const int32_t* pos, int n, int* chunk, int* units) {
+  long long total = 0;
+  for (int i = 0; i < n; ++i) total += pos[i] + 1;
+  long long ch = (n_kv_heads * total + grid - 1) / grid;
+  ch = std::max<long long>(16, (ch + 15) / 16 * 16);
+  long long u = 0;
+  for (int i = 0; i < n; ++i) u += n_kv_heads * ((pos[i] + 1 + ch - 1) / ch);
+  *chunk = (int)ch;
+  *units = (int)u;
+}
+
+int host_check_model(const mk_model_desc* d, const mk_weights* w, int* shape, LayerW* lw) {
+  if (int r = validate_desc(d, shape)) return r;
+  if (!w || !w->layers) return fail(MK_ERR_INVALID_ARG, "weights or weights->layers is NULL");
+  const bool int4 = d->wdtype == MK_INT4_G64;
+  if (int r = check_aux(w->embed, "embed", -1)) return r;
+  if (int r = check_aux(w->final_norm, "final_norm", -1)) return r;
+  if (int r = check_lin(w->lm_head, int4, "lm_head", -1)) return r;
+  for (int l = 0; l < d->n_layers; ++l) {
+    const mk_layer_weights& L = w->layers[l];
+    LayerW& o = lw[l];
+    std::memset(&o, 0, sizeof(o));
+    if (int r = check_aux(L.attn_norm, "attn_norm", l)) return r;
+    if (int r = check_aux(L.ffn_norm, "ffn_norm", l)) return r;
+    const mk_linear* lin[NLIN] = {&L.wq, &L.wk, &L.wv, &L.wo, &L.gate, &L.up, &L.down,
+                                  &L.exp_gate, &L.exp_up, &L.exp_down};
+    static const char* names[NLIN] = {"wq", "wk", "wv", "wo", "gate", "up", "down",
+                                      "exp_gate", "exp_up", "exp_down"};
+    const bool dense = l < d->n_dense;
+    for (int k = 0; k < NLIN; ++k) {
+      const bool used = k <= WO || (dense ? (k >= GATE && k <= DOWN) : k >= EGATE);
+      if (!used) continue;
+      if (int r = check_lin(*lin[k], int4, names[k], l)) return r;
+      o.w[k] = lin[k]->w;
+      o.s[k] = int4 ? lin[k]->scales : nullptr;
+    }
+    if (!dense) {
+      if (int r = check_aux(L.router, "router", l)) return r;
+      o.router = L.router;
+    }
+    o.attn_norm = L.attn_norm;
+    o.ffn_norm = L.ffn_norm;
+  }
+  return MK_OK;
+}
+
+}  // namespace mk
+
 extern "C" {
 
 MK_API const char* mk_last_error(void) { return g_err.c_str(); }

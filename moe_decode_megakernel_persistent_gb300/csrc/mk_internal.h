@@ -100,4 +100,13 @@ struct KernelInfo {
 // Returns the kernel for (shape, wdtype) or fn == nullptr if not compiled.
 KernelInfo get_kernel(int shape, int wdtype);
 
+// Host helpers of mk_host.cpp shared with the allocation-free entry point.
+// host_check_model: validates the description and weight pointers and fills
+// the per-layer pointer table (status code; message via mk_last_error).
+int host_check_model(const mk_model_desc* d, const mk_weights* w, int* shape, LayerW* layers);
+size_t host_carve_scratch(const mk_model_desc& d, int grid, int max_units, char* base, Scratch* sc);
+void host_attention_split(int n_kv_heads, int grid, const int32_t* pos, int n, int* chunk, int* units);
+int host_fail(int code, const char* msg);
+void host_clear_error();
+
 }  // namespace mk

@@ -1,0 +1,192 @@
+// mk_decode_step_static: the decode step for callers that cannot allocate
+// device memory.  It launches the same decode kernel as mk_decode_step, but
+// everything the library would otherwise cudaMalloc (the per-layer pointer
+// table, the RoPE table and the kernel's scratch: residual stream, attention
+// partials, router partials, expert activations, argmax candidates, barrier
+// counters and the error word) lives in one file-scope device array of
+// kStaticBytes bytes.  Every GPU that loads the library holds that array
+// until the process exits.  Weights, the KV cache and its block table,
+// tokens and outputs are the caller's memory.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "mk_internal.h"
+
+namespace mk {
+namespace {
+
+constexpr size_t kStaticBytes = size_t(8) << 20;  // 8 MiB per device
+constexpr int kStaticRopePositions = 8192;         // positions the RoPE table covers
+constexpr int kMaxDevices = 64;
+constexpr int kMaxStaticLayers = 128;
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
+
+// Set-up state per device: the array's device address and which RoPE table
+// (theta, head_dim) it currently holds.
+struct DeviceState {
+  bool ready = false;
+  char* base = nullptr;
+  float rope_theta = 0.f;
+  int head_dim = 0;
+};
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+size_t rope_bytes(int head_dim) {
+  return sizeof(float2) * (size_t)kStaticRopePositions * (head_dim / 2);
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Once per device (with that device current): resolve the array's device
+// address; (re)build the RoPE table when theta or head_dim changes.  The
+// table upload is a synchronous copy, so the first call on a device, or the
+// first after a theta / head_dim change, must not run under stream capture.
+int setup(int dev, const mk_model_desc& d, char** base) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess)
+      return host_fail(MK_ERR_CUDA, (std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e)).c_str());
+    s.base = static_cast<char*>(ptr);
+    s.ready = true;
+  }
+  if (s.rope_theta != d.rope_theta || s.head_dim != d.head_dim) {
+    const int half = d.head_dim / 2;
+    std::vector<float2> rope((size_t)kStaticRopePositions * half);
+    for (int p = 0; p < kStaticRopePositions; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double ang = (double)p * std::pow((double)d.rope_theta, -2.0 * i / d.head_dim);
+        rope[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    cudaError_t e = cudaMemcpy(s.base, rope.data(), rope_bytes(d.head_dim), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess)
+      return host_fail(MK_ERR_CUDA, (std::string("RoPE table upload: ") + cudaGetErrorString(e)).c_str());
+    s.rope_theta = d.rope_theta;
+    s.head_dim = d.head_dim;
+  }
+  *base = s.base;
+  return MK_OK;
+}
+
+}  // namespace
+}  // namespace mk
+
+using namespace mk;
+
+extern "C" MK_API int mk_decode_step_static(
+    const mk_model_desc* d, const mk_weights* w, void* kv_dev, int32_t n_pages,
+    int32_t* block_table_dev, int32_t max_pages_per_seq, const int32_t* slots_host,
+    const int32_t* positions_host, const int32_t* pages_host, int32_t n,
+    const int32_t* tokens_dev, int32_t* out_tokens_dev, int32_t* status_dev, void* stream) {
+  host_clear_error();
+  int shape = -1;
+  if (!d || !w) return host_fail(MK_ERR_INVALID_ARG, "model description or weights is NULL");
+  if (d->n_layers > kMaxStaticLayers)
+    return host_fail(MK_ERR_INVALID_ARG, "more layers than the static layer table holds (128)");
+  LayerW layers[kMaxStaticLayers];
+  if (int r = host_check_model(d, w, &shape, layers)) return r;
+  if (!kv_dev || !block_table_dev || !slots_host || !positions_host || !pages_host || !tokens_dev ||
+      !out_tokens_dev)
+    return host_fail(MK_ERR_INVALID_ARG, "NULL argument");
+  if (n < 1 || n > d->max_batch) return host_fail(MK_ERR_INVALID_ARG, "n must be in [1, max_batch]");
+  if (n_pages < 1 || max_pages_per_seq < 1)
+    return host_fail(MK_ERR_INVALID_ARG, "n_pages and max_pages_per_seq must be >= 1");
+  for (int i = 0; i < n; ++i) {
+    if (slots_host[i] < 0 || slots_host[i] >= d->max_seqs)
+      return host_fail(MK_ERR_INVALID_ARG, "slot out of range [0, max_seqs)");
+    for (int j = 0; j < i; ++j)
+      if (slots_host[j] == slots_host[i]) return host_fail(MK_ERR_INVALID_ARG, "slots must be distinct");
+    const int p = positions_host[i];
+    if (p < 0 || p >= d->max_ctx || p >= kStaticRopePositions)
+      return host_fail(MK_ERR_INVALID_ARG,
+                       "position out of range (the static RoPE table covers positions < 8192)");
+    if (p / kPageTokens >= max_pages_per_seq)
+      return host_fail(MK_ERR_INVALID_ARG, "position beyond max_pages_per_seq pages");
+    if (pages_host[i] < 0 || pages_host[i] >= n_pages)
+      return host_fail(MK_ERR_INVALID_ARG, "page out of range [0, n_pages)");
+  }
+  const KernelInfo kern = get_kernel(shape, d->wdtype);
+  if (!kern.fn) return host_fail(MK_ERR_UNSUPPORTED, "no kernel for this shape and dtype");
+
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return host_fail(MK_ERR_CUDA, cudaGetErrorString(e));
+  if (dev >= kMaxDevices) return host_fail(MK_ERR_UNSUPPORTED, "device ordinal >= 64");
+  if ((d->hidden + sms - 1) / sms > kMaxRowsPerBlock)
+    return host_fail(MK_ERR_UNSUPPORTED, "too few SMs for the compiled per-block row budget");
+
+  // layout of the static array: RoPE table | layer table | kernel scratch
+  const int grid = sms;
+  const int max_units = grid + d->n_kv_heads * kMaxBatch;
+  const size_t off_layers = align256(rope_bytes(d->head_dim));
+  const size_t off_scratch = align256(off_layers + sizeof(LayerW) * d->n_layers);
+  const size_t need = off_scratch + host_carve_scratch(*d, grid, max_units, nullptr, nullptr);
+  if (need > kStaticBytes)
+    return host_fail(MK_ERR_UNSUPPORTED,
+                     ("model needs " + std::to_string(need) + " bytes of static scratch; the array holds " +
+                      std::to_string(kStaticBytes)).c_str());
+
+  char* base = nullptr;
+  if (int r = setup(dev, *d, &base)) return r;
+  e = cudaFuncSetAttribute(kern.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kern.smem_bytes);
+  if (e != cudaSuccess) return host_fail(MK_ERR_CUDA, cudaGetErrorString(e));
+
+  StepArgs a;
+  std::memset(&a, 0, sizeof(a));
+  host_carve_scratch(*d, grid, max_units, base + off_scratch, &a.sc);
+  host_attention_split(d->n_kv_heads, grid, positions_host, n, &a.chunk, &a.n_units);
+  if (a.n_units > max_units) return host_fail(MK_ERR_INVALID_ARG, "attention split exceeds its buffer");
+  for (int i = 0; i < n; ++i) {
+    a.slot[i] = slots_host[i];
+    a.pos[i] = positions_host[i];
+    a.cur_page[i] = pages_host[i];
+    a.upd[a.n_upd++] = PageUpd{slots_host[i], positions_host[i] / kPageTokens, pages_host[i]};
+  }
+  a.layers = reinterpret_cast<const LayerW*>(base + off_layers);
+  a.embed = w->embed;
+  a.final_norm = w->final_norm;
+  a.lm_head = w->lm_head.w;
+  a.lm_head_s = d->wdtype == MK_INT4_G64 ? w->lm_head.scales : nullptr;
+  a.rope = reinterpret_cast<const float2*>(base);
+  a.kv = static_cast<uint16_t*>(kv_dev);
+  a.block_table = block_table_dev;
+  a.tokens = tokens_dev;
+  a.out_tokens = out_tokens_dev;
+  a.n_pages = n_pages;
+  a.max_pages_per_seq = max_pages_per_seq;
+  a.n = n;
+  a.n_layers = d->n_layers;
+  a.n_dense = d->n_dense;
+  a.vocab = d->vocab;
+  a.eps = d->rms_eps;
+  a.out_first = 0;
+  a.max_units = max_units;
+  a.spin_limit_ns = 1000000000ull;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: counters, merge counts and
+  // the error word must start at zero
+  e = cudaMemsetAsync(a.sc.merge_cnt, 0, sizeof(int32_t) * kMaxBatch * d->n_kv_heads, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(a.sc.sync, 0, sizeof(uint32_t) * 128, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(a.sc.err, 0, sizeof(int32_t) * 4, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(base + off_layers, layers, sizeof(LayerW) * d->n_layers, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return host_fail(MK_ERR_CUDA, cudaGetErrorString(e));
+  void* args[] = {&a};
+  e = cudaLaunchCooperativeKernel(kern.fn, dim3(grid), dim3(kThreads), args, (size_t)kern.smem_bytes, st);
+  if (e != cudaSuccess)
+    return host_fail(MK_ERR_CUDA, (std::string("cudaLaunchCooperativeKernel: ") + cudaGetErrorString(e)).c_str());
+  if (status_dev) {
+    e = cudaMemcpyAsync(status_dev, a.sc.err, sizeof(int32_t), cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return host_fail(MK_ERR_CUDA, cudaGetErrorString(e));
+  }
+  return MK_OK;
+}
