@@ -202,6 +202,13 @@ MK_API int mk_sync(mk_ctx* ctx, void* stream);
  * Errors: INVALID_ARG. */
 #define MK_DBG_TRACE 1u
 #define MK_DBG_SKIP_ARRIVAL 2u
+#define MK_DBG_TIMING 4u   /* trace_dev receives uint64 %globaltimer stamps (ns) of
+                              block 0 instead of the trace: [0] kernel start; for layer l
+                              and phase p (0 qkv, 1 attention, 2 o_proj, 3 routing and
+                              gate/up, 4 down) [1 + 16*l + 3*p + k] with k = 0 staging
+                              done, 1 phase work done, 2 grid barrier released; then
+                              [1 + 16*n_layers] lm_head done.  Size: 8 * (16 * n_layers
+                              + 2) bytes.  Not combinable with MK_DBG_TRACE. */
 MK_API int mk_set_debug(mk_ctx* ctx, uint32_t flags, uint32_t arg, void* trace_dev,
                         size_t trace_bytes, uint32_t spin_limit_us);
 

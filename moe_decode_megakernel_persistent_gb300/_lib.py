@@ -24,6 +24,7 @@ MK_F32, MK_BF16, MK_INT4_G64 = 0, 1, 2
 WDTYPES = {"f32": MK_F32, "bf16": MK_BF16, "int4": MK_INT4_G64}
 MK_DBG_TRACE = 1
 MK_DBG_SKIP_ARRIVAL = 2
+MK_DBG_TIMING = 4
 
 
 class MKError(RuntimeError):

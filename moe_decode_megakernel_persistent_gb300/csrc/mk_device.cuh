@@ -67,6 +67,17 @@ __device__ __forceinline__ float ld_aux(const void* p, int i) {
   else return bf16_to_f(__ldg(reinterpret_cast<const unsigned short*>(p) + i));
 }
 
+// Four consecutive aux values (elements 4*i4 .. 4*i4+3) as float4.
+template <int AUX>
+__device__ __forceinline__ float4 ld_aux4(const void* p, size_t i4) {
+  if constexpr (AUX == WF32) return __ldg(reinterpret_cast<const float4*>(p) + i4);
+  else {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p) + i4);
+    return make_float4(bf16_to_f(u.x & 0xffff), bf16_to_f(u.x >> 16), bf16_to_f(u.y & 0xffff),
+                       bf16_to_f(u.y >> 16));
+  }
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -262,121 +273,346 @@ struct Gemv {
     return acc;
   }
 
-  // Stage y[k] = f(k) (k < K) into shared memory at `dst` (one warp).
-  template <class F>
-  __device__ static __forceinline__ void stage(uint8_t* dst, int lane, F f) {
-    for (int c = lane; c < NCH; c += 32) {
-      float y[VPC];
+  // Dot products of two rows with one staged activation, the activation read
+  // chunk by chunk from shared memory (fewer live registers than load_act).
+  __device__ static __forceinline__ void dot2_smem(const Row& r0, const Row& r1, const uint8_t* base,
+                                                   int lane, float& v0, float& v1) {
+    float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-      for (int i = 0; i < VPC; ++i) y[i] = f(c * VPC + i);
-      if constexpr (WDT == WINT4) {
-        float amax = 0.f;
+    for (int j = 0; j < CPL; ++j) {
+      const int c = lane + 32 * j;
+      if (NCH % 32 == 0 || c < NCH) {
+        if constexpr (WDT == WINT4) {
+          uint4 p[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(y[i]));
-        const float inv = amax > 0.f ? 32767.f / amax : 0.f;
-        int sum = 0;
-        // dp2a operand order per 8-value word t: (0,2) (4,6) (1,3) (5,7)
+          for (int t = 0; t < 4; ++t) p[t] = *reinterpret_cast<const uint4*>(base + (t * NCH + c) * 16);
+          const int2 m = *reinterpret_cast<const int2*>(base + NCH * SUBS * 16 + c * 8);
+          const uint32_t av[16] = {p[0].x, p[0].y, p[0].z, p[0].w, p[1].x, p[1].y, p[1].z, p[1].w,
+                                   p[2].x, p[2].y, p[2].z, p[2].w, p[3].x, p[3].y, p[3].z, p[3].w};
+          const uint32_t w0[4] = {r0.w[j].x, r0.w[j].y, r0.w[j].z, r0.w[j].w};
+          const uint32_t w1[4] = {r1.w[j].x, r1.w[j].y, r1.w[j].z, r1.w[j].w};
+          int i0 = 0, i1 = 0;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          int v[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            v[i] = __float2int_rn(y[8 * t + i] * inv);
-            sum += v[i];
+          for (int t = 0; t < 4; ++t) {
+            const uint32_t x0 = w0[t] ^ 0x88888888u, x1 = w1[t] ^ 0x88888888u;
+            const uint32_t be0 = x0 & 0x0F0F0F0Fu, bo0 = (x0 >> 4) & 0x0F0F0F0Fu;
+            const uint32_t be1 = x1 & 0x0F0F0F0Fu, bo1 = (x1 >> 4) & 0x0F0F0F0Fu;
+            asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(i0) : "r"(av[4 * t + 0]), "r"(be0));
+            asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(i0) : "r"(av[4 * t + 1]), "r"(be0));
+            asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(i0) : "r"(av[4 * t + 2]), "r"(bo0));
+            asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(i0) : "r"(av[4 * t + 3]), "r"(bo0));
+            asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(i1) : "r"(av[4 * t + 0]), "r"(be1));
+            asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(i1) : "r"(av[4 * t + 1]), "r"(be1));
+            asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(i1) : "r"(av[4 * t + 2]), "r"(bo1));
+            asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(i1) : "r"(av[4 * t + 3]), "r"(bo1));
           }
-          *reinterpret_cast<uint4*>(dst + (t * NCH + c) * 16) =
-              make_uint4((uint32_t)(v[0] & 0xFFFF) | ((uint32_t)v[2] << 16),
-                         (uint32_t)(v[4] & 0xFFFF) | ((uint32_t)v[6] << 16),
-                         (uint32_t)(v[1] & 0xFFFF) | ((uint32_t)v[3] << 16),
-                         (uint32_t)(v[5] & 0xFFFF) | ((uint32_t)v[7] << 16));
-        }
-        *reinterpret_cast<int2*>(dst + NCH * SUBS * 16 + c * 8) =
-            make_int2(__float_as_int(amax / 32767.f), 8 * sum);
-      } else {
+          const float sa = __int_as_float(m.x);
+          acc0 = fmaf((float)(i0 - m.y), sa * r0.s[j], acc0);
+          acc1 = fmaf((float)(i1 - m.y), sa * r1.s[j], acc1);
+        } else {
 #pragma unroll
-        for (int t = 0; t < SUBS; ++t)
-          *reinterpret_cast<float4*>(dst + (t * NCH + c) * 16) =
-              make_float4(y[4 * t], y[4 * t + 1], y[4 * t + 2], y[4 * t + 3]);
+          for (int t = 0; t < SUBS; ++t) {
+            const uint4 ap = *reinterpret_cast<const uint4*>(base + (t * NCH + c) * 16);
+            const float av[4] = {__uint_as_float(ap.x), __uint_as_float(ap.y), __uint_as_float(ap.z),
+                                 __uint_as_float(ap.w)};
+            if constexpr (WDT == WBF16) {
+              const uint32_t a0 = t == 0 ? r0.w[j].x : r0.w[j].z, b0 = t == 0 ? r0.w[j].y : r0.w[j].w;
+              const uint32_t a1 = t == 0 ? r1.w[j].x : r1.w[j].z, b1 = t == 0 ? r1.w[j].y : r1.w[j].w;
+              acc0 = fmaf(__uint_as_float(a0 << 16), av[0], acc0);
+              acc0 = fmaf(__uint_as_float(a0 & 0xFFFF0000u), av[1], acc0);
+              acc0 = fmaf(__uint_as_float(b0 << 16), av[2], acc0);
+              acc0 = fmaf(__uint_as_float(b0 & 0xFFFF0000u), av[3], acc0);
+              acc1 = fmaf(__uint_as_float(a1 << 16), av[0], acc1);
+              acc1 = fmaf(__uint_as_float(a1 & 0xFFFF0000u), av[1], acc1);
+              acc1 = fmaf(__uint_as_float(b1 << 16), av[2], acc1);
+              acc1 = fmaf(__uint_as_float(b1 & 0xFFFF0000u), av[3], acc1);
+            } else {
+              acc0 = fmaf(__uint_as_float(r0.w[j].x), av[0], acc0);
+              acc0 = fmaf(__uint_as_float(r0.w[j].y), av[1], acc0);
+              acc0 = fmaf(__uint_as_float(r0.w[j].z), av[2], acc0);
+              acc0 = fmaf(__uint_as_float(r0.w[j].w), av[3], acc0);
+              acc1 = fmaf(__uint_as_float(r1.w[j].x), av[0], acc1);
+              acc1 = fmaf(__uint_as_float(r1.w[j].y), av[1], acc1);
+              acc1 = fmaf(__uint_as_float(r1.w[j].z), av[2], acc1);
+              acc1 = fmaf(__uint_as_float(r1.w[j].w), av[3], acc1);
+            }
+          }
+        }
       }
     }
+    v0 = warp_sum(acc0);
+    v1 = warp_sum(acc1);
+  }
+
+  // Write one chunk of activation values into its staged form at `dst`.
+  __device__ static __forceinline__ void store_chunk(uint8_t* dst, int c, const float* y) {
+    if constexpr (WDT == WINT4) {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(y[i]));
+      const float inv = amax > 0.f ? 32767.f / amax : 0.f;
+      int sum = 0;
+      // dp2a operand order per 8-value word t: (0,2) (4,6) (1,3) (5,7)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        int v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[i] = __float2int_rn(y[8 * t + i] * inv);
+          sum += v[i];
+        }
+        *reinterpret_cast<uint4*>(dst + (t * NCH + c) * 16) =
+            make_uint4((uint32_t)(v[0] & 0xFFFF) | ((uint32_t)v[2] << 16),
+                       (uint32_t)(v[4] & 0xFFFF) | ((uint32_t)v[6] << 16),
+                       (uint32_t)(v[1] & 0xFFFF) | ((uint32_t)v[3] << 16),
+                       (uint32_t)(v[5] & 0xFFFF) | ((uint32_t)v[7] << 16));
+      }
+      *reinterpret_cast<int2*>(dst + NCH * SUBS * 16 + c * 8) =
+          make_int2(__float_as_int(amax / 32767.f), 8 * sum);
+    } else {
+#pragma unroll
+      for (int t = 0; t < SUBS; ++t)
+        *reinterpret_cast<float4*>(dst + (t * NCH + c) * 16) =
+            make_float4(y[4 * t], y[4 * t + 1], y[4 * t + 2], y[4 * t + 3]);
+    }
+  }
+
+  // Stage y[k] = f(k) (k < K) into shared memory at `dst` (one warp).  All
+  // of a lane's loads are issued before any is consumed.
+  template <class F>
+  __device__ static __forceinline__ void stage(uint8_t* dst, int lane, F f) {
+    float y[CPL][VPC];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      const int c = lane + 32 * j;
+      if (NCH % 32 == 0 || c < NCH) {
+#pragma unroll
+        for (int i = 0; i < VPC; ++i) y[j][i] = f(c * VPC + i);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      const int c = lane + 32 * j;
+      if (NCH % 32 == 0 || c < NCH) store_chunk(dst, c, y[j]);
+    }
+  }
+
+  // Stage the RMS-normalised vector y[k] = x[k] / sqrt(mean(x^2) + eps) * w[k]
+  // (one warp): x is read once into registers, its sum of squares reduced
+  // across the warp, then scaled, weighted and stored.
+  template <class LX, class LW>
+  __device__ static __forceinline__ float stage_rms(uint8_t* dst, int lane, float eps, LX x, LW w) {
+    float y[CPL][VPC];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      const int c = lane + 32 * j;
+      if (NCH % 32 == 0 || c < NCH) {
+#pragma unroll
+        for (int i = 0; i < VPC; ++i) {
+          y[j][i] = x(c * VPC + i);
+          ss = fmaf(y[j][i], y[j][i], ss);
+        }
+      }
+    }
+    const float r = rsqrtf(warp_sum(ss) / K + eps);
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      const int c = lane + 32 * j;
+      if (NCH % 32 == 0 || c < NCH) {
+#pragma unroll
+        for (int i = 0; i < VPC; ++i) y[j][i] = y[j][i] * r * w(c * VPC + i);
+        store_chunk(dst, c, y[j]);
+      }
+    }
+    return r;
   }
 };
 
-// Sum of squares of a K-vector from a value function (one warp, all lanes get it).
-template <int K, class F>
-__device__ __forceinline__ float warp_sumsq(int lane, F f) {
-  float s = 0.f;
-  for (int k = lane; k < K; k += 32) {
-    const float v = f(k);
-    s = fmaf(v, v, s);
+// Block-cooperative staging of `rows` activation vectors of K floats into the
+// staged form of Gemv<WDT, K> (vector r at dst + r * ACT_BYTES).  Thread t
+// loads float4 number t (coalesced: the block reads each vector as one
+// contiguous stream), optionally RMS-normalises the row (block reduction in a
+// fixed order, so every block gets the same scale) and multiplies by a
+// weight, then writes its part of the staged chunk; for int4 the 8 lanes
+// holding one 32-value chunk agree on its scale with shuffles.
+//   LD(row, f4) -> float4 values 4*f4 .. 4*f4+3 of vector `row`
+//   WT(f4)      -> float4 weights (only with norm)
+//   red         -> shared scratch of kWarps * 4 floats
+//   rscale      -> if non-null, receives each row's RMS scale (shared memory)
+template <int WDT, int K, class LD, class WT>
+__device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, bool norm, float eps, WT wt,
+                                            float* red, float* rscale) {
+  using Gv = Gemv<WDT, K>;
+  constexpr int NF4 = K / 4;
+  static_assert(K % 32 == 0, "vectors are whole chunks");
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  constexpr int RG = 4;                          // rows per pass
+  constexpr int PER = (RG * NF4 + kThreads - 1) / kThreads;
+  for (int r0 = 0; r0 < rows; r0 += RG) {
+    const int nrg = min(RG, rows - r0);
+    float4 v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int it = tid + i * kThreads;
+      if (it < nrg * NF4) v[i] = ld(r0 + it / NF4, it % NF4);
+    }
+    float rs[RG] = {1.f, 1.f, 1.f, 1.f};
+    if (norm) {
+      float ss[RG] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int it = tid + i * kThreads;
+        if (it < nrg * NF4) {
+          const float q = v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+#pragma unroll
+          for (int g = 0; g < RG; ++g) ss[g] += (it / NF4 == g) ? q : 0.f;
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < RG; ++g) {
+        ss[g] = warp_sum(ss[g]);
+        if (lane == 0) red[wid * RG + g] = ss[g];
+      }
+      __syncthreads();
+#pragma unroll
+      for (int g = 0; g < RG; ++g) {
+        float t = 0.f;
+        for (int w = 0; w < kWarps; ++w) t += red[w * RG + g];
+        rs[g] = rsqrtf(t / K + eps);
+      }
+      if (rscale && tid < nrg) rscale[r0 + tid] = rs[tid];
+      __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int it = tid + i * kThreads;
+      // int4 chunks span 8 consecutive lanes: keep the whole warp in the shuffles
+      const bool live = it < nrg * NF4;
+      if constexpr (WDT != WINT4) {
+        if (!live) continue;
+      } else {
+        if (__all_sync(0xffffffffu, !live)) continue;
+      }
+      const int row = live ? it / NF4 : 0, f4 = live ? it % NF4 : 0;
+      float4 y = v[i];
+      if (norm && live) {
+        const float4 w = wt(f4);
+        float r = rs[0];
+#pragma unroll
+        for (int g = 1; g < RG; ++g) r = row == g ? rs[g] : r;
+        y = make_float4(y.x * r * w.x, y.y * r * w.y, y.z * r * w.z, y.w * r * w.w);
+      }
+      uint8_t* base = dst + (r0 + row) * Gv::ACT_BYTES;
+      if constexpr (WDT == WINT4) {
+        // chunk c = f4 / 8 (32 values) lives in lanes 8j .. 8j+7
+        float amax = live ? fmaxf(fmaxf(fabsf(y.x), fabsf(y.y)), fmaxf(fabsf(y.z), fabsf(y.w))) : 0.f;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float inv = amax > 0.f ? 32767.f / amax : 0.f;
+        const int q0 = __float2int_rn(y.x * inv), q1 = __float2int_rn(y.y * inv);
+        const int q2 = __float2int_rn(y.z * inv), q3 = __float2int_rn(y.w * inv);
+        int sum = q0 + q1 + q2 + q3;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        // word group t = (f4 % 8) / 2 holds values 8t .. 8t+7 of the chunk:
+        // dp2a operand order (0,2) (4,6) (1,3) (5,7); the even lane of the
+        // pair holds values 0-3, the odd lane 4-7
+        const uint32_t pa = (uint32_t)(q0 & 0xFFFF) | ((uint32_t)q2 << 16);
+        const uint32_t pb = (uint32_t)(q1 & 0xFFFF) | ((uint32_t)q3 << 16);
+        const uint32_t oa = __shfl_xor_sync(0xffffffffu, pa, 1);
+        const uint32_t ob = __shfl_xor_sync(0xffffffffu, pb, 1);
+        const int c = f4 >> 3, t = (f4 & 7) >> 1;
+        if (live && (f4 & 1) == 0) {
+          *reinterpret_cast<uint4*>(base + (t * Gv::NCH + c) * 16) = make_uint4(pa, oa, pb, ob);
+          if (t == 0)
+            *reinterpret_cast<int2*>(base + Gv::NCH * Gv::SUBS * 16 + c * 8) =
+                make_int2(__float_as_int(amax / 32767.f), 8 * sum);
+        }
+      } else {
+        // chunk c holds VPC values = VPC/4 float4; sub t of chunk c at (t*NCH + c)*16
+        const int c = f4 / (Gv::VPC / 4), t = f4 % (Gv::VPC / 4);
+        *reinterpret_cast<float4*>(base + (t * Gv::NCH + c) * 16) = y;
+      }
+    }
   }
-  return warp_sum(s);
 }
 
 // Block-level task runner.  Tasks t = warp, warp + 16, ... ; each task has RP
 // weight rows and a list of staged activations; the warp loads each row once
-// and forms its dot product with every activation of the task.
-//   T::row(t, r, &w, &s)       row pointers of row r of task t
-//   T::acts(t, &list, &start)  -> count; activation i is list ? list[start+i] : start+i
-//   T::out(t, ai, i, v[RP])    result for activation ai (i-th of the task), all lanes
+// and forms its dot product with every activation of the task.  A task
+// object provides (all inlined, results returned by value):
+//   RowRef row(t, r)        row pointers of row r of task t
+//   ActRange acts(t)        activations: i-th is list ? list[start+i] : start+i
+//   void out(t, ai, i, v0, v1)  results for activation ai (i-th of the task), all lanes
+struct RowRef {
+  const uint8_t* w;
+  const uint16_t* s;
+};
+struct ActRange {
+  const uint8_t* list;
+  int start, count;
+};
+
 template <int WDT, int K, int RP, class T>
-__device__ __forceinline__ void run_tasks(int ntasks, const uint8_t* act_base, T& task) {
+__device__ __forceinline__ void run_tasks(int ntasks, const uint8_t* act_base, const T& task) {
   using Gv = Gemv<WDT, K>;
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   typename Gv::Act a;
   int loaded = -1;
+  auto prefetch_rows_l2 = [&](int tf) {
+#pragma unroll
+    for (int r = 0; r < RP; ++r) {
+      const RowRef rr = task.row(tf, r);
+#pragma unroll
+      for (int j = 0; j < Gv::CPL; ++j) {
+        const int c = lane + 32 * j;
+        if (Gv::NCH % 32 == 0 || c < Gv::NCH) asm volatile("prefetch.global.L2 [%0];" ::"l"(rr.w + 16 * c));
+      }
+    }
+  };
   if constexpr (Gv::PIPE && RP == 1) {
-    typename Gv::Row cur[RP], nxt[RP];
+    typename Gv::Row cur, nxt;
     int t = wid;
     if (t < ntasks) {
-#pragma unroll
-      for (int r = 0; r < RP; ++r) {
-        const uint8_t* w; const uint16_t* s;
-        task.row(t, r, &w, &s);
-        Gv::load_row(cur[r], w, s, lane);
-      }
+      const RowRef rr = task.row(t, 0);
+      Gv::load_row(cur, rr.w, rr.s, lane);
     }
     for (; t < ntasks; t += kWarps) {
       const int tn = t + kWarps;
       if (tn < ntasks) {
-#pragma unroll
-        for (int r = 0; r < RP; ++r) {
-          const uint8_t* w; const uint16_t* s;
-          task.row(tn, r, &w, &s);
-          Gv::load_row(nxt[r], w, s, lane);
-        }
+        const RowRef rr = task.row(tn, 0);
+        Gv::load_row(nxt, rr.w, rr.s, lane);
       }
-      const uint8_t* list; int start;
-      const int cnt = task.acts(t, &list, &start);
-      for (int i = 0; i < cnt; ++i) {
-        const int ai = list ? list[start + i] : start + i;
+      if (t + 4 * kWarps < ntasks) prefetch_rows_l2(t + 4 * kWarps);  // keep HBM busy further ahead
+      const ActRange ar = task.acts(t);
+      for (int i = 0; i < ar.count; ++i) {
+        const int ai = ar.list ? ar.list[ar.start + i] : ar.start + i;
         if (ai != loaded) { Gv::load_act(a, act_base + ai * Gv::ACT_BYTES, lane); loaded = ai; }
-        float v[RP];
-#pragma unroll
-        for (int r = 0; r < RP; ++r) v[r] = warp_sum(Gv::dot(cur[r], a, lane));
-        task.out(t, ai, i, v);
+        const float v0 = warp_sum(Gv::dot(cur, a, lane));
+        task.out(t, ai, i, v0, 0.f);
       }
-#pragma unroll
-      for (int r = 0; r < RP; ++r) cur[r] = nxt[r];
+      cur = nxt;
     }
   } else {
-    typename Gv::Row row;
+    // activations read from shared memory per chunk: no activation registers
+    // live across the task loop
+    typename Gv::Row row[2];
     for (int t = wid; t < ntasks; t += kWarps) {
-      const uint8_t* list; int start;
-      const int cnt = task.acts(t, &list, &start);
-      for (int i = 0; i < cnt; ++i) {
-        const int ai = list ? list[start + i] : start + i;
-        if (ai != loaded) { Gv::load_act(a, act_base + ai * Gv::ACT_BYTES, lane); loaded = ai; }
-        float v[RP];
+      if (t + kWarps < ntasks) prefetch_rows_l2(t + kWarps);  // warm L2 for this warp's next task
 #pragma unroll
-        for (int r = 0; r < RP; ++r) {
-          const uint8_t* w; const uint16_t* s;
-          task.row(t, r, &w, &s);
-          Gv::load_row(row, w, s, lane);
-          v[r] = warp_sum(Gv::dot(row, a, lane));
-        }
-        task.out(t, ai, i, v);
+      for (int r = 0; r < RP; ++r) {
+        const RowRef rr = task.row(t, r);
+        Gv::load_row(row[r], rr.w, rr.s, lane);
+      }
+      if (RP == 1) row[1] = row[0];
+      const ActRange ar = task.acts(t);
+      for (int i = 0; i < ar.count; ++i) {
+        const int ai = ar.list ? ar.list[ar.start + i] : ar.start + i;
+        float v0, v1;
+        Gv::dot2_smem(row[0], row[1], act_base + ai * Gv::ACT_BYTES, lane, v0, v1);
+        task.out(t, ai, i, v0, v1);
       }
     }
   }

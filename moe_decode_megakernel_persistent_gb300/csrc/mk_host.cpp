@@ -129,7 +129,7 @@ size_t carve_scratch(const mk_model_desc& d, int grid, int max_units, char* base
   s.h = (float*)take(sizeof(float) * kMaxBatch * H);
   s.q = (float*)take(sizeof(float) * kMaxBatch * QD);
   s.attn = (float*)take(sizeof(float) * kMaxBatch * QD);
-  s.part = (float*)take(sizeof(float) * (size_t)max_units * GQA * (d.head_dim + 2));
+  s.part = (float*)take(sizeof(float) * (size_t)max_units * GQA * (d.head_dim + 4));
   s.rpart = (float*)take(sizeof(float) * (size_t)grid * kMaxBatch * d.n_experts);
   s.rlogit = (float*)take(sizeof(float) * kMaxBatch * d.n_experts);
   s.act = (float*)take(sizeof(float) * kMaxBatch * d.top_k * d.expert_ffn);
@@ -163,6 +163,8 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
   if (!c->kv_dev) return fail(MK_ERR_STATE, "mk_kv_alloc has not been called");
   if ((c->dbg_flags & MK_DBG_TRACE) && c->trace_bytes < mk_trace_bytes(&c->d, n))
     return fail(MK_ERR_INVALID_ARG, "trace buffer is smaller than mk_trace_bytes(rows)");
+  if ((c->dbg_flags & MK_DBG_TIMING) && c->trace_bytes < sizeof(uint64_t) * (16 * (size_t)c->d.n_layers + 2))
+    return fail(MK_ERR_INVALID_ARG, "timing buffer is smaller than 8 * (16 * n_layers + 2) bytes");
   StepArgs a;
   std::memset(&a, 0, sizeof(a));
   std::vector<std::pair<int, int32_t>> taken;  // (slot, page) handed out by this call
@@ -211,6 +213,7 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
   a.tokens = tokens_dev;
   a.out_tokens = out_dev;
   a.trace = (c->dbg_flags & MK_DBG_TRACE) ? c->trace : nullptr;
+  a.timing = (c->dbg_flags & MK_DBG_TIMING) ? reinterpret_cast<uint64_t*>(c->trace) : nullptr;
   a.n_pages = c->n_pages;
   a.max_pages_per_seq = c->max_pages_per_seq;
   a.n = n;
@@ -562,8 +565,10 @@ MK_API int mk_set_debug(mk_ctx* c, uint32_t flags, uint32_t arg, void* trace_dev
                         uint32_t spin_limit_us) {
   g_err.clear();
   if (!c) return fail(MK_ERR_INVALID_ARG, "ctx is NULL");
-  if ((flags & MK_DBG_TRACE) && (!trace_dev || trace_bytes == 0))
-    return fail(MK_ERR_INVALID_ARG, "MK_DBG_TRACE needs a trace buffer");
+  if ((flags & (MK_DBG_TRACE | MK_DBG_TIMING)) && (!trace_dev || trace_bytes == 0))
+    return fail(MK_ERR_INVALID_ARG, "MK_DBG_TRACE / MK_DBG_TIMING need a buffer");
+  if ((flags & MK_DBG_TRACE) && (flags & MK_DBG_TIMING))
+    return fail(MK_ERR_INVALID_ARG, "MK_DBG_TRACE and MK_DBG_TIMING share the buffer: pick one");
   if ((flags & MK_DBG_SKIP_ARRIVAL) && (int)(arg & 0xffffu) >= c->grid)
     return fail(MK_ERR_INVALID_ARG, "MK_DBG_SKIP_ARRIVAL block index out of range");
   c->dbg_flags = flags;

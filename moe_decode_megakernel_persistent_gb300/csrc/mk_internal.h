@@ -65,6 +65,7 @@ struct StepArgs {
   const int32_t* tokens;     // [n] (device)
   int32_t* out_tokens;       // written for rows >= out_first at out_tokens[row - out_first]
   float* trace;              // debug trace or null
+  uint64_t* timing;          // per-phase timestamps (block 0) or null
   int32_t n_pages;
   int32_t max_pages_per_seq;
   int32_t n;                 // rows in this launch

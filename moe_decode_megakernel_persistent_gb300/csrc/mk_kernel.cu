@@ -25,7 +25,20 @@ namespace mk {
 
 constexpr int kMaxEnt = kMaxBatch * 8; // (row, expert slot) entries
 
+// Per-launch, per-block context shared by the phases; it lives in shared
+// memory (inside Fixed) so the phases read it with shared-memory loads.
+struct Ctx {
+  uint8_t* act;    // staging area in shared memory
+  int G, bid, n;
+  int r0, nr;      // hidden rows owned by this block
+  float *tr_x, *tr_attn, *tr_rl, *tr_tk, *tr_fin;
+  uint64_t* tm;    // timing stamps (block 0, thread 0 only) or null
+};
+
 struct Fixed {
+  StepArgs args;   // copy of the launch arguments
+  Ctx ctx;
+  int tok[kMaxBatch];
   int topk_id[kMaxBatch][8];
   float topk_w[kMaxBatch][8];
   float dots[kMaxEnt][kMaxRowsPerBlock];
@@ -34,6 +47,7 @@ struct Fixed {
   float best_v[kWarps][kMaxBatch];
   int best_i[kWarps][kMaxBatch];
   int unit_start[kMaxBatch + 1];
+  float rnorm[kMaxBatch];
   int16_t ue_expert[64], ue_start[64], ue_len[64];
   int16_t run_start[kMaxEnt], run_len[kMaxEnt], run_mat[kMaxEnt];
   uint8_t ent_b[kMaxEnt], ent_j[kMaxEnt];
@@ -42,6 +56,11 @@ struct Fixed {
 };
 constexpr int kActOffset = (sizeof(Fixed) + 127) / 128 * 128;
 constexpr int kActBytes = kSmemBytes - kActOffset;
+
+__device__ __forceinline__ Fixed& fixed() {
+  extern __shared__ __align__(128) uint8_t smem_dyn[];
+  return *reinterpret_cast<Fixed*>(smem_dyn);
+}
 
 __device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
 
@@ -54,17 +73,11 @@ struct Kv {
   }
 };
 
-// Per-launch context shared by the phases (one per block, in registers of
-// the caller and passed by reference).
-struct Ctx {
-  const StepArgs* a;
-  Fixed* F;
-  uint8_t* act;    // staging area in shared memory
-  const int* tok;  // token ids of the rows (shared memory)
-  int tid, lane, wid, G, bid, n;
-  int r0, nr;      // hidden rows owned by this block
-  float *tr_x, *tr_attn, *tr_rl, *tr_tk, *tr_fin;
-};
+// Timing record layout (uint64 ns): [0] start; per layer l and phase p:
+// [1 + 16 l + 3 p + k], k = 0 staging done, 1 work done, 2 barrier released;
+// [1 + 16 L] lm_head done.
+#define MK_STAMP(c, l, p, k) \
+  if ((c).tm && threadIdx.x == 0) (c).tm[1 + 16 * (l) + 3 * (p) + (k)] = globaltimer()
 
 template <class S, int WDT>
 struct Model {
@@ -84,8 +97,86 @@ struct Model {
   static_assert(kWarps * GQA * (HD + 2) * 4 <= kActBytes, "attention combine buffer");
   static_assert(TOPK <= 8 && E <= 64, "router tables");
 
-  __device__ static __forceinline__ float emb(const Ctx& c, int b, int k) {
-    return ld_aux<AUX>(c.a->embed, c.tok[b] * H + k);
+
+
+  static constexpr int PR = HD + 4;  // partial row: m, l, pad, pad, o[HD] (16-byte rows)
+  static constexpr int TU = 4;
+
+  __device__ static __forceinline__ void unit_of(const StepArgs& a, const int* unit_start, int u, int n,
+                                                 int& b, int& g, int& ci, int& nch) {
+    b = 0;
+    while (b + 1 < n && unit_start[b + 1] <= u) ++b;
+    nch = (a.pos[b] + 1 + a.chunk - 1) / a.chunk;
+    const int rem = u - unit_start[b];
+    g = rem / nch;
+    ci = rem % nch;
+  }
+
+  static constexpr int NQP = NH * HALF, NKP = NKV * HALF, NP = NQP + 2 * NKP;
+
+  // Weight rows of QKV task p (a RoPE pair of q or k rows, or two v rows).
+  __device__ static __forceinline__ RowRef qkv_row(const LayerW& Lw, int p, int r) {
+    int m, row;
+    if (p < NQP) { m = WQ; row = (p / HALF) * HD + p % HALF + r * HALF; }
+    else if (p < NQP + NKP) { const int q = p - NQP; m = WK; row = (q / HALF) * HD + q % HALF + r * HALF; }
+    else { const int q = p - NQP - NKP; m = WV; row = (q / HALF) * HD + 2 * (q % HALF) + r; }
+    return {(const uint8_t*)Lw.w[m] + (size_t)row * GH::ROW_BYTES,
+            (const uint16_t*)Lw.s[m] + (size_t)row * (H / 64)};
+  }
+
+  // --- L2 warm-up (thread 0): bytes a block reads in a later phase are
+  // requested from HBM early, so that phase's loads find them in L2.
+  __device__ static void prefetch_rows(const void* w, const void* s, size_t row0, int rows, int row_bytes,
+                                       int scale_bytes) {
+    if (rows <= 0) return;
+    prefetch_l2((const uint8_t*)w + row0 * row_bytes, rows * row_bytes);
+    if (WDT == WINT4) prefetch_l2((const uint8_t*)s + row0 * scale_bytes, rows * scale_bytes);
+  }
+
+  // QKV rows and o_proj rows of layer l owned by this block.
+  __device__ static void prefetch_attn_weights(int l) {
+    const Ctx& c = fixed().ctx;
+    const LayerW& Lw = fixed().args.layers[l];
+    int p0, p1;
+    split_range(NP, c.G, c.bid, p0, p1);
+    // rows of consecutive tasks are consecutive within a head: merge them
+    for (int r = 0; r < 2; ++r) {
+      const uint8_t* run_w = nullptr; const uint16_t* run_s = nullptr;
+      int run_n = 0;
+      for (int p = p0; p <= p1; ++p) {
+        const uint8_t* w = nullptr; const uint16_t* s = nullptr;
+        if (p < p1) { const RowRef rr = qkv_row(Lw, p, r); w = rr.w; s = rr.s; }
+        if (run_n && p < p1 && w == run_w + (size_t)run_n * GH::ROW_BYTES) { ++run_n; continue; }
+        if (run_n) prefetch_rows(run_w, run_s, 0, run_n, GH::ROW_BYTES, H / 64 * 2);
+        run_w = w; run_s = s; run_n = p < p1 ? 1 : 0;
+      }
+    }
+    prefetch_rows(Lw.w[WO], Lw.s[WO], c.r0, c.nr, GQ::ROW_BYTES, QD / 64 * 2);
+  }
+
+  // Cached K/V of this block's attention units at layer l.  Pages come from
+  // the block table, or for a row's newest page from the launch arguments;
+  // out-of-range entries are skipped.
+  __device__ static void prefetch_kv(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    (void)tid; (void)lane; (void)wid;
+    for (int u = c.bid; u < a.n_units; u += c.G) {
+      int b, g, ci, nch;
+      unit_of(a, fixed().unit_start, u, c.n, b, g, ci, nch);
+      const int t0 = ci * a.chunk, t1 = min(a.pos[b] + 1, t0 + a.chunk);
+      for (int pi = t0 / kPageTokens; pi <= (t1 - 1) / kPageTokens; ++pi) {
+        int page = pi == a.pos[b] / kPageTokens ? a.cur_page[b]
+                 : (pi < a.max_pages_per_seq ? __ldcg(a.block_table + a.slot[b] * a.max_pages_per_seq + pi) : -1);
+        if (page < 0 || page >= a.n_pages) continue;
+        const int s0 = max(t0, pi * kPageTokens) % kPageTokens;
+        const int s1 = (min(t1, (pi + 1) * kPageTokens) - 1) % kPageTokens + 1;
+        for (int kv = 0; kv < 2; ++kv)
+          prefetch_l2(a.kv + Kv<S>::offset(l, a.n_pages, page, kv, g, s0), (s1 - s0) * HD * 2);
+      }
+    }
   }
 
   // ---------------------------------------------------------------- P1
@@ -93,45 +184,50 @@ struct Model {
   // the QKV projection.  A task is a RoPE pair of q or k rows (i, i + HD/2)
   // of one head, or two adjacent v rows, so the warp that forms a pair also
   // rotates it and writes it: q to scratch, k and v as bf16 into the page.
-  __device__ static __noinline__ void qkv(const Ctx& c, int l) {
-    const StepArgs& a = *c.a;
+  __device__ static __noinline__ void qkv(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    (void)tid; (void)lane; (void)wid;
     const LayerW& Lw = a.layers[l];
-    const int n = c.n, lane = c.lane;
+    const int n = c.n;
     if (l == 0 && c.bid == 0)
-      for (int i = c.tid; i < a.n_upd; i += kThreads)
+      for (int i = tid; i < a.n_upd; i += kThreads)
         a.block_table[a.upd[i].slot * a.max_pages_per_seq + a.upd[i].index] = a.upd[i].page;
-    for (int b = c.wid; b < n; b += kWarps) {
-      const float* xb = a.sc.x + b * H;
-      auto xv = [&](int k) -> float { return l == 0 ? emb(c, b, k) : __ldcg(xb + k); };
-      const float r = rsqrtf(warp_sumsq<H>(lane, xv) / H + a.eps);
-      GH::stage(c.act + b * GH::ACT_BYTES, lane,
-                [&](int k) { return xv(k) * r * ld_aux<AUX>(Lw.attn_norm, k); });
+    {
+      const void* nw = Lw.attn_norm;
+      const void* embed = a.embed;
+      const float* x = a.sc.x;
+      const int* tok = F.tok;
+      const bool first = l == 0;
+      stage_block<WDT, H>(
+          c.act, n,
+          [&](int r, int f4) -> float4 {
+            return first ? ld_aux4<AUX>(embed, (size_t)tok[r] * (H / 4) + f4)
+                         : __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4);
+          },
+          true, a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
     }
     if (l == 0)  // residual rows this block reads back in P3
-      for (int i = c.tid; i < n * c.nr; i += kThreads) {
+      for (int i = tid; i < n * c.nr; i += kThreads) {
         const int b = i / c.nr, r = c.r0 + i % c.nr;
-        a.sc.x[b * H + r] = emb(c, b, r);
+        a.sc.x[b * H + r] = ld_aux<AUX>(a.embed, (size_t)F.tok[b] * H + r);
       }
     __syncthreads();
+    MK_STAMP(c, l, 0, 0);
 
-    constexpr int NQP = NH * HALF, NKP = NKV * HALF, NP = NQP + 2 * NKP;
     int p0, p1;
     split_range(NP, c.G, c.bid, p0, p1);
     struct {
       const StepArgs* a; const LayerW* Lw; int p0, l, lane;
-      __device__ void row(int t, int r, const uint8_t** w, const uint16_t** s) const {
-        const int p = p0 + t;
-        int m, row;
-        if (p < NQP) { m = WQ; row = (p / HALF) * HD + p % HALF + r * HALF; }
-        else if (p < NQP + NKP) { const int q = p - NQP; m = WK; row = (q / HALF) * HD + q % HALF + r * HALF; }
-        else { const int q = p - NQP - NKP; m = WV; row = (q / HALF) * HD + 2 * (q % HALF) + r; }
-        *w = (const uint8_t*)Lw->w[m] + (size_t)row * GH::ROW_BYTES;
-        *s = (const uint16_t*)Lw->s[m] + (size_t)row * (H / 64);
+      __device__ __forceinline__ RowRef row(int t, int r) const {
+        return qkv_row(*Lw, p0 + t, r);
       }
-      __device__ int acts(int, const uint8_t** list, int* start) const {
-        *list = nullptr; *start = 0; return a->n;
+      __device__ __forceinline__ ActRange acts(int) const {
+        return {nullptr, 0, a->n};
       }
-      __device__ void out(int t, int b, int, const float* v) const {
+      __device__ __forceinline__ void out(int t, int b, int, float v0, float v1) const {
         if (lane != 0) return;
         const int p = p0 + t;
         const int pos = a->pos[b];
@@ -139,8 +235,8 @@ struct Model {
           const int q = p < NQP ? p : p - NQP;
           const int hh = q / HALF, i = q % HALF;
           const float2 cs = __ldg(a->rope + (size_t)pos * HALF + i);
-          const float e0 = v[0] * cs.x - v[1] * cs.y;
-          const float e1 = v[1] * cs.x + v[0] * cs.y;
+          const float e0 = v0 * cs.x - v1 * cs.y;
+          const float e1 = v1 * cs.x + v0 * cs.y;
           if (p < NQP) {
             a->sc.q[b * QD + hh * HD + i] = e0;
             a->sc.q[b * QD + hh * HD + i + HALF] = e1;
@@ -153,8 +249,8 @@ struct Model {
           const int q = p - NQP - NKP;
           const int g = q / HALF, i2 = 2 * (q % HALF);
           uint16_t* dst = a->kv + Kv<S>::offset(l, a->n_pages, a->cur_page[b], 1, g, pos % kPageTokens);
-          dst[i2] = f_to_bf16(v[0]);
-          dst[i2 + 1] = f_to_bf16(v[1]);
+          dst[i2] = f_to_bf16(v0);
+          dst[i2 + 1] = f_to_bf16(v1);
         }
       }
     } task{&a, &Lw, p0, l, lane};
@@ -163,32 +259,25 @@ struct Model {
 
   // ---------------------------------------------------------------- P2
   // Split attention over the paged cache.  Unit = (row, kv head, chunk of
-  // positions); warps take positions of the chunk, keep a running max, sum
-  // and weighted value (online softmax) for the GQA heads of the kv head,
-  // combine across warps, and write the unit's partial (m, l, o).  The last
-  // unit of a (row, kv head) to finish merges all its chunks in chunk order.
-  __device__ static __noinline__ void attention(const Ctx& c, int l) {
-    const StepArgs& a = *c.a;
-    Fixed& F = *c.F;
-    const int n = c.n, tid = c.tid, lane = c.lane, wid = c.wid;
-    if (tid == 0) {
-      int acc = 0;
-      for (int b = 0; b < n; ++b) {
-        F.unit_start[b] = acc;
-        acc += NKV * ((a.pos[b] + 1 + a.chunk - 1) / a.chunk);
-      }
-      F.unit_start[n] = acc;
-    }
-    __syncthreads();
+  // positions); each warp takes TU positions at a time (their K and V rows
+  // loaded together), keeps a running max, sum and weighted value (online
+  // softmax) for the GQA heads of the kv head; the warps are combined and
+  // the unit's partial (m, l, o) written.  The last unit of a (row, kv head)
+  // to finish copies all its chunk partials into shared memory and merges
+  // them in chunk order (log-sum-exp).
+  __device__ static __noinline__ void attention(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    (void)tid; (void)lane; (void)wid;
+    const int n = c.n;
     float* comb = reinterpret_cast<float*>(c.act);  // [warp][GQA][HD + 2]
     const float qscale = rsqrtf((float)HD);
     for (int u = c.bid; u < a.n_units; u += c.G) {
-      int b = 0;
-      while (b + 1 < n && F.unit_start[b + 1] <= u) ++b;
+      int b, g, ci, nch;
+      unit_of(a, F.unit_start, u, n, b, g, ci, nch);
       const int ctx = a.pos[b] + 1;
-      const int nch = (ctx + a.chunk - 1) / a.chunk;
-      const int rem = u - F.unit_start[b];
-      const int g = rem / nch, ci = rem % nch;
       const int t0 = ci * a.chunk, t1 = min(ctx, t0 + a.chunk);
       const int* bt = a.block_table + a.slot[b] * a.max_pages_per_seq;
 
@@ -205,43 +294,52 @@ struct Model {
 #pragma unroll
         for (int d = 0; d < DPL; ++d) o[i][d] = 0.f;
       }
-      for (int t = t0 + wid; t < t1; t += kWarps) {
-        const int pi = t / kPageTokens;
-        int page = pi < a.max_pages_per_seq ? __ldcg(bt + pi) : -1;
-        if (page < 0 || page >= a.n_pages) {
-          set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_PAGE, t);
-          page = 0;
+      for (int tb = t0 + wid; tb < t1; tb += kWarps * TU) {
+        float kf[TU][DPL], vf[TU][DPL];
+#pragma unroll
+        for (int k = 0; k < TU; ++k) {
+          const int t = tb + k * kWarps;
+          if (t >= t1) break;
+          const int pi = t / kPageTokens;
+          int page = pi < a.max_pages_per_seq ? __ldcg(bt + pi) : -1;
+          if (page < 0 || page >= a.n_pages) {
+            set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_PAGE, t);
+            page = 0;
+          }
+          const int slot = t % kPageTokens;
+          const uint16_t* kp = a.kv + Kv<S>::offset(l, a.n_pages, page, 0, g, slot) + lane * DPL;
+          const uint16_t* vp = a.kv + Kv<S>::offset(l, a.n_pages, page, 1, g, slot) + lane * DPL;
+          if constexpr (DPL == 4) {
+            const uint2 kr = __ldcg(reinterpret_cast<const uint2*>(kp));
+            const uint2 vr = __ldcg(reinterpret_cast<const uint2*>(vp));
+            kf[k][0] = bf16_to_f(kr.x & 0xffff); kf[k][1] = bf16_to_f(kr.x >> 16);
+            kf[k][2] = bf16_to_f(kr.y & 0xffff); kf[k][3] = bf16_to_f(kr.y >> 16);
+            vf[k][0] = bf16_to_f(vr.x & 0xffff); vf[k][1] = bf16_to_f(vr.x >> 16);
+            vf[k][2] = bf16_to_f(vr.y & 0xffff); vf[k][3] = bf16_to_f(vr.y >> 16);
+          } else {
+            const uint32_t kr = __ldcg(reinterpret_cast<const unsigned int*>(kp));
+            const uint32_t vr = __ldcg(reinterpret_cast<const unsigned int*>(vp));
+            kf[k][0] = bf16_to_f(kr & 0xffff); kf[k][1] = bf16_to_f(kr >> 16);
+            vf[k][0] = bf16_to_f(vr & 0xffff); vf[k][1] = bf16_to_f(vr >> 16);
+          }
         }
-        const int slot = t % kPageTokens;
-        const uint16_t* kp = a.kv + Kv<S>::offset(l, a.n_pages, page, 0, g, slot) + lane * DPL;
-        const uint16_t* vp = a.kv + Kv<S>::offset(l, a.n_pages, page, 1, g, slot) + lane * DPL;
-        float kf[DPL], vf[DPL];
-        if constexpr (DPL == 4) {
-          const uint2 kr = __ldcg(reinterpret_cast<const uint2*>(kp));
-          const uint2 vr = __ldcg(reinterpret_cast<const uint2*>(vp));
-          kf[0] = bf16_to_f(kr.x & 0xffff); kf[1] = bf16_to_f(kr.x >> 16);
-          kf[2] = bf16_to_f(kr.y & 0xffff); kf[3] = bf16_to_f(kr.y >> 16);
-          vf[0] = bf16_to_f(vr.x & 0xffff); vf[1] = bf16_to_f(vr.x >> 16);
-          vf[2] = bf16_to_f(vr.y & 0xffff); vf[3] = bf16_to_f(vr.y >> 16);
-        } else {
-          const uint32_t kr = __ldcg(reinterpret_cast<const unsigned int*>(kp));
-          const uint32_t vr = __ldcg(reinterpret_cast<const unsigned int*>(vp));
-          kf[0] = bf16_to_f(kr & 0xffff); kf[1] = bf16_to_f(kr >> 16);
-          vf[0] = bf16_to_f(vr & 0xffff); vf[1] = bf16_to_f(vr >> 16);
-        }
 #pragma unroll
-        for (int i = 0; i < GQA; ++i) {
-          float s = 0.f;
+        for (int k = 0; k < TU; ++k) {
+          if (tb + k * kWarps >= t1) break;
 #pragma unroll
-          for (int d = 0; d < DPL; ++d) s = fmaf(q[i][d], kf[d], s);
-          s = warp_sum(s);
-          const float mn = fmaxf(m[i], s);
-          const float corr = expf(m[i] - mn);
-          const float p = expf(s - mn);
-          lsum[i] = lsum[i] * corr + p;
+          for (int i = 0; i < GQA; ++i) {
+            float sc = 0.f;
 #pragma unroll
-          for (int d = 0; d < DPL; ++d) o[i][d] = fmaf(o[i][d], corr, p * vf[d]);
-          m[i] = mn;
+            for (int d = 0; d < DPL; ++d) sc = fmaf(q[i][d], kf[k][d], sc);
+            sc = warp_sum(sc);
+            const float mn = fmaxf(m[i], sc);
+            const float corr = expf(m[i] - mn);
+            const float p = expf(sc - mn);
+            lsum[i] = lsum[i] * corr + p;
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) o[i][d] = fmaf(o[i][d], corr, p * vf[k][d]);
+            m[i] = mn;
+          }
         }
       }
 #pragma unroll
@@ -253,7 +351,7 @@ struct Model {
       }
       __syncthreads();
       if (u >= a.max_units) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, u);
-      float* pu = a.sc.part + (size_t)min(u, a.max_units - 1) * GQA * (HD + 2);
+      float* pu = a.sc.part + (size_t)min(u, a.max_units - 1) * GQA * PR;
       for (int idx = tid; idx < GQA * HD; idx += kThreads) {
         const int i = idx / HD, d = idx % HD;
         float M = -INFINITY;
@@ -265,8 +363,8 @@ struct Model {
           L = fmaf(cw[1], f, L);
           O = fmaf(cw[2 + d], f, O);
         }
-        if (d == 0) { pu[i * (HD + 2)] = M; pu[i * (HD + 2) + 1] = L; }
-        pu[i * (HD + 2) + 2 + d] = O;
+        if (d == 0) { pu[i * PR] = M; pu[i * PR + 1] = L; }
+        pu[i * PR + 4 + d] = O;
       }
       __syncthreads();
       if (tid == 0) {
@@ -277,17 +375,30 @@ struct Model {
       __syncthreads();
       if (F.flag) {  // last unit of (b, g): log-sum-exp merge of its chunks
         __threadfence();
-        const float* pb = a.sc.part + (size_t)(F.unit_start[b] + g * nch) * GQA * (HD + 2);
+        const float4* src = reinterpret_cast<const float4*>(
+            a.sc.part + (size_t)(F.unit_start[b] + g * nch) * GQA * PR);
+        float4* pm = reinterpret_cast<float4*>(c.act);   // [chunk][GQA][PR]
+        const int nv = nch * GQA * PR / 4;
+        // a chunk is at least ctx * n_kv_heads / grid positions, so a (row,
+        // kv head) has at most grid / n_kv_heads + 1 chunks; guard anyway
+        if (nv * 16 > kActBytes) {
+          if (tid == 0) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, nch);
+          __syncthreads();
+          continue;
+        }
+        for (int v = tid; v < nv; v += kThreads) pm[v] = __ldcg(src + v);
+        __syncthreads();
+        const float* ps = reinterpret_cast<const float*>(pm);
         for (int idx = tid; idx < GQA * HD; idx += kThreads) {
           const int i = idx / HD, d = idx % HD;
           float M = -INFINITY;
-          for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(pb + (cc * GQA + i) * (HD + 2)));
+          for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, ps[(cc * GQA + i) * PR]);
           float L = 0.f, O = 0.f;
           for (int cc = 0; cc < nch; ++cc) {
-            const float* pc = pb + (cc * GQA + i) * (HD + 2);
-            const float f = expf(__ldcg(pc) - M);
-            L = fmaf(__ldcg(pc + 1), f, L);
-            O = fmaf(__ldcg(pc + 2 + d), f, O);
+            const float* pc = ps + (cc * GQA + i) * PR;
+            const float f = expf(pc[0] - M);
+            L = fmaf(pc[1], f, L);
+            O = fmaf(pc[4 + d], f, O);
           }
           const float val = O / L;
           a.sc.attn[b * QD + (g * GQA + i) * HD + d] = val;
@@ -305,28 +416,34 @@ struct Model {
   // row times w2, so logits = rsqrt(mean(h^2) + eps) * sum_blocks(partials);
   // the scalar is applied in P4.  The last block to finish adds the
   // partials in block order (deterministic).
-  __device__ static __noinline__ void oproj(const Ctx& c, int l) {
-    const StepArgs& a = *c.a;
-    Fixed& F = *c.F;
+  __device__ static __noinline__ void oproj(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    (void)tid; (void)lane; (void)wid;
     const LayerW& Lw = a.layers[l];
-    const int n = c.n, tid = c.tid, lane = c.lane;
-    for (int b = c.wid; b < n; b += kWarps) {
-      const float* ab = a.sc.attn + b * QD;
-      GQ::stage(c.act + b * GQ::ACT_BYTES, lane, [&](int k) { return __ldcg(ab + k); });
+    const int n = c.n;
+    {
+      const float* at = a.sc.attn;
+      stage_block<WDT, QD>(
+          c.act, n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(at + r * QD) + f4); },
+          false, 0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
     }
     __syncthreads();
+    MK_STAMP(c, l, 2, 0);
     struct {
       const StepArgs* a; const LayerW* Lw; Fixed* F; int r0, lane;
-      __device__ void row(int t, int, const uint8_t** w, const uint16_t** s) const {
-        *w = (const uint8_t*)Lw->w[WO] + (size_t)(r0 + t) * GQ::ROW_BYTES;
-        *s = (const uint16_t*)Lw->s[WO] + (size_t)(r0 + t) * (QD / 64);
+      __device__ __forceinline__ RowRef row(int t, int) const {
+        return {(const uint8_t*)Lw->w[WO] + (size_t)(r0 + t) * GQ::ROW_BYTES,
+                (const uint16_t*)Lw->s[WO] + (size_t)(r0 + t) * (QD / 64)};
       }
-      __device__ int acts(int, const uint8_t** list, int* start) const {
-        *list = nullptr; *start = 0; return a->n;
+      __device__ __forceinline__ ActRange acts(int) const {
+        return {nullptr, 0, a->n};
       }
-      __device__ void out(int t, int b, int, const float* v) const {
+      __device__ __forceinline__ void out(int t, int b, int, float v0, float v1) const {
         if (lane != 0) return;
-        const float hv = __ldcg(a->sc.x + b * H + r0 + t) + v[0];
+        const float hv = __ldcg(a->sc.x + b * H + r0 + t) + v0;
         a->sc.h[b * H + r0 + t] = hv;
         F->hs[b][t] = hv;
       }
@@ -357,7 +474,14 @@ struct Model {
         int g0, g1;
         split_range(c.G, NS, sp, g0, g1);
         float s = 0.f;
-        for (int g = g0; g < g1; ++g) s += __ldcg(a.sc.rpart + ((size_t)g * kMaxBatch + b) * E + e);
+        for (int g = g0; g < g1; g += 8) {
+          float v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            v[u] = g + u < g1 ? __ldcg(a.sc.rpart + ((size_t)(g + u) * kMaxBatch + b) * E + e) : 0.f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) s += v[u];
+        }
         if (NS == 1) a.sc.rlogit[b * E + e] = s;
         else F.red[idx] = s;
       }
@@ -374,165 +498,217 @@ struct Model {
   }
 
   // ---------------------------------------------------------------- P4a
-  // RMSNorm of h (every block) and, in MoE layers, softmax over the experts,
-  // top-k (ties -> lower expert id) and renormalised weights, then the
-  // selections grouped by expert.
-  __device__ static __noinline__ void route(const Ctx& c, int l) {
-    const StepArgs& a = *c.a;
-    Fixed& F = *c.F;
+  // Routing, then the post-attention RMSNorm.  The router logits of a row are
+  // rsqrt(mean(h^2) + eps) times the block-summed partials of P3; that factor
+  // is positive and common to the row, so the top-k selection (ties -> lower
+  // expert id) is made from the partials before the norm is known.  The
+  // selected experts' weights are then requested from HBM while the norm is
+  // computed, and the softmax weights (renormalised over the selection) are
+  // formed from the scaled logits.  Dense layers only norm.
+  __device__ static __noinline__ void route(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    (void)tid; (void)lane; (void)wid;
     const LayerW& Lw = a.layers[l];
     const bool moe = l >= a.n_dense;
-    const int n = c.n, lane = c.lane, wid = c.wid;
+    const int n = c.n;
     constexpr int EJ = (E + 31) / 32;
-    for (int b = wid; b < n; b += kWarps) {
-      const float* hb = a.sc.h + b * H;
-      auto hv = [&](int k) -> float { return __ldcg(hb + k); };
-      const float r = rsqrtf(warp_sumsq<H>(lane, hv) / H + a.eps);
-      GH::stage(c.act + b * GH::ACT_BYTES, lane,
-                [&](int k) { return hv(k) * r * ld_aux<AUX>(Lw.ffn_norm, k); });
-      if (!moe) continue;
-      float lg[EJ];
-#pragma unroll
-      for (int j = 0; j < EJ; ++j) {
-        const int e = lane + 32 * j;
-        lg[j] = e < E ? r * __ldcg(a.sc.rlogit + b * E + e) : -INFINITY;
-        if (c.tr_rl && c.bid == 0 && e < E) c.tr_rl[((size_t)l * n + b) * E + e] = lg[j];
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < EJ; ++j) mx = fmaxf(mx, lg[j]);
-      mx = warp_max(mx);
-      float wsum = 0.f, wk[TOPK];
-      int ids[TOPK];
-#pragma unroll
-      for (int k = 0; k < TOPK; ++k) {
-        float bv = -INFINITY;
-        int be = INT_MAX;
+    if (moe) {
+      for (int b = wid; b < n; b += kWarps) {
+        float lg[EJ];
 #pragma unroll
         for (int j = 0; j < EJ; ++j) {
           const int e = lane + 32 * j;
-          if (e < E && (lg[j] > bv || (lg[j] == bv && e < be))) { bv = lg[j]; be = e; }
+          lg[j] = e < E ? __ldcg(a.sc.rlogit + b * E + e) : -INFINITY;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-          if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-        }
-        ids[k] = be;
-        wk[k] = expf(bv - mx);
-        wsum += wk[k];
-#pragma unroll
-        for (int j = 0; j < EJ; ++j)
-          if (lane + 32 * j == be) lg[j] = -INFINITY;
-      }
-      if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < TOPK; ++k) {
-          F.topk_id[b][k] = ids[k];
+          float bv = -INFINITY;
+          int be = INT_MAX;
+#pragma unroll
+          for (int j = 0; j < EJ; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E && (lg[j] > bv || (lg[j] == bv && e < be))) { bv = lg[j]; be = e; }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+          }
+          if (lane == 0) { F.topk_id[b][k] = be; F.topk_w[b][k] = bv; }  // partial logit for now
+#pragma unroll
+          for (int j = 0; j < EJ; ++j)
+            if (lane + 32 * j == be) lg[j] = -INFINITY;
+        }
+      }
+      __syncthreads();
+      if (wid == 0) {
+        // entries sorted by (expert, row, slot); one run of rows per distinct expert
+        int base = 0, nue = 0;
+#pragma unroll
+        for (int j = 0; j < EJ; ++j) {
+          const int e = lane + 32 * j;
+          int cnt = 0;
+          for (int b = 0; b < n; ++b)
+            for (int k = 0; k < TOPK; ++k) cnt += F.topk_id[b][k] == e;
+          const int has = cnt > 0;
+          int incl = cnt, hincl = has;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            const int hy = __shfl_up_sync(0xffffffffu, hincl, o);
+            if (lane >= o) { incl += y; hincl += hy; }
+          }
+          const int start = base + incl - cnt;
+          const int ue = nue + hincl - has;
+          if (has) {
+            F.ue_expert[ue] = (int16_t)e;
+            F.ue_start[ue] = (int16_t)start;
+            F.ue_len[ue] = (int16_t)cnt;
+            int pos = start;
+            for (int b = 0; b < n; ++b)
+              for (int k = 0; k < TOPK; ++k)
+                if (F.topk_id[b][k] == e) {
+                  F.ent_b[pos] = (uint8_t)b;
+                  F.ent_j[pos] = (uint8_t)k;
+                  F.ent_of[b][k] = (uint8_t)pos;
+                  ++pos;
+                }
+          }
+          base += __shfl_sync(0xffffffffu, incl, 31);
+          nue += __shfl_sync(0xffffffffu, hincl, 31);
+        }
+        if (lane == 0) F.n_ue = nue;
+      }
+      __syncthreads();
+    }
+    {
+      const void* nw = Lw.ffn_norm;
+      const float* hp = a.sc.h;
+      stage_block<WDT, H>(
+          c.act, n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(hp + r * H) + f4); },
+          true, a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, F.rnorm);
+    }
+    __syncthreads();
+    MK_STAMP(c, l, 3, 0);
+    if (tid == 0) prefetch_ffn_and_next(l);
+    if (!moe) return;
+    for (int b = wid; b < n; b += kWarps) {
+      const float r = F.rnorm[b];
+      if (c.tr_rl && c.bid == 0)
+        for (int e = lane; e < E; e += 32)
+          c.tr_rl[((size_t)l * n + b) * E + e] = r * __ldcg(a.sc.rlogit + b * E + e);
+      if (lane == 0) {
+        // softmax over the selection = softmax over all experts renormalised
+        const float top = r * F.topk_w[b][0];
+        float wk[TOPK], wsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < TOPK; ++k) {
+          wk[k] = expf(r * F.topk_w[b][k] - top);
+          wsum += wk[k];
+        }
+#pragma unroll
+        for (int k = 0; k < TOPK; ++k) {
           F.topk_w[b][k] = wk[k] / wsum;
           if (c.tr_tk && c.bid == 0) {
-            c.tr_tk[((size_t)l * n + b) * 2 * TOPK + k] = (float)ids[k];
+            c.tr_tk[((size_t)l * n + b) * 2 * TOPK + k] = (float)F.topk_id[b][k];
             c.tr_tk[((size_t)l * n + b) * 2 * TOPK + TOPK + k] = wk[k] / wsum;
           }
         }
       }
     }
-    __syncthreads();
-    if (!moe || wid != 0) return;
-    // entries sorted by (expert, row, slot); one run of rows per distinct expert
-    int base = 0, nue = 0;
-#pragma unroll
-    for (int j = 0; j < EJ; ++j) {
-      const int e = lane + 32 * j;
-      int cnt = 0;
-      for (int b = 0; b < n; ++b)
-        for (int k = 0; k < TOPK; ++k) cnt += F.topk_id[b][k] == e;
-      const int has = cnt > 0;
-      int incl = cnt, hincl = has;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        const int hy = __shfl_up_sync(0xffffffffu, hincl, o);
-        if (lane >= o) { incl += y; hincl += hy; }
+  }
+
+  // Thread 0 after routing: this block's gate/up and down rows of layer l,
+  // then the attention weights and cached K/V of layer l + 1 (or the start of
+  // its lm_head rows after the last layer).
+  __device__ static void prefetch_ffn_and_next(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    (void)tid; (void)lane; (void)wid;
+    const LayerW& Lw = a.layers[l];
+    if (l >= a.n_dense) {
+      int u0, u1;
+      split_range(F.n_ue * FE, c.G, c.bid, u0, u1);
+      for (int ue = u0 / FE; ue < F.n_ue && ue * FE < u1; ++ue) {
+        const int e = F.ue_expert[ue];
+        const int f0 = max(u0, ue * FE) - ue * FE, f1 = min(u1, (ue + 1) * FE) - ue * FE;
+        for (int m = EGATE; m <= EUP; ++m)
+          prefetch_rows(Lw.w[m], Lw.s[m], (size_t)e * FE + f0, f1 - f0, GH::ROW_BYTES, H / 64 * 2);
       }
-      const int start = base + incl - cnt;
-      const int ue = nue + hincl - has;
-      if (has) {
-        F.ue_expert[ue] = (int16_t)e;
-        F.ue_start[ue] = (int16_t)start;
-        F.ue_len[ue] = (int16_t)cnt;
-        int pos = start;
-        for (int b = 0; b < n; ++b)
-          for (int k = 0; k < TOPK; ++k)
-            if (F.topk_id[b][k] == e) {
-              F.ent_b[pos] = (uint8_t)b;
-              F.ent_j[pos] = (uint8_t)k;
-              F.ent_of[b][k] = (uint8_t)pos;
-              ++pos;
-            }
-      }
-      base += __shfl_sync(0xffffffffu, incl, 31);
-      nue += __shfl_sync(0xffffffffu, hincl, 31);
+      for (int ue = 0; ue < F.n_ue; ++ue)
+        prefetch_rows(Lw.w[EDOWN], Lw.s[EDOWN], (size_t)F.ue_expert[ue] * H + c.r0, c.nr, GE::ROW_BYTES,
+                      FE / 64 * 2);
+    } else {
+      int f0, f1;
+      split_range(FD, c.G, c.bid, f0, f1);
+      for (int m = GATE; m <= UP; ++m) prefetch_rows(Lw.w[m], Lw.s[m], f0, f1 - f0, GH::ROW_BYTES, H / 64 * 2);
+      prefetch_rows(Lw.w[DOWN], Lw.s[DOWN], c.r0, c.nr, NSEG * GS::ROW_BYTES, FD / 64 * 2);
     }
-    if (lane == 0) F.n_ue = nue;
+    if (l + 1 < a.n_layers) {
+      prefetch_attn_weights(l + 1);
+      prefetch_kv(l + 1);
+    } else if (a.out_first < c.n) {
+      int v0, v1;
+      split_range(a.vocab, c.G, c.bid, v0, v1);
+      prefetch_rows(a.lm_head, a.lm_head_s, v0, min(v1 - v0, 128), GH::ROW_BYTES, H / 64 * 2);
+    }
   }
 
   // ---------------------------------------------------------------- P4b
   // Gate/up rows -> silu(gate) * up.  MoE: units (distinct expert, ffn row),
   // each computed for every row routed to that expert.  Dense: ffn rows.
-  __device__ static __noinline__ void gateup(const Ctx& c, int l) {
-    const StepArgs& a = *c.a;
-    Fixed& F = *c.F;
+  __device__ static __noinline__ void gateup(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    (void)tid; (void)lane; (void)wid;
     const LayerW& Lw = a.layers[l];
-    if (c.tid == 0) {  // warm L2 with this block's down-projection rows
-      if (l >= a.n_dense) {
-        for (int ue = 0; ue < F.n_ue; ++ue)
-          prefetch_l2((const uint8_t*)Lw.w[EDOWN] + ((size_t)F.ue_expert[ue] * H + c.r0) * GE::ROW_BYTES,
-                      c.nr * GE::ROW_BYTES);
-      } else {
-        prefetch_l2((const uint8_t*)Lw.w[DOWN] + (size_t)c.r0 * NSEG * GS::ROW_BYTES, c.nr * NSEG * GS::ROW_BYTES);
-      }
-    }
     if (l >= a.n_dense) {
       int u0, u1;
       split_range(F.n_ue * FE, c.G, c.bid, u0, u1);
       struct {
         const StepArgs* a; const LayerW* Lw; Fixed* F; int u0, lane;
-        __device__ void row(int t, int r, const uint8_t** w, const uint16_t** s) const {
+        __device__ __forceinline__ RowRef row(int t, int r) const {
           const int u = u0 + t, e = F->ue_expert[u / FE], f = u % FE;
           const size_t rr = (size_t)e * FE + f;
-          *w = (const uint8_t*)Lw->w[r ? EUP : EGATE] + rr * GH::ROW_BYTES;
-          *s = (const uint16_t*)Lw->s[r ? EUP : EGATE] + rr * (H / 64);
+          return {(const uint8_t*)Lw->w[r ? EUP : EGATE] + rr * GH::ROW_BYTES,
+                  (const uint16_t*)Lw->s[r ? EUP : EGATE] + rr * (H / 64)};
         }
-        __device__ int acts(int t, const uint8_t** list, int* start) const {
+        __device__ __forceinline__ ActRange acts(int t) const {
           const int ue = (u0 + t) / FE;
-          *list = F->ent_b; *start = F->ue_start[ue]; return F->ue_len[ue];
+          return {F->ent_b, F->ue_start[ue], F->ue_len[ue]};
         }
-        __device__ void out(int t, int b, int i, const float* v) const {
+        __device__ __forceinline__ void out(int t, int b, int i, float v0, float v1) const {
           if (lane != 0) return;
           const int u = u0 + t, f = u % FE;
           const int j = F->ent_j[F->ue_start[u / FE] + i];
-          a->sc.act[(b * TOPK + j) * FE + f] = silu(v[0]) * v[1];
+          a->sc.act[(b * TOPK + j) * FE + f] = silu(v0) * v1;
         }
-      } task{&a, &Lw, &F, u0, c.lane};
+      } task{&a, &Lw, &F, u0, lane};
       run_tasks<WDT, H, 2>(u1 - u0, c.act, task);
     } else {
       int f0, f1;
       split_range(FD, c.G, c.bid, f0, f1);
       struct {
         const StepArgs* a; const LayerW* Lw; int f0, lane;
-        __device__ void row(int t, int r, const uint8_t** w, const uint16_t** s) const {
-          *w = (const uint8_t*)Lw->w[r ? UP : GATE] + (size_t)(f0 + t) * GH::ROW_BYTES;
-          *s = (const uint16_t*)Lw->s[r ? UP : GATE] + (size_t)(f0 + t) * (H / 64);
+        __device__ __forceinline__ RowRef row(int t, int r) const {
+          return {(const uint8_t*)Lw->w[r ? UP : GATE] + (size_t)(f0 + t) * GH::ROW_BYTES,
+                  (const uint16_t*)Lw->s[r ? UP : GATE] + (size_t)(f0 + t) * (H / 64)};
         }
-        __device__ int acts(int, const uint8_t** list, int* start) const {
-          *list = nullptr; *start = 0; return a->n;
+        __device__ __forceinline__ ActRange acts(int) const {
+          return {nullptr, 0, a->n};
         }
-        __device__ void out(int t, int b, int, const float* v) const {
-          if (lane == 0) a->sc.dact[b * FD + f0 + t] = silu(v[0]) * v[1];
+        __device__ __forceinline__ void out(int t, int b, int, float v0, float v1) const {
+          if (lane == 0) a->sc.dact[b * FD + f0 + t] = silu(v0) * v1;
         }
-      } task{&a, &Lw, f0, c.lane};
+      } task{&a, &Lw, f0, lane};
       run_tasks<WDT, H, 2>(f1 - f0, c.act, task);
     }
   }
@@ -544,20 +720,32 @@ struct Model {
   // one weight matrix form a run, so each weight row is read once per run.
   // The weighted sum over experts is taken in slot order, then the residual.
   template <bool MOE>
-  __device__ static __noinline__ void down(const Ctx& c, int l) {
-    const StepArgs& a = *c.a;
-    Fixed& F = *c.F;
+  __device__ static __noinline__ void down(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    (void)tid; (void)lane; (void)wid;
     const LayerW& Lw = a.layers[l];
     using GD = typename std::conditional<MOE, GE, GS>::type;
-    const int n = c.n, tid = c.tid, lane = c.lane, nr = c.nr;
+    const int n = c.n, nr = c.nr;
     const int nent = MOE ? n * TOPK : n * NSEG;
     const int cap = kActBytes / GD::ACT_BYTES;
     for (int base = 0; base < nent; base += cap) {
       const int cnt = min(cap, nent - base);
-      for (int en = base + c.wid; en < base + cnt; en += kWarps) {
-        const float* src = MOE ? a.sc.act + (F.ent_b[en] * TOPK + F.ent_j[en]) * FE
-                               : a.sc.dact + (en % n) * FD + (en / n) * KSD;
-        GD::stage(c.act + (en - base) * GD::ACT_BYTES, lane, [&](int k) { return __ldcg(src + k); });
+      {
+        const float* act = a.sc.act;
+        const float* dact = a.sc.dact;
+        const Fixed* Fp = &F;
+        stage_block<WDT, MOE ? FE : KSD>(
+            c.act, cnt,
+            [&](int r, int f4) -> float4 {
+              const int en = base + r;
+              const float* src = MOE ? act + (Fp->ent_b[en] * TOPK + Fp->ent_j[en]) * FE
+                                     : dact + (en % n) * FD + (en / n) * KSD;
+              return __ldcg(reinterpret_cast<const float4*>(src) + f4);
+            },
+            false, 0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
       }
       if (tid == 0) {
         int nrun = 0;
@@ -574,26 +762,27 @@ struct Model {
         F.n_runs = nrun;
       }
       __syncthreads();
+      MK_STAMP(c, l, 4, 0);
       struct {
         const LayerW* Lw; Fixed* F; int r0, nr, base, lane;
-        __device__ void row(int t, int, const uint8_t** w, const uint16_t** s) const {
+        __device__ __forceinline__ RowRef row(int t, int) const {
           const int run = t / nr, rr = t % nr, mat = F->run_mat[run];
           if (MOE) {
             const size_t row = (size_t)mat * H + r0 + rr;
-            *w = (const uint8_t*)Lw->w[EDOWN] + row * GD::ROW_BYTES;
-            *s = (const uint16_t*)Lw->s[EDOWN] + row * (FE / 64);
+            return {(const uint8_t*)Lw->w[EDOWN] + row * GD::ROW_BYTES,
+                    (const uint16_t*)Lw->s[EDOWN] + row * (FE / 64)};
           } else {
             const size_t row = (size_t)(r0 + rr);
-            *w = (const uint8_t*)Lw->w[DOWN] + (row * NSEG + mat) * GD::ROW_BYTES;
-            *s = (const uint16_t*)Lw->s[DOWN] + row * (FD / 64) + mat * (KSD / 64);
+            return {(const uint8_t*)Lw->w[DOWN] + (row * NSEG + mat) * GD::ROW_BYTES,
+                    (const uint16_t*)Lw->s[DOWN] + row * (FD / 64) + mat * (KSD / 64)};
           }
         }
-        __device__ int acts(int t, const uint8_t** list, int* start) const {
+        __device__ __forceinline__ ActRange acts(int t) const {
           const int run = t / nr;
-          *list = nullptr; *start = F->run_start[run]; return F->run_len[run];
+          return {nullptr, F->run_start[run], F->run_len[run]};
         }
-        __device__ void out(int t, int ai, int, const float* v) const {
-          if (lane == 0) F->dots[base + ai][t % nr] = v[0];
+        __device__ __forceinline__ void out(int t, int ai, int, float v0, float v1) const {
+          if (lane == 0) F->dots[base + ai][t % nr] = v0;
         }
       } task{&Lw, &F, c.r0, nr, base, lane};
       run_tasks<WDT, MOE ? FE : KSD, 1>(F.n_runs * nr, c.act, task);
@@ -616,16 +805,20 @@ struct Model {
   // Final RMSNorm, this block's vocabulary rows, argmax per row of the batch
   // (ties -> lowest token id); the last block to finish reduces the blocks'
   // candidates in block order and writes the tokens.
-  __device__ static __noinline__ void lm_head(const Ctx& c) {
-    const StepArgs& a = *c.a;
-    Fixed& F = *c.F;
-    const int n = c.n, tid = c.tid, lane = c.lane, wid = c.wid;
-    for (int b = a.out_first + wid; b < n; b += kWarps) {
-      const float* xb = a.sc.x + b * H;
-      auto xv = [&](int k) -> float { return __ldcg(xb + k); };
-      const float r = rsqrtf(warp_sumsq<H>(lane, xv) / H + a.eps);
-      GH::stage(c.act + b * GH::ACT_BYTES, lane,
-                [&](int k) { return xv(k) * r * ld_aux<AUX>(a.final_norm, k); });
+  __device__ static __noinline__ void lm_head() {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    (void)tid; (void)lane; (void)wid;
+    const int n = c.n;
+    {
+      const void* nw = a.final_norm;
+      const float* x = a.sc.x + a.out_first * H;
+      stage_block<WDT, H>(
+          c.act + a.out_first * GH::ACT_BYTES, n - a.out_first,
+          [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4); },
+          true, a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
     }
     for (int i = tid; i < kWarps * kMaxBatch; i += kThreads) {
       F.best_v[i / kMaxBatch][i % kMaxBatch] = -INFINITY;
@@ -635,20 +828,20 @@ struct Model {
     int v0, v1;
     split_range(a.vocab, c.G, c.bid, v0, v1);
     struct {
-      const StepArgs* a; Fixed* F; float* tr; int v0, lane, wid;
-      __device__ void row(int t, int, const uint8_t** w, const uint16_t** s) const {
-        *w = (const uint8_t*)a->lm_head + (size_t)(v0 + t) * GH::ROW_BYTES;
-        *s = (const uint16_t*)a->lm_head_s + (size_t)(v0 + t) * (H / 64);
+      const StepArgs* a; Fixed* F; float* tr; int vr0, lane, wid;
+      __device__ __forceinline__ RowRef row(int t, int) const {
+        return {(const uint8_t*)a->lm_head + (size_t)(vr0 + t) * GH::ROW_BYTES,
+                (const uint16_t*)a->lm_head_s + (size_t)(vr0 + t) * (H / 64)};
       }
-      __device__ int acts(int, const uint8_t** list, int* start) const {
-        *list = nullptr; *start = a->out_first; return a->n - a->out_first;
+      __device__ __forceinline__ ActRange acts(int) const {
+        return {nullptr, a->out_first, a->n - a->out_first};
       }
-      __device__ void out(int t, int b, int, const float* v) const {
+      __device__ __forceinline__ void out(int t, int b, int, float v0, float v1) const {
         if (lane != 0) return;
-        const int tok = v0 + t;
+        const int tok = vr0 + t;
         // a warp visits its rows in increasing order: '>' keeps the lowest id
-        if (v[0] > F->best_v[wid][b]) { F->best_v[wid][b] = v[0]; F->best_i[wid][b] = tok; }
-        if (tr) tr[(size_t)b * a->vocab + tok] = v[0];
+        if (v0 > F->best_v[wid][b]) { F->best_v[wid][b] = v0; F->best_i[wid][b] = tok; }
+        if (tr) tr[(size_t)b * a->vocab + tok] = v0;
       }
     } task{&a, &F, c.tr_fin, v0, lane, wid};
     run_tasks<WDT, H, 1>(v1 - v0, c.act, task);
@@ -672,8 +865,7 @@ struct Model {
     __syncthreads();
     if (!F.flag) return;
     __threadfence();
-    const int b = wid;
-    if (b >= a.out_first && b < n) {
+    for (int b = a.out_first + wid; b < n; b += kWarps) {
       float bv = -INFINITY;
       int bi = INT_MAX;
       for (int g = lane; g < c.G; g += 32) {
@@ -697,60 +889,90 @@ template <class S, int WDT>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepArgs a) {
   using M = Model<S, WDT>;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_tok[kMaxBatch];
-  Ctx c;
-  c.a = &a;
-  c.F = reinterpret_cast<Fixed*>(smem);
-  c.act = smem + kActOffset;
-  c.tok = s_tok;
-  c.tid = threadIdx.x;
-  c.lane = c.tid & 31;
-  c.wid = c.tid >> 5;
-  c.G = gridDim.x;
-  c.bid = blockIdx.x;
-  c.n = a.n;
-  int r1;
-  split_range(S::H, c.G, c.bid, c.r0, r1);
-  c.nr = r1 - c.r0;
+  Fixed& F = *reinterpret_cast<Fixed*>(smem);
+  const int tid = threadIdx.x;
+  // launch arguments into shared memory: the phases read them from there
+  {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(&a);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(&F.args);
+    static_assert(sizeof(StepArgs) % 4 == 0, "word copy");
+    for (int i = tid; i < (int)(sizeof(StepArgs) / 4); i += kThreads) dst[i] = src[i];
+  }
   const int n = a.n;
-  c.tr_x = a.trace;
-  c.tr_attn = a.trace ? c.tr_x + (size_t)a.n_layers * n * S::H : nullptr;
-  c.tr_rl = a.trace ? c.tr_attn + (size_t)a.n_layers * n * M::QD : nullptr;
-  c.tr_tk = a.trace ? c.tr_rl + (size_t)a.n_layers * n * S::E : nullptr;
-  c.tr_fin = a.trace ? c.tr_tk + (size_t)a.n_layers * n * 2 * S::TOPK : nullptr;
-
+  if (tid == 0) {
+    Ctx& c = F.ctx;
+    c.act = smem + kActOffset;
+    c.G = gridDim.x;
+    c.bid = blockIdx.x;
+    c.n = n;
+    int r0, r1;
+    split_range(S::H, c.G, c.bid, r0, r1);
+    c.r0 = r0;
+    c.nr = r1 - r0;
+    c.tr_x = a.trace;
+    c.tr_attn = a.trace ? c.tr_x + (size_t)a.n_layers * n * S::H : nullptr;
+    c.tr_rl = a.trace ? c.tr_attn + (size_t)a.n_layers * n * M::QD : nullptr;
+    c.tr_tk = a.trace ? c.tr_rl + (size_t)a.n_layers * n * S::E : nullptr;
+    c.tr_fin = a.trace ? c.tr_tk + (size_t)a.n_layers * n * 2 * S::TOPK : nullptr;
+    c.tm = (a.timing && blockIdx.x == 0) ? a.timing : nullptr;
+    // attention work units: (row, kv head, chunk), row-major
+    int acc = 0;
+    for (int b = 0; b < n; ++b) {
+      F.unit_start[b] = acc;
+      acc += S::NKV * ((a.pos[b] + 1 + a.chunk - 1) / a.chunk);
+    }
+    F.unit_start[n] = acc;
+  }
   // token ids (device memory; may be the previous step's output)
-  if (c.tid < n) {
-    int t = a.tokens[c.tid];
+  if (tid < n) {
+    int t = a.tokens[tid];
     if (t < 0 || t >= a.vocab) {
       set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_TOKEN, t);
       t = 0;
     }
-    s_tok[c.tid] = t;
+    F.tok[tid] = t;
+  }
+  __syncthreads();
+  const Ctx& c = F.ctx;
+  if (tid == 0) {
+    M::prefetch_attn_weights(0);
+    M::prefetch_kv(0);
   }
   __syncthreads();
 
   uint32_t nbar = 0;
+  if (c.tm && tid == 0) c.tm[0] = globaltimer();
   for (int l = 0; l < a.n_layers; ++l) {
-    M::qkv(c, l);
+    M::qkv(l);
+    MK_STAMP(c, l, 0, 1);
     if (!grid_barrier(a, nbar)) goto done;
-    M::attention(c, l);
+    MK_STAMP(c, l, 0, 2);
+    M::attention(l);
+    MK_STAMP(c, l, 1, 1);
     if (!grid_barrier(a, nbar)) goto done;
-    M::oproj(c, l);
+    MK_STAMP(c, l, 1, 2);
+    M::oproj(l);
+    MK_STAMP(c, l, 2, 1);
     if (!grid_barrier(a, nbar)) goto done;
-    M::route(c, l);
+    MK_STAMP(c, l, 2, 2);
+    M::route(l);
     __syncthreads();
-    M::gateup(c, l);
+    M::gateup(l);
+    MK_STAMP(c, l, 3, 1);
     if (!grid_barrier(a, nbar)) goto done;
-    if (l >= a.n_dense) M::template down<true>(c, l);
-    else M::template down<false>(c, l);
+    MK_STAMP(c, l, 3, 2);
+    if (l >= a.n_dense) M::template down<true>(l);
+    else M::template down<false>(l);
+    MK_STAMP(c, l, 4, 1);
     if (!grid_barrier(a, nbar)) goto done;
+    MK_STAMP(c, l, 4, 2);
   }
-  if (a.out_first < n) M::lm_head(c);
+  if (a.out_first < n) M::lm_head();
+  if (c.tm && tid == 0) c.tm[1 + 16 * a.n_layers] = globaltimer();
 
 done:
   __syncthreads();
-  if (c.tid == 0) {
+  if (tid == 0) {
     __threadfence();
     if (atomicAdd(a.sc.sync + 32, 1u) == (uint32_t)(c.G - 1)) {
       // every block has left its work: reset the launch-scoped counters

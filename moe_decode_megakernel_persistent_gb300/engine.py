@@ -120,6 +120,34 @@ class Engine:
         self.trace = torch.zeros(nbytes // 4, dtype=torch.float32, device="cuda")
         L.mk_set_debug(self.ctx, L.MK_DBG_TRACE, 0, _ptr(self.trace), nbytes, 0)
 
+    def enable_timing(self):
+        """Per-phase %globaltimer stamps of block 0 for each following launch."""
+        n = 16 * self.shape.n_layers + 2
+        self.timing = torch.zeros(n, dtype=torch.int64, device="cuda")
+        L.mk_set_debug(self.ctx, L.MK_DBG_TIMING, 0, _ptr(self.timing), 8 * n, 0)
+
+    def phase_times_us(self) -> dict:
+        """Durations (us) of the last timed launch, summed over layers: per
+        phase the activation staging, the rest of the block's own work, and the
+        wait at the following grid barrier."""
+        t = self.timing.cpu().numpy().astype("float64")
+        Ln = self.shape.n_layers
+        names = ["qkv", "attention", "oproj", "route+gateup", "down"]
+        out = {k: {"stage": 0.0, "work": 0.0, "barrier": 0.0} for k in names}
+        prev = t[0]
+        for l in range(Ln):
+            for p, k in enumerate(names):
+                st, end, rel = t[1 + 16 * l + 3 * p: 4 + 16 * l + 3 * p]
+                if st == 0:
+                    st = prev
+                out[k]["stage"] += (st - prev) / 1e3
+                out[k]["work"] += (end - st) / 1e3
+                out[k]["barrier"] += (rel - end) / 1e3
+                prev = rel
+        out["lm_head"] = (t[1 + 16 * Ln] - prev) / 1e3
+        out["total"] = (t[1 + 16 * Ln] - t[0]) / 1e3
+        return out
+
     def disable_trace(self):
         L.mk_set_debug(self.ctx, 0, 0, 0, 0, 0)
         self.trace = None
