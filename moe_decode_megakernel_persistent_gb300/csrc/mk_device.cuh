@@ -56,6 +56,15 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   }
 }
 
+// L2 warm-up of a byte range by the whole block: each thread requests every
+// kThreads-th 128-byte line (cheap to issue, no registers held).
+__device__ __forceinline__ void prefetch_l2_block(const void* p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p) & ~uintptr_t(127);
+  const uintptr_t e = reinterpret_cast<uintptr_t>(p) + bytes;
+  for (uintptr_t q = a + (uintptr_t)threadIdx.x * 128; q < e; q += (uintptr_t)kThreads * 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
+}
+
 __device__ __forceinline__ float bf16_to_f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 __device__ __forceinline__ uint16_t f_to_bf16(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
@@ -83,6 +92,37 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+// Transposing butterfly: reduce NV (a power of two <= 32) per-lane partial
+// values across the warp with NV - 1 + log2(32 / NV) shuffles instead of
+// 5 * NV.  Returns, in every lane, the full sum of value number
+// bitrev(lane mod NV) (bit-reversed over log2(NV) bits).
+template <int NV>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NV], int lane) {
+  static_assert(NV >= 1 && NV <= 32 && (NV & (NV - 1)) == 0, "power of two");
+  int m = 1;
+#pragma unroll
+  for (int h = NV / 2; h >= 1; h >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < h; ++j) {
+      const float keep = up ? v[j + h] : v[j];
+      const float send = up ? v[j] : v[j + h];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+    m <<= 1;
+  }
+#pragma unroll
+  for (int mm = NV; mm < 32; mm <<= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], mm);
+  return v[0];
+}
+
+template <int BITS>
+__device__ __forceinline__ constexpr int bitrev(int x) {
+  int r = 0;
+  for (int i = 0; i < BITS; ++i) r |= ((x >> i) & 1) << (BITS - 1 - i);
+  return r;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -487,13 +527,12 @@ __device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, bool 
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int it = tid + i * kThreads;
-      // int4 chunks span 8 consecutive lanes: keep the whole warp in the shuffles
+      // int4 chunks span 8 consecutive lanes, so the whole warp takes part in
+      // the shuffles; lanes past the end are predicated off (no continue: the
+      // loop stays unrolled and v[] stays in registers)
       const bool live = it < nrg * NF4;
-      if constexpr (WDT != WINT4) {
-        if (!live) continue;
-      } else {
-        if (__all_sync(0xffffffffu, !live)) continue;
-      }
+      const bool warp_live = WDT == WINT4 ? __any_sync(0xffffffffu, live) : live;
+      if (warp_live) {
       const int row = live ? it / NF4 : 0, f4 = live ? it % NF4 : 0;
       float4 y = v[i];
       if (norm && live) {
@@ -533,6 +572,7 @@ __device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, bool 
         // chunk c holds VPC values = VPC/4 float4; sub t of chunk c at (t*NCH + c)*16
         const int c = f4 / (Gv::VPC / 4), t = f4 % (Gv::VPC / 4);
         *reinterpret_cast<float4*>(base + (t * Gv::NCH + c) * 16) = y;
+      }
       }
     }
   }

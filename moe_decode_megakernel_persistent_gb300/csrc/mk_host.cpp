@@ -130,7 +130,6 @@ size_t carve_scratch(const mk_model_desc& d, int grid, int max_units, char* base
   s.q = (float*)take(sizeof(float) * kMaxBatch * QD);
   s.attn = (float*)take(sizeof(float) * kMaxBatch * QD);
   s.part = (float*)take(sizeof(float) * (size_t)max_units * GQA * (d.head_dim + 4));
-  s.rpart = (float*)take(sizeof(float) * (size_t)grid * kMaxBatch * d.n_experts);
   s.rlogit = (float*)take(sizeof(float) * kMaxBatch * d.n_experts);
   s.act = (float*)take(sizeof(float) * kMaxBatch * d.top_k * d.expert_ffn);
   s.dact = (float*)take(sizeof(float) * kMaxBatch * d.dense_ffn);
@@ -146,9 +145,13 @@ size_t carve_scratch(const mk_model_desc& d, int grid, int max_units, char* base
 // Split of the attention work: chunk length (a multiple of 16 positions)
 // chosen so that all (row, kv-head, chunk) units roughly fill the grid once.
 void attention_split(const mk_ctx* c, const int32_t* pos, int n, int* chunk, int* units) {
-  long long total = 0;
-  for (int i = 0; i < n; ++i) total += pos[i] + 1;
+  long long total = 0, longest = 0;
+  for (int i = 0; i < n; ++i) {
+    total += pos[i] + 1;
+    longest = std::max<long long>(longest, pos[i] + 1);
+  }
   long long ch = (c->d.n_kv_heads * total + c->grid - 1) / c->grid;
+  ch = std::max(ch, (longest + kMaxChunks - 1) / kMaxChunks);  // at most kMaxChunks chunks per row
   ch = std::max<long long>(16, (ch + 15) / 16 * 16);
   long long u = 0;
   for (int i = 0; i < n; ++i) u += c->d.n_kv_heads * ((pos[i] + 1 + ch - 1) / ch);
@@ -252,9 +255,13 @@ size_t host_carve_scratch(const mk_model_desc& d, int grid, int max_units, char*
 }
 
 void host_attention_split(int n_kv_heads, int grid, const int32_t* pos, int n, int* chunk, int* units) {
-  long long total = 0;
-  for (int i = 0; i < n; ++i) total += pos[i] + 1;
+  long long total = 0, longest = 0;
+  for (int i = 0; i < n; ++i) {
+    total += pos[i] + 1;
+    longest = std::max<long long>(longest, pos[i] + 1);
+  }
   long long ch = (n_kv_heads * total + grid - 1) / grid;
+  ch = std::max(ch, (longest + kMaxChunks - 1) / kMaxChunks);  // at most kMaxChunks chunks per row
   ch = std::max<long long>(16, (ch + 15) / 16 * 16);
   long long u = 0;
   for (int i = 0; i < n; ++i) u += n_kv_heads * ((pos[i] + 1 + ch - 1) / ch);

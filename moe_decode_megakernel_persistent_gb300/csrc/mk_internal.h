@@ -13,6 +13,7 @@ constexpr int kThreads = 512;        // threads per block (16 warps)
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxUpd = 64;          // block-table updates carried by one launch
 constexpr int kMaxRowsPerBlock = 32; // hidden rows owned by one block (hidden / grid)
+constexpr int kMaxChunks = 64;       // attention chunks per (row, kv head): one per lane-pair of a warp
 constexpr int kSmemBytes = 200 * 1024;  // dynamic shared memory per block
 
 // Linear-weight slots of a layer.
@@ -40,15 +41,14 @@ struct Scratch {
   float* q;          // [kMaxBatch][n_heads*hd] roped queries
   float* attn;       // [kMaxBatch][n_heads*hd] merged attention output
   float* part;       // [max_units][gqa][hd + 2] attention partials (m, l, o[hd])
-  float* rpart;      // [grid][kMaxBatch][E] router partial logits
-  float* rlogit;     // [kMaxBatch][E] reduced (un-normalised) router logits
+  float* rlogit;     // [kMaxBatch][E] router logits before the RMS scale (block partials summed)
   float* act;        // [kMaxBatch][top_k][Fe] expert activations
   float* dact;       // [kMaxBatch][Fd] dense-MLP activations
   float* amax_v;     // [grid][kMaxBatch] per-block best logit
   int32_t* amax_i;   // [grid][kMaxBatch] per-block best token
   int32_t* merge_cnt;   // [kMaxBatch][n_kv] attention merge arrivals
   uint32_t* sync;       // counters, one per 128-byte line: [0] barrier, [32] exit,
-                        // [64] router reduce, [96] argmax reduce
+                        // [96] argmax reduce
   int32_t* err;         // [0] status, [1] site, [2] detail
 };
 

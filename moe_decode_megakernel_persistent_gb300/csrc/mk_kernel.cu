@@ -124,13 +124,14 @@ struct Model {
             (const uint16_t*)Lw.s[m] + (size_t)row * (H / 64)};
   }
 
-  // --- L2 warm-up (thread 0): bytes a block reads in a later phase are
-  // requested from HBM early, so that phase's loads find them in L2.
+  // --- L2 warm-up (all threads of the block): bytes a block reads in a
+  // later phase are requested from HBM early, so that phase's loads find
+  // them in L2.
   __device__ static void prefetch_rows(const void* w, const void* s, size_t row0, int rows, int row_bytes,
                                        int scale_bytes) {
     if (rows <= 0) return;
-    prefetch_l2((const uint8_t*)w + row0 * row_bytes, rows * row_bytes);
-    if (WDT == WINT4) prefetch_l2((const uint8_t*)s + row0 * scale_bytes, rows * scale_bytes);
+    prefetch_l2_block((const uint8_t*)w + row0 * row_bytes, (size_t)rows * row_bytes);
+    if (WDT == WINT4) prefetch_l2_block((const uint8_t*)s + row0 * scale_bytes, (size_t)rows * scale_bytes);
   }
 
   // QKV rows and o_proj rows of layer l owned by this block.
@@ -174,7 +175,7 @@ struct Model {
         const int s0 = max(t0, pi * kPageTokens) % kPageTokens;
         const int s1 = (min(t1, (pi + 1) * kPageTokens) - 1) % kPageTokens + 1;
         for (int kv = 0; kv < 2; ++kv)
-          prefetch_l2(a.kv + Kv<S>::offset(l, a.n_pages, page, kv, g, s0), (s1 - s0) * HD * 2);
+          prefetch_l2_block(a.kv + Kv<S>::offset(l, a.n_pages, page, kv, g, s0), (size_t)(s1 - s0) * HD * 2);
       }
     }
   }
@@ -195,6 +196,8 @@ struct Model {
     if (l == 0 && c.bid == 0)
       for (int i = tid; i < a.n_upd; i += kThreads)
         a.block_table[a.upd[i].slot * a.max_pages_per_seq + a.upd[i].index] = a.upd[i].page;
+    if (c.bid == 0 && l >= a.n_dense)  // router logits are accumulated in P3
+      for (int i = tid; i < n * E; i += kThreads) a.sc.rlogit[i] = 0.f;
     {
       const void* nw = Lw.attn_norm;
       const void* embed = a.embed;
@@ -295,18 +298,23 @@ struct Model {
         for (int d = 0; d < DPL; ++d) o[i][d] = 0.f;
       }
       for (int tb = t0 + wid; tb < t1; tb += kWarps * TU) {
+        // TU positions per warp: all K/V loads issued before any is used;
+        // positions past the chunk are predicated off (no break: the loops
+        // stay fully unrolled and the arrays stay in registers)
         float kf[TU][DPL], vf[TU][DPL];
+        bool ok[TU];
 #pragma unroll
         for (int k = 0; k < TU; ++k) {
           const int t = tb + k * kWarps;
-          if (t >= t1) break;
-          const int pi = t / kPageTokens;
+          ok[k] = t < t1;
+          const int tt = ok[k] ? t : t0;
+          const int pi = tt / kPageTokens;
           int page = pi < a.max_pages_per_seq ? __ldcg(bt + pi) : -1;
           if (page < 0 || page >= a.n_pages) {
-            set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_PAGE, t);
+            set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_PAGE, tt);
             page = 0;
           }
-          const int slot = t % kPageTokens;
+          const int slot = tt % kPageTokens;
           const uint16_t* kp = a.kv + Kv<S>::offset(l, a.n_pages, page, 0, g, slot) + lane * DPL;
           const uint16_t* vp = a.kv + Kv<S>::offset(l, a.n_pages, page, 1, g, slot) + lane * DPL;
           if constexpr (DPL == 4) {
@@ -323,23 +331,47 @@ struct Model {
             vf[k][0] = bf16_to_f(vr & 0xffff); vf[k][1] = bf16_to_f(vr >> 16);
           }
         }
+        // scores of the TU positions for the GQA heads: lane partials, one
+        // transposing reduction for all of them, then broadcast back
+        constexpr int NV = TU * GQA;
+        constexpr int NB = NV == 32 ? 5 : NV == 16 ? 4 : NV == 8 ? 3 : NV == 4 ? 2 : NV == 2 ? 1 : 0;
+        float sv[NV];
 #pragma unroll
-        for (int k = 0; k < TU; ++k) {
-          if (tb + k * kWarps >= t1) break;
+        for (int k = 0; k < TU; ++k)
 #pragma unroll
           for (int i = 0; i < GQA; ++i) {
-            float sc = 0.f;
+            float acc = 0.f;
 #pragma unroll
-            for (int d = 0; d < DPL; ++d) sc = fmaf(q[i][d], kf[k][d], sc);
-            sc = warp_sum(sc);
-            const float mn = fmaxf(m[i], sc);
-            const float corr = expf(m[i] - mn);
-            const float p = expf(sc - mn);
-            lsum[i] = lsum[i] * corr + p;
-#pragma unroll
-            for (int d = 0; d < DPL; ++d) o[i][d] = fmaf(o[i][d], corr, p * vf[k][d]);
-            m[i] = mn;
+            for (int d = 0; d < DPL; ++d) acc = fmaf(q[i][d], kf[k][d], acc);
+            sv[k * GQA + i] = acc;
           }
+        const float mine = warp_reduce_scatter<NV>(sv, lane);
+        float sc[TU][GQA];
+#pragma unroll
+        for (int idx = 0; idx < NV; ++idx)
+          sc[idx / GQA][idx % GQA] = __shfl_sync(0xffffffffu, mine, bitrev<NB>(idx));
+        // one online-softmax update per head for the whole batch
+#pragma unroll
+        for (int i = 0; i < GQA; ++i) {
+          float mn = m[i];
+#pragma unroll
+          for (int k = 0; k < TU; ++k) mn = ok[k] ? fmaxf(mn, sc[k][i]) : mn;
+          const float corr = __expf(m[i] - mn);
+          float psum = 0.f, p[TU];
+#pragma unroll
+          for (int k = 0; k < TU; ++k) {
+            p[k] = ok[k] ? __expf(sc[k][i] - mn) : 0.f;
+            psum += p[k];
+          }
+          lsum[i] = fmaf(lsum[i], corr, psum);
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) {
+            float acc = o[i][d] * corr;
+#pragma unroll
+            for (int k = 0; k < TU; ++k) acc = fmaf(p[k], vf[k][d], acc);
+            o[i][d] = acc;
+          }
+          m[i] = mn;
         }
       }
 #pragma unroll
@@ -352,57 +384,88 @@ struct Model {
       __syncthreads();
       if (u >= a.max_units) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, u);
       float* pu = a.sc.part + (size_t)min(u, a.max_units - 1) * GQA * PR;
+      // factors exp(m_w - M) once per (warp, head), then a weighted sum per dim
+      float* fac = F.red;                 // [kWarps][GQA], then M[GQA]
+      float* Ms = F.red + kWarps * GQA;
+      if (tid < GQA) {
+        float M = -INFINITY;
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, comb[(w * GQA + tid) * (HD + 2)]);
+        Ms[tid] = M;
+      }
+      __syncthreads();
+      if (tid < kWarps * GQA) {
+        const int w = tid / GQA, i = tid % GQA;
+        const float mw = comb[(w * GQA + i) * (HD + 2)];
+        fac[tid] = mw == -INFINITY ? 0.f : __expf(mw - Ms[i]);
+      }
+      __syncthreads();
       for (int idx = tid; idx < GQA * HD; idx += kThreads) {
         const int i = idx / HD, d = idx % HD;
-        float M = -INFINITY;
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, comb[(w * GQA + i) * (HD + 2)]);
         float L = 0.f, O = 0.f;
+#pragma unroll
         for (int w = 0; w < kWarps; ++w) {
           const float* cw = comb + (w * GQA + i) * (HD + 2);
-          const float f = cw[0] == -INFINITY ? 0.f : expf(cw[0] - M);
-          L = fmaf(cw[1], f, L);
-          O = fmaf(cw[2 + d], f, O);
+          L = fmaf(cw[1], fac[w * GQA + i], L);
+          O = fmaf(cw[2 + d], fac[w * GQA + i], O);
         }
-        if (d == 0) { pu[i * PR] = M; pu[i * PR + 1] = L; }
+        if (d == 0) { pu[i * PR] = Ms[i]; pu[i * PR + 1] = L; }
         pu[i * PR + 4 + d] = O;
       }
       __syncthreads();
       if (tid == 0) {
-        __threadfence();
-        const int old = atomicAdd(a.sc.merge_cnt + b * NKV + g, 1);
+        // release this unit's partial, acquire the others' if it is the last
+        int old;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                     : "=r"(old) : "l"(a.sc.merge_cnt + b * NKV + g) : "memory");
         F.flag = old == nch - 1;
       }
       __syncthreads();
       if (F.flag) {  // last unit of (b, g): log-sum-exp merge of its chunks
-        __threadfence();
-        const float4* src = reinterpret_cast<const float4*>(
-            a.sc.part + (size_t)(F.unit_start[b] + g * nch) * GQA * PR);
-        float4* pm = reinterpret_cast<float4*>(c.act);   // [chunk][GQA][PR]
-        const int nv = nch * GQA * PR / 4;
-        // a chunk is at least ctx * n_kv_heads / grid positions, so a (row,
-        // kv head) has at most grid / n_kv_heads + 1 chunks; guard anyway
-        if (nv * 16 > kActBytes) {
+        if (nch > kMaxChunks || nch * GQA > kThreads) {
           if (tid == 0) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, nch);
           __syncthreads();
           continue;
         }
-        for (int v = tid; v < nv; v += kThreads) pm[v] = __ldcg(src + v);
+        const float* pb = a.sc.part + (size_t)(F.unit_start[b] + g * nch) * GQA * PR;
+        // one warp per head: M = max_c m_c, L = sum_c l_c exp(m_c - M), and the
+        // chunk factors exp(m_c - M) / L into shared memory
+        float* mfac = F.red;  // [nch][GQA]
+        if (wid < GQA) {
+          const int i = wid;
+          float mv[2], lv[2];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int cc = lane + 32 * r;
+            mv[r] = cc < nch ? __ldcg(pb + (cc * GQA + i) * PR) : -INFINITY;
+            lv[r] = cc < nch ? __ldcg(pb + (cc * GQA + i) * PR + 1) : 0.f;
+          }
+          const float M = warp_max(fmaxf(mv[0], mv[1]));
+          float f[2];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) f[r] = mv[r] == -INFINITY ? 0.f : __expf(mv[r] - M);
+          const float Linv = 1.f / warp_sum(fmaf(lv[0], f[0], lv[1] * f[1]));
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int cc = lane + 32 * r;
+            if (cc < nch) mfac[cc * GQA + i] = f[r] * Linv;
+          }
+        }
         __syncthreads();
-        const float* ps = reinterpret_cast<const float*>(pm);
+        // weighted sum of the chunk outputs, read from L2 eight chunks at a time
         for (int idx = tid; idx < GQA * HD; idx += kThreads) {
           const int i = idx / HD, d = idx % HD;
-          float M = -INFINITY;
-          for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, ps[(cc * GQA + i) * PR]);
-          float L = 0.f, O = 0.f;
-          for (int cc = 0; cc < nch; ++cc) {
-            const float* pc = ps + (cc * GQA + i) * PR;
-            const float f = expf(pc[0] - M);
-            L = fmaf(pc[1], f, L);
-            O = fmaf(pc[4 + d], f, O);
+          float O = 0.f;
+          for (int c0 = 0; c0 < nch; c0 += 8) {
+            float ov[8];
+#pragma unroll
+            for (int u2 = 0; u2 < 8; ++u2)
+              ov[u2] = c0 + u2 < nch ? __ldcg(pb + ((c0 + u2) * GQA + i) * PR + 4 + d) : 0.f;
+#pragma unroll
+            for (int u2 = 0; u2 < 8; ++u2)
+              if (c0 + u2 < nch) O = fmaf(ov[u2], mfac[(c0 + u2) * GQA + i], O);
           }
-          const float val = O / L;
-          a.sc.attn[b * QD + (g * GQA + i) * HD + d] = val;
-          if (c.tr_attn) c.tr_attn[((size_t)l * n + b) * QD + (g * GQA + i) * HD + d] = val;
+          a.sc.attn[b * QD + (g * GQA + i) * HD + d] = O;
+          if (c.tr_attn) c.tr_attn[((size_t)l * n + b) * QD + (g * GQA + i) * HD + d] = O;
         }
         if (tid == 0) a.sc.merge_cnt[b * NKV + g] = 0;
       }
@@ -456,44 +519,9 @@ struct Model {
       float s = 0.f;
       for (int t = 0; t < c.nr; ++t)
         s = fmaf(F.hs[b][t] * ld_aux<AUX>(Lw.ffn_norm, c.r0 + t), ld_aux<AUX>(Lw.router, e * H + c.r0 + t), s);
-      a.sc.rpart[((size_t)c.bid * kMaxBatch + b) * E + e] = s;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      F.flag = atomicAdd(a.sc.sync + 64, 1u) == (uint32_t)(c.G - 1);
-    }
-    __syncthreads();
-    if (F.flag) {
-      __threadfence();
-      const int P = n * E;
-      const int NS = max(1, kThreads / P);
-      for (int idx = tid; idx < P * NS; idx += kThreads) {
-        const int p = idx % P, sp = idx / P;
-        const int b = p / E, e = p % E;
-        int g0, g1;
-        split_range(c.G, NS, sp, g0, g1);
-        float s = 0.f;
-        for (int g = g0; g < g1; g += 8) {
-          float v[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            v[u] = g + u < g1 ? __ldcg(a.sc.rpart + ((size_t)(g + u) * kMaxBatch + b) * E + e) : 0.f;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) s += v[u];
-        }
-        if (NS == 1) a.sc.rlogit[b * E + e] = s;
-        else F.red[idx] = s;
-      }
-      if (NS > 1) {
-        __syncthreads();
-        for (int p = tid; p < P; p += kThreads) {
-          float s = 0.f;
-          for (int sp = 0; sp < NS; ++sp) s += F.red[sp * P + p];
-          a.sc.rlogit[p] = s;
-        }
-      }
-      if (tid == 0) a.sc.sync[64] = 0;
+      // every block adds its partial; after the grid barrier all blocks read
+      // the same totals (the order of the additions may differ run to run)
+      atomicAdd(a.sc.rlogit + b * E + e, s);
     }
   }
 
@@ -594,7 +622,6 @@ struct Model {
     }
     __syncthreads();
     MK_STAMP(c, l, 3, 0);
-    if (tid == 0) prefetch_ffn_and_next(l);
     if (!moe) return;
     for (int b = wid; b < n; b += kWarps) {
       const float r = F.rnorm[b];
@@ -622,7 +649,7 @@ struct Model {
     }
   }
 
-  // Thread 0 after routing: this block's gate/up and down rows of layer l,
+  // After routing (all threads): this block's gate/up and down rows of layer l,
   // then the attention weights and cached K/V of layer l + 1 (or the start of
   // its lm_head rows after the last layer).
   __device__ static void prefetch_ffn_and_next(int l) {
@@ -934,11 +961,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   }
   __syncthreads();
   const Ctx& c = F.ctx;
-  if (tid == 0) {
-    M::prefetch_attn_weights(0);
-    M::prefetch_kv(0);
-  }
-  __syncthreads();
 
   uint32_t nbar = 0;
   if (c.tm && tid == 0) c.tm[0] = globaltimer();
@@ -977,7 +999,6 @@ done:
     if (atomicAdd(a.sc.sync + 32, 1u) == (uint32_t)(c.G - 1)) {
       // every block has left its work: reset the launch-scoped counters
       a.sc.sync[0] = 0;
-      a.sc.sync[64] = 0;
       a.sc.sync[96] = 0;
       for (int i = 0; i < kMaxBatch * S::NKV; ++i) a.sc.merge_cnt[i] = 0;
       __threadfence();
