@@ -37,6 +37,7 @@ struct Ctx {
 
 struct Fixed {
   StepArgs args;   // copy of the launch arguments
+  LayerW lw;       // the current layer's weight pointers
   Ctx ctx;
   int tok[kMaxBatch];
   int topk_id[kMaxBatch][8];
@@ -47,6 +48,7 @@ struct Fixed {
   float best_v[kWarps][kMaxBatch];
   int best_i[kWarps][kMaxBatch];
   int unit_start[kMaxBatch + 1];
+  int upages[2][64];   // pool pages of this block's attention units (same for every layer)
   float rnorm[kMaxBatch];
   int16_t ue_expert[64], ue_start[64], ue_len[64];
   int16_t run_start[kMaxEnt], run_len[kMaxEnt], run_mat[kMaxEnt];
@@ -94,7 +96,7 @@ struct Model {
   using GS = Gemv<WDT, KSD>;
   static_assert(kMaxBatch * GH::ACT_BYTES <= kActBytes, "staging area holds a full batch");
   static_assert(kMaxBatch * GQ::ACT_BYTES <= kActBytes, "staging area holds a full batch");
-  static_assert(kWarps * GQA * (HD + 2) * 4 <= kActBytes, "attention combine buffer");
+  static_assert((kWarps * GQA * (HD + 2) + GQA * HD) * 4 <= kActBytes, "attention combine + query buffers");
   static_assert(TOPK <= 8 && E <= 64, "router tables");
 
 
@@ -137,7 +139,7 @@ struct Model {
   // QKV rows and o_proj rows of layer l owned by this block.
   __device__ static void prefetch_attn_weights(int l) {
     const Ctx& c = fixed().ctx;
-    const LayerW& Lw = fixed().args.layers[l];
+    const LayerW& Lw = fixed().args.layers[l];  // (a later layer: read from global)
     int p0, p1;
     split_range(NP, c.G, c.bid, p0, p1);
     // rows of consecutive tasks are consecutive within a head: merge them
@@ -191,7 +193,7 @@ struct Model {
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     (void)tid; (void)lane; (void)wid;
-    const LayerW& Lw = a.layers[l];
+    const LayerW& Lw = F.lw;
     const int n = c.n;
     if (l == 0 && c.bid == 0)
       for (int i = tid; i < a.n_upd; i += kThreads)
@@ -276,20 +278,53 @@ struct Model {
     (void)tid; (void)lane; (void)wid;
     const int n = c.n;
     float* comb = reinterpret_cast<float*>(c.act);  // [warp][GQA][HD + 2]
+    float* qs = comb + kWarps * GQA * (HD + 2);     // [GQA][HD] this unit's queries
     const float qscale = rsqrtf((float)HD);
-    for (int u = c.bid; u < a.n_units; u += c.G) {
+    if (l == 0) {
+      // the pool pages of this block's units, read once per launch (after the
+      // block table got this launch's new pages): every warp of every unit
+      // reading the table itself would queue on the same L2 lines
+      int k = 0;
+      for (int u = c.bid; u < a.n_units; u += c.G, ++k) {
+        int b, g, ci, nch;
+        unit_of(a, F.unit_start, u, n, b, g, ci, nch);
+        const int t0 = ci * a.chunk, t1 = min(a.pos[b] + 1, t0 + a.chunk);
+        const int p0 = t0 / kPageTokens, np = (t1 - 1) / kPageTokens - p0 + 1;
+        if (k >= 2 || np > 64) {
+          if (tid == 0) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, u);
+          continue;
+        }
+        for (int j = tid; j < np; j += kThreads) {
+          const int pi = p0 + j;
+          int page = pi < a.max_pages_per_seq ? __ldcg(a.block_table + a.slot[b] * a.max_pages_per_seq + pi) : -1;
+          if (page < 0 || page >= a.n_pages) {
+            set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_PAGE, pi);
+            page = 0;
+          }
+          F.upages[k][j] = page;
+        }
+      }
+      __syncthreads();
+    }
+    int k_unit = 0;
+    for (int u = c.bid; u < a.n_units; u += c.G, ++k_unit) {
       int b, g, ci, nch;
       unit_of(a, F.unit_start, u, n, b, g, ci, nch);
       const int ctx = a.pos[b] + 1;
       const int t0 = ci * a.chunk, t1 = min(ctx, t0 + a.chunk);
-      const int* bt = a.block_table + a.slot[b] * a.max_pages_per_seq;
+      const int pbase = t0 / kPageTokens;
+      const int* upg = F.upages[min(k_unit, 1)];
+      // this unit's queries into shared memory once (coalesced), not per warp
+      for (int v = tid; v < GQA * HD / 4; v += kThreads)
+        reinterpret_cast<float4*>(qs)[v] =
+            __ldcg(reinterpret_cast<const float4*>(a.sc.q + b * QD + g * GQA * HD) + v);
+      __syncthreads();
 
       float q[GQA][DPL];
 #pragma unroll
       for (int i = 0; i < GQA; ++i)
 #pragma unroll
-        for (int d = 0; d < DPL; ++d)
-          q[i][d] = __ldcg(a.sc.q + b * QD + (g * GQA + i) * HD + lane * DPL + d) * qscale;
+        for (int d = 0; d < DPL; ++d) q[i][d] = qs[i * HD + lane * DPL + d] * qscale;
       float m[GQA], lsum[GQA], o[GQA][DPL];
 #pragma unroll
       for (int i = 0; i < GQA; ++i) {
@@ -308,12 +343,7 @@ struct Model {
           const int t = tb + k * kWarps;
           ok[k] = t < t1;
           const int tt = ok[k] ? t : t0;
-          const int pi = tt / kPageTokens;
-          int page = pi < a.max_pages_per_seq ? __ldcg(bt + pi) : -1;
-          if (page < 0 || page >= a.n_pages) {
-            set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_PAGE, tt);
-            page = 0;
-          }
+          const int page = upg[tt / kPageTokens - pbase];
           const int slot = tt % kPageTokens;
           const uint16_t* kp = a.kv + Kv<S>::offset(l, a.n_pages, page, 0, g, slot) + lane * DPL;
           const uint16_t* vp = a.kv + Kv<S>::offset(l, a.n_pages, page, 1, g, slot) + lane * DPL;
@@ -485,7 +515,7 @@ struct Model {
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     (void)tid; (void)lane; (void)wid;
-    const LayerW& Lw = a.layers[l];
+    const LayerW& Lw = F.lw;
     const int n = c.n;
     {
       const float* at = a.sc.attn;
@@ -539,7 +569,7 @@ struct Model {
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     (void)tid; (void)lane; (void)wid;
-    const LayerW& Lw = a.layers[l];
+    const LayerW& Lw = F.lw;
     const bool moe = l >= a.n_dense;
     const int n = c.n;
     constexpr int EJ = (E + 31) / 32;
@@ -658,7 +688,7 @@ struct Model {
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     (void)tid; (void)lane; (void)wid;
-    const LayerW& Lw = a.layers[l];
+    const LayerW& Lw = F.lw;
     if (l >= a.n_dense) {
       int u0, u1;
       split_range(F.n_ue * FE, c.G, c.bid, u0, u1);
@@ -696,7 +726,7 @@ struct Model {
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     (void)tid; (void)lane; (void)wid;
-    const LayerW& Lw = a.layers[l];
+    const LayerW& Lw = F.lw;
     if (l >= a.n_dense) {
       int u0, u1;
       split_range(F.n_ue * FE, c.G, c.bid, u0, u1);
@@ -753,7 +783,7 @@ struct Model {
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     (void)tid; (void)lane; (void)wid;
-    const LayerW& Lw = a.layers[l];
+    const LayerW& Lw = F.lw;
     using GD = typename std::conditional<MOE, GE, GS>::type;
     const int n = c.n, nr = c.nr;
     const int nent = MOE ? n * TOPK : n * NSEG;
@@ -965,6 +995,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   uint32_t nbar = 0;
   if (c.tm && tid == 0) c.tm[0] = globaltimer();
   for (int l = 0; l < a.n_layers; ++l) {
+    {  // this layer's weight pointers into shared memory (read by every task)
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(a.layers + l);
+      uint32_t* dst = reinterpret_cast<uint32_t*>(&F.lw);
+      for (int i = tid; i < (int)(sizeof(LayerW) / 4); i += kThreads) dst[i] = __ldg(src + i);
+      __syncthreads();
+    }
     M::qkv(l);
     MK_STAMP(c, l, 0, 1);
     if (!grid_barrier(a, nbar)) goto done;
