@@ -108,6 +108,23 @@ def measured_traffic(workload: str):
     return traffic
 
 
+# ------------------------------------------------------------------ replicas
+
+def aggregate_over_ranks(ms: float, tokens: int, device):
+    """Replicas only: every rank decodes its own sequences, no data-path
+    collective.  The step time is the slowest rank's, the throughput all
+    ranks' tokens over it."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms, tokens
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    k = torch.tensor([tokens], dtype=torch.int64, device=device)
+    dist.all_reduce(k, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(k.item())
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -252,11 +269,7 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     clk = clocks.stop()
     eng.sync()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, total_tokens = aggregate_over_ranks(e0.elapsed_time(e1), K, dev)
     ms_per_step = ms / K
 
     # end to end through the public API with host buffers: each step copies
@@ -287,7 +300,7 @@ def run_ours(args, rank, world):
     traffic = measured_traffic(w.name)
     out = {
         "metric": METRIC,
-        "value": round(world * K / (ms / 1e3), 2),
+        "value": round(total_tokens / (ms / 1e3), 2),
         "unit": "tok/s",
         "n_gpus": world,
         "steps": K,

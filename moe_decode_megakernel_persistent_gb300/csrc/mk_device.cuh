@@ -192,20 +192,52 @@ __device__ __forceinline__ bool grid_barrier(const StepArgs& a, uint32_t& k) {
 // block in shared memory in the same chunk order, and each warp holds the
 // chunks of its lanes in registers, so a row costs one pass over its bytes.
 //
-// int4 weights: chunk = 32 codes.  The activation chunk is quantised to
-// int16 with its own scale (max |y| / 32767, relative error <= 1.5e-5 of the
-// chunk maximum); products are formed exactly with dp2a (two int16 x two
-// 4-bit codes per instruction) in int32, and each chunk's integer dot is
-// scaled to float32 (weight scale x activation scale) and accumulated in
-// float32.  bf16 / fp32 weights: chunk = 8 / 4 values, float32 activations,
-// float32 FMA.
+// int4 weights: chunk = 32 codes.  The activation chunk is held as 30-bit
+// fixed point (scale max|y| / 2^30, i.e. float32 precision), split into a
+// signed high half and an unsigned low half of 16 bits each; the products
+// with the 4-bit codes are formed exactly with dp2a (two halves x two codes
+// per instruction, two passes) in int32, combined as 65536 * high + low, and
+// each chunk's dot is scaled to float32 (weight scale x activation scale) and
+// accumulated in float32.  bf16 / fp32 weights: chunk = 8 / 4 values, float32
+// activations, float32 FMA.
+// Dot product of one 16-byte chunk of int4 codes (32 values) with a staged
+// activation chunk: pieces p[0..3] hold the high halves, p[4..7] the low
+// halves, each as (0,2) (4,6) (1,3) (5,7) pairs of every 8-value word.
+// Returns sum_k y_k * q_k in units of the activation scale (exact integer
+// parts, one float rounding at the end).
+__device__ __forceinline__ float int4_chunk_dot(const uint4 w4, const uint4* p, int ch, int cl) {
+  const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+  int ih = 0;
+  uint32_t il = 0;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t x = wv[t] ^ 0x88888888u;      // two's complement -> q + 8
+    const uint32_t be = x & 0x0F0F0F0Fu;          // codes of k+0, k+2, k+4, k+6
+    const uint32_t bo = (x >> 4) & 0x0F0F0F0Fu;   // codes of k+1, k+3, k+5, k+7
+    const uint32_t h[4] = {p[t].x, p[t].y, p[t].z, p[t].w};
+    const uint32_t lo[4] = {p[4 + t].x, p[4 + t].y, p[4 + t].z, p[4 + t].w};
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(ih) : "r"(h[0]), "r"(be));
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(ih) : "r"(h[1]), "r"(be));
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(ih) : "r"(h[2]), "r"(bo));
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(ih) : "r"(h[3]), "r"(bo));
+    asm("dp2a.lo.u32.u32 %0, %1, %2, %0;" : "+r"(il) : "r"(lo[0]), "r"(be));
+    asm("dp2a.hi.u32.u32 %0, %1, %2, %0;" : "+r"(il) : "r"(lo[1]), "r"(be));
+    asm("dp2a.lo.u32.u32 %0, %1, %2, %0;" : "+r"(il) : "r"(lo[2]), "r"(bo));
+    asm("dp2a.hi.u32.u32 %0, %1, %2, %0;" : "+r"(il) : "r"(lo[3]), "r"(bo));
+  }
+  // sum y (q + 8) - 8 sum y = sum y q, per half, exactly in int32
+  return fmaf((float)(ih - ch), 65536.f, (float)((int)il - cl));
+}
+
 template <int WDT, int K>
 struct Gemv {
   static constexpr int VPC = WDT == WINT4 ? 32 : (WDT == WBF16 ? 8 : 4);
   static constexpr int NCH = K / VPC;
   static constexpr int CPL = (NCH + 31) / 32;
-  static constexpr int SUBS = WDT == WINT4 ? 4 : VPC / 4;  // 16-byte pieces of a staged chunk
-  static constexpr int META = WDT == WINT4 ? 8 : 0;        // (scale, offset correction)
+  static constexpr int SUBS = WDT == WINT4 ? 8 : VPC / 4;  // 16-byte pieces of a staged chunk
+  // int4 chunk metadata: activation scale, 8 * sum of high halves, 8 * sum of
+  // low halves (the nibbles are read as q + 8), padding
+  static constexpr int META = WDT == WINT4 ? 16 : 0;
   static constexpr int ACT_BYTES = NCH * SUBS * 16 + NCH * META;
   static constexpr int ROW_BYTES = WDT == WINT4 ? K / 2 : (WDT == WBF16 ? 2 * K : 4 * K);
   static constexpr bool PIPE = CPL <= 2;  // registers allow loading the next task early
@@ -220,7 +252,7 @@ struct Gemv {
   struct Act {
     uint4 v[AR][SUBS];
     float s[AR];
-    int corr[AR];
+    int ch[AR], cl[AR];
     const uint8_t* base;
   };
   struct Row {
@@ -251,9 +283,10 @@ struct Gemv {
           for (int t = 0; t < SUBS; ++t)
             a.v[j][t] = *reinterpret_cast<const uint4*>(base + (t * NCH + c) * 16);
           if constexpr (WDT == WINT4) {
-            const int2 m = *reinterpret_cast<const int2*>(base + NCH * SUBS * 16 + c * 8);
+            const int4 m = *reinterpret_cast<const int4*>(base + NCH * SUBS * 16 + c * 16);
             a.s[j] = __int_as_float(m.x);
-            a.corr[j] = m.y;
+            a.ch[j] = m.y;
+            a.cl[j] = m.z;
           }
         }
       }
@@ -273,23 +306,7 @@ struct Gemv {
       const int c = lane + 32 * j;
       if (NCH % 32 == 0 || c < NCH) {
         if constexpr (WDT == WINT4) {
-          const uint32_t wv[4] = {r.w[j].x, r.w[j].y, r.w[j].z, r.w[j].w};
-          const uint32_t av[16] = {a.v[j][0].x, a.v[j][0].y, a.v[j][0].z, a.v[j][0].w,
-                                   a.v[j][1].x, a.v[j][1].y, a.v[j][1].z, a.v[j][1].w,
-                                   a.v[j][2].x, a.v[j][2].y, a.v[j][2].z, a.v[j][2].w,
-                                   a.v[j][3].x, a.v[j][3].y, a.v[j][3].z, a.v[j][3].w};
-          int ia = 0;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const uint32_t x = wv[t] ^ 0x88888888u;          // two's complement -> q + 8
-            const uint32_t be = x & 0x0F0F0F0Fu;              // codes of k+0, k+2, k+4, k+6
-            const uint32_t bo = (x >> 4) & 0x0F0F0F0Fu;       // codes of k+1, k+3, k+5, k+7
-            asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(ia) : "r"(av[4 * t + 0]), "r"(be));
-            asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(ia) : "r"(av[4 * t + 1]), "r"(be));
-            asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(ia) : "r"(av[4 * t + 2]), "r"(bo));
-            asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(ia) : "r"(av[4 * t + 3]), "r"(bo));
-          }
-          acc = fmaf((float)(ia - a.corr[j]), a.s[j] * r.s[j], acc);
+          acc = fmaf(int4_chunk_dot(r.w[j], a.v[j], a.ch[j], a.cl[j]), a.s[j] * r.s[j], acc);
         } else if constexpr (WDT == WBF16) {
           const uint32_t wv[4] = {r.w[j].x, r.w[j].y, r.w[j].z, r.w[j].w};
           const uint4 a0 = act_piece(a, j, 0, c), a1 = act_piece(a, j, 1, c);
@@ -323,32 +340,13 @@ struct Gemv {
       const int c = lane + 32 * j;
       if (NCH % 32 == 0 || c < NCH) {
         if constexpr (WDT == WINT4) {
-          uint4 p[4];
+          uint4 p[8];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) p[t] = *reinterpret_cast<const uint4*>(base + (t * NCH + c) * 16);
-          const int2 m = *reinterpret_cast<const int2*>(base + NCH * SUBS * 16 + c * 8);
-          const uint32_t av[16] = {p[0].x, p[0].y, p[0].z, p[0].w, p[1].x, p[1].y, p[1].z, p[1].w,
-                                   p[2].x, p[2].y, p[2].z, p[2].w, p[3].x, p[3].y, p[3].z, p[3].w};
-          const uint32_t w0[4] = {r0.w[j].x, r0.w[j].y, r0.w[j].z, r0.w[j].w};
-          const uint32_t w1[4] = {r1.w[j].x, r1.w[j].y, r1.w[j].z, r1.w[j].w};
-          int i0 = 0, i1 = 0;
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const uint32_t x0 = w0[t] ^ 0x88888888u, x1 = w1[t] ^ 0x88888888u;
-            const uint32_t be0 = x0 & 0x0F0F0F0Fu, bo0 = (x0 >> 4) & 0x0F0F0F0Fu;
-            const uint32_t be1 = x1 & 0x0F0F0F0Fu, bo1 = (x1 >> 4) & 0x0F0F0F0Fu;
-            asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(i0) : "r"(av[4 * t + 0]), "r"(be0));
-            asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(i0) : "r"(av[4 * t + 1]), "r"(be0));
-            asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(i0) : "r"(av[4 * t + 2]), "r"(bo0));
-            asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(i0) : "r"(av[4 * t + 3]), "r"(bo0));
-            asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(i1) : "r"(av[4 * t + 0]), "r"(be1));
-            asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(i1) : "r"(av[4 * t + 1]), "r"(be1));
-            asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(i1) : "r"(av[4 * t + 2]), "r"(bo1));
-            asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(i1) : "r"(av[4 * t + 3]), "r"(bo1));
-          }
+          for (int t = 0; t < 8; ++t) p[t] = *reinterpret_cast<const uint4*>(base + (t * NCH + c) * 16);
+          const int4 m = *reinterpret_cast<const int4*>(base + NCH * SUBS * 16 + c * 16);
           const float sa = __int_as_float(m.x);
-          acc0 = fmaf((float)(i0 - m.y), sa * r0.s[j], acc0);
-          acc1 = fmaf((float)(i1 - m.y), sa * r1.s[j], acc1);
+          acc0 = fmaf(int4_chunk_dot(r0.w[j], p, m.y, m.z), sa * r0.s[j], acc0);
+          acc1 = fmaf(int4_chunk_dot(r1.w[j], p, m.y, m.z), sa * r1.s[j], acc1);
         } else {
 #pragma unroll
           for (int t = 0; t < SUBS; ++t) {
@@ -384,89 +382,6 @@ struct Gemv {
     v1 = warp_sum(acc1);
   }
 
-  // Write one chunk of activation values into its staged form at `dst`.
-  __device__ static __forceinline__ void store_chunk(uint8_t* dst, int c, const float* y) {
-    if constexpr (WDT == WINT4) {
-      float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(y[i]));
-      const float inv = amax > 0.f ? 32767.f / amax : 0.f;
-      int sum = 0;
-      // dp2a operand order per 8-value word t: (0,2) (4,6) (1,3) (5,7)
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        int v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          v[i] = __float2int_rn(y[8 * t + i] * inv);
-          sum += v[i];
-        }
-        *reinterpret_cast<uint4*>(dst + (t * NCH + c) * 16) =
-            make_uint4((uint32_t)(v[0] & 0xFFFF) | ((uint32_t)v[2] << 16),
-                       (uint32_t)(v[4] & 0xFFFF) | ((uint32_t)v[6] << 16),
-                       (uint32_t)(v[1] & 0xFFFF) | ((uint32_t)v[3] << 16),
-                       (uint32_t)(v[5] & 0xFFFF) | ((uint32_t)v[7] << 16));
-      }
-      *reinterpret_cast<int2*>(dst + NCH * SUBS * 16 + c * 8) =
-          make_int2(__float_as_int(amax / 32767.f), 8 * sum);
-    } else {
-#pragma unroll
-      for (int t = 0; t < SUBS; ++t)
-        *reinterpret_cast<float4*>(dst + (t * NCH + c) * 16) =
-            make_float4(y[4 * t], y[4 * t + 1], y[4 * t + 2], y[4 * t + 3]);
-    }
-  }
-
-  // Stage y[k] = f(k) (k < K) into shared memory at `dst` (one warp).  All
-  // of a lane's loads are issued before any is consumed.
-  template <class F>
-  __device__ static __forceinline__ void stage(uint8_t* dst, int lane, F f) {
-    float y[CPL][VPC];
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      const int c = lane + 32 * j;
-      if (NCH % 32 == 0 || c < NCH) {
-#pragma unroll
-        for (int i = 0; i < VPC; ++i) y[j][i] = f(c * VPC + i);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      const int c = lane + 32 * j;
-      if (NCH % 32 == 0 || c < NCH) store_chunk(dst, c, y[j]);
-    }
-  }
-
-  // Stage the RMS-normalised vector y[k] = x[k] / sqrt(mean(x^2) + eps) * w[k]
-  // (one warp): x is read once into registers, its sum of squares reduced
-  // across the warp, then scaled, weighted and stored.
-  template <class LX, class LW>
-  __device__ static __forceinline__ float stage_rms(uint8_t* dst, int lane, float eps, LX x, LW w) {
-    float y[CPL][VPC];
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      const int c = lane + 32 * j;
-      if (NCH % 32 == 0 || c < NCH) {
-#pragma unroll
-        for (int i = 0; i < VPC; ++i) {
-          y[j][i] = x(c * VPC + i);
-          ss = fmaf(y[j][i], y[j][i], ss);
-        }
-      }
-    }
-    const float r = rsqrtf(warp_sum(ss) / K + eps);
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      const int c = lane + 32 * j;
-      if (NCH % 32 == 0 || c < NCH) {
-#pragma unroll
-        for (int i = 0; i < VPC; ++i) y[j][i] = y[j][i] * r * w(c * VPC + i);
-        store_chunk(dst, c, y[j]);
-      }
-    }
-    return r;
-  }
 };
 
 // Block-cooperative staging of `rows` activation vectors of K floats into the
@@ -548,25 +463,36 @@ __device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, bool 
         float amax = live ? fmaxf(fmaxf(fabsf(y.x), fabsf(y.y)), fmaxf(fabsf(y.z), fabsf(y.w))) : 0.f;
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float inv = amax > 0.f ? 32767.f / amax : 0.f;
+        // 30-bit fixed point: |q| <= 2^30, split q = 65536 * hi + lo
+        const float inv = amax > 0.f ? 1073741824.f / amax : 0.f;
         const int q0 = __float2int_rn(y.x * inv), q1 = __float2int_rn(y.y * inv);
         const int q2 = __float2int_rn(y.z * inv), q3 = __float2int_rn(y.w * inv);
-        int sum = q0 + q1 + q2 + q3;
+        const int h0 = q0 >> 16, h1 = q1 >> 16, h2 = q2 >> 16, h3 = q3 >> 16;
+        const int l0 = q0 & 0xFFFF, l1 = q1 & 0xFFFF, l2 = q2 & 0xFFFF, l3 = q3 & 0xFFFF;
+        int sh = h0 + h1 + h2 + h3, sl = l0 + l1 + l2 + l3;
 #pragma unroll
-        for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        for (int o = 1; o < 8; o <<= 1) {
+          sh += __shfl_xor_sync(0xffffffffu, sh, o);
+          sl += __shfl_xor_sync(0xffffffffu, sl, o);
+        }
         // word group t = (f4 % 8) / 2 holds values 8t .. 8t+7 of the chunk:
         // dp2a operand order (0,2) (4,6) (1,3) (5,7); the even lane of the
         // pair holds values 0-3, the odd lane 4-7
-        const uint32_t pa = (uint32_t)(q0 & 0xFFFF) | ((uint32_t)q2 << 16);
-        const uint32_t pb = (uint32_t)(q1 & 0xFFFF) | ((uint32_t)q3 << 16);
-        const uint32_t oa = __shfl_xor_sync(0xffffffffu, pa, 1);
-        const uint32_t ob = __shfl_xor_sync(0xffffffffu, pb, 1);
+        const uint32_t ha = (uint32_t)(h0 & 0xFFFF) | ((uint32_t)h2 << 16);
+        const uint32_t hb = (uint32_t)(h1 & 0xFFFF) | ((uint32_t)h3 << 16);
+        const uint32_t la = (uint32_t)l0 | ((uint32_t)l2 << 16);
+        const uint32_t lb = (uint32_t)l1 | ((uint32_t)l3 << 16);
+        const uint32_t oha = __shfl_xor_sync(0xffffffffu, ha, 1);
+        const uint32_t ohb = __shfl_xor_sync(0xffffffffu, hb, 1);
+        const uint32_t ola = __shfl_xor_sync(0xffffffffu, la, 1);
+        const uint32_t olb = __shfl_xor_sync(0xffffffffu, lb, 1);
         const int c = f4 >> 3, t = (f4 & 7) >> 1;
         if (live && (f4 & 1) == 0) {
-          *reinterpret_cast<uint4*>(base + (t * Gv::NCH + c) * 16) = make_uint4(pa, oa, pb, ob);
+          *reinterpret_cast<uint4*>(base + (t * Gv::NCH + c) * 16) = make_uint4(ha, oha, hb, ohb);
+          *reinterpret_cast<uint4*>(base + ((4 + t) * Gv::NCH + c) * 16) = make_uint4(la, ola, lb, olb);
           if (t == 0)
-            *reinterpret_cast<int2*>(base + Gv::NCH * Gv::SUBS * 16 + c * 8) =
-                make_int2(__float_as_int(amax / 32767.f), 8 * sum);
+            *reinterpret_cast<int4*>(base + Gv::NCH * Gv::SUBS * 16 + c * 16) =
+                make_int4(__float_as_int(amax * 9.3132257461547852e-10f), 8 * sh, 8 * sl, 0);
         }
       } else {
         // chunk c holds VPC values = VPC/4 float4; sub t of chunk c at (t*NCH + c)*16
