@@ -309,7 +309,7 @@ def run_ours(args, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "int4 weights x int16 activations (dp2a), fp32 accumulate" if m.wdtype == "int4"
+        "dtype": "int4 weights x 24-bit fixed-point activations (dp4a), fp32 accumulate" if m.wdtype == "int4"
                  else f"{m.wdtype} weights, fp32 activations and accumulate",
         "data": "synthetic: seeded N(0,0.02) weights, seeded uniform prompt tokens",
         "config": {"workload": f"{w.name}: Flint-shaped MoE (49 layers, hidden 2048, 64 experts top-6, "

@@ -1,5 +1,6 @@
 // Device building blocks of the decode megakernel: memory access helpers,
-// the grid barrier, activation staging and the warp-level GEMV engine.
+// the grid barrier, the shared-memory weight ring (mbarriers + bulk copies),
+// activation staging and the warp-level GEMV engine.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -23,46 +24,20 @@ struct ShapeTiny {
 };
 
 // ------------------------------------------------------------------ memory
-__device__ __forceinline__ uint4 ld_weight16(const void* p) {
-  // weights are read-only for the launch and read once: no L1 allocation
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint4 lds128(const void* p) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+               : "r"(smem_u32(p)));
   return v;
 }
-__device__ __forceinline__ uint16_t ld_weight2(const void* p) {
+__device__ __forceinline__ uint32_t lds16(const void* p) {
   uint16_t v;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(smem_u32(p)));
   return v;
-}
-// Data written by other blocks during the launch: read at L2, never from a
-// (non-coherent) L1 line.
-__device__ __forceinline__ float ld_shared_f(const float* p) { return __ldcg(p); }
-__device__ __forceinline__ float4 ld_shared_f4(const float* p) {
-  return __ldcg(reinterpret_cast<const float4*>(p));
-}
-__device__ __forceinline__ int ld_shared_i(const int* p) { return __ldcg(p); }
-
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  // bulk L2 prefetch (TMA unit); addresses and sizes rounded to 16 bytes
-  uintptr_t a = reinterpret_cast<uintptr_t>(p) & ~uintptr_t(15);
-  uintptr_t e = (reinterpret_cast<uintptr_t>(p) + bytes + 15) & ~uintptr_t(15);
-  while (a < e) {
-    const uintptr_t left = e - a;
-    uint32_t n = (uint32_t)(left < 32768 ? left : 32768);
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(n) : "memory");
-    a += n;
-  }
-}
-
-// L2 warm-up of a byte range by the whole block: each thread requests every
-// kThreads-th 128-byte line (cheap to issue, no registers held).
-__device__ __forceinline__ void prefetch_l2_block(const void* p, size_t bytes) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p) & ~uintptr_t(127);
-  const uintptr_t e = reinterpret_cast<uintptr_t>(p) + bytes;
-  for (uintptr_t q = a + (uintptr_t)threadIdx.x * 128; q < e; q += (uintptr_t)kThreads * 128)
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
 }
 
 __device__ __forceinline__ float bf16_to_f(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
@@ -142,25 +117,26 @@ __device__ __forceinline__ void set_error(int32_t* err, int code, int site, int 
   }
 }
 
+// Barrier among the compute warps only (the streaming warp never joins).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
 // ------------------------------------------------------------------ grid barrier
 // One monotonically increasing arrival counter per launch: barrier k of the
 // launch completes when the counter reaches k * gridDim.x.  The arrive is a
-// release reduction, the wait an acquire load, so every write before the
+// release reduction (cumulative over the block's writes ordered before it by
+// the block barrier), the wait an acquire load, so every write before the
 // barrier is visible to every block after it.  The wait is bounded: it gives
 // up when another block has recorded an error, or after spin_limit_ns, and
 // then records MK_ERR_BARRIER_TIMEOUT; the caller skips to the exit path.
-__device__ __forceinline__ bool grid_barrier(const StepArgs& a, uint32_t& k) {
-  __shared__ int s_ok;
-  __syncthreads();
+// `ok` is a shared-memory word used to broadcast the outcome.
+__device__ __forceinline__ bool grid_barrier(const StepArgs& a, uint32_t& k, volatile int* ok_word) {
+  csync();
   if (threadIdx.x == 0) {
     ++k;
     uint32_t* ctr = a.sc.sync;
     bool skip = (a.dbg_flags & MK_DBG_SKIP_ARRIVAL) && (a.dbg_arg >> 16) == k &&
                 (a.dbg_arg & 0xffffu) == blockIdx.x;
-    if (!skip) {
-      __threadfence();
-      asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(1u) : "memory");
-    }
+    if (!skip) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(1u) : "memory");
     const uint32_t target = k * gridDim.x;
     int ok = 1;
     uint64_t t0 = 0;
@@ -179,54 +155,119 @@ __device__ __forceinline__ bool grid_barrier(const StepArgs& a, uint32_t& k) {
         }
       }
     }
-    s_ok = ok;
+    *ok_word = ok;
   }
-  __syncthreads();
-  return s_ok != 0;
+  csync();
+  return *ok_word != 0;
+}
+
+// ------------------------------------------------------------------ weight ring
+// Shared-memory stages filled by bulk copies (cp.async.bulk, the TMA unit)
+// and tracked by mbarriers: full[s] completes when the bytes of stage s have
+// landed (one arrival by the streaming warp plus the copies' transaction
+// bytes), empty[s] when all compute warps have released it.  Item k of the
+// launch's stream uses stage k % NS in round k / NS; the parity of the round
+// selects the mbarrier phase.
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the given phase parity: gives up (returns false) when
+// `abort` is set, an error is recorded, or after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, const volatile int* abort,
+                                          int32_t* err, uint64_t limit_ns, int site_detail) {
+  if (mbar_try(b, parity)) return true;
+  uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(b, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (*abort || *(volatile int32_t*)err != 0) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        set_error(err, MK_ERR_BARRIER_TIMEOUT, SITE_RING, site_detail);
+        return false;
+      }
+    }
+  }
+}
+// Bounded wait that ignores abort and errors: used on the exit path, where
+// copies still in flight into shared memory must land before the block ends.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* b, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try(b, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(b, parity)) return true;
+    if ((i & 15u) == 0 && globaltimer() - t0 > limit_ns) return false;
+  }
+}
+// Global -> shared bulk copy completing on mbarrier `b` (addresses and size
+// multiples of 16 bytes).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(b))
+      : "memory");
 }
 
 // ------------------------------------------------------------------ GEMV engine
 // A row of K weights is read as 16-byte chunks; lane l of a warp owns chunks
-// l, l+32, l+64, ...  (coalesced: each warp load instruction reads 512
-// contiguous bytes of the row).  The activation vector is staged once per
-// block in shared memory in the same chunk order, and each warp holds the
-// chunks of its lanes in registers, so a row costs one pass over its bytes.
+// l, l+32, l+64, ...  The rows come from the weight ring in shared memory; the
+// activation vector is staged once per block in shared memory in the same
+// chunk order, and (for short rows) each warp keeps the chunks of its lanes in
+// registers, so a row costs one pass over its bytes.
 //
-// int4 weights: chunk = 32 codes.  The activation chunk is held as 30-bit
-// fixed point (scale max|y| / 2^30, i.e. float32 precision), split into a
-// signed high half and an unsigned low half of 16 bits each; the products
-// with the 4-bit codes are formed exactly with dp2a (two halves x two codes
-// per instruction, two passes) in int32, combined as 65536 * high + low, and
-// each chunk's dot is scaled to float32 (weight scale x activation scale) and
-// accumulated in float32.  bf16 / fp32 weights: chunk = 8 / 4 values, float32
-// activations, float32 FMA.
-// Dot product of one 16-byte chunk of int4 codes (32 values) with a staged
-// activation chunk: pieces p[0..3] hold the high halves, p[4..7] the low
-// halves, each as (0,2) (4,6) (1,3) (5,7) pairs of every 8-value word.
-// Returns sum_k y_k * q_k in units of the activation scale (exact integer
-// parts, one float rounding at the end).
-__device__ __forceinline__ float int4_chunk_dot(const uint4 w4, const uint4* p, int ch, int cl) {
+// int4 weights: chunk = 32 codes.  The activation chunk is held as 24-bit
+// fixed point (scale max|y| / (2^23 - 1), float32 precision) in three byte
+// planes: low and middle bytes unsigned, high byte signed.  Each plane's dot
+// product with the codes is formed exactly with dp4a (four codes per
+// instruction, the codes read as q + 8 and corrected with the plane sum), the
+// planes combine as 65536 * high + 256 * middle + low, and each chunk's dot
+// is scaled to float32 (group scale x activation scale) and accumulated in
+// float32.  bf16 / fp32 weights: chunk = 8 / 4 values, float32 activations,
+// float32 FMA.
+//
+// Staged int4 chunk: six 16-byte pieces, piece 2p + e of plane p holds, in
+// word t, the plane's bytes of values 8t + {0, 2, 4, 6} (e = 0) or
+// 8t + {1, 3, 5, 7} (e = 1) -- the order in which a code word splits into
+// even and odd nibbles -- followed by {scale, 8 sum high, 8 sum middle,
+// 8 sum low}.
+__device__ __forceinline__ float int4_chunk_dot(const uint4 w4, const uint4 (&p)[6], const int4 m) {
   const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-  int ih = 0;
-  uint32_t il = 0;
+  const uint32_t p0[4] = {p[0].x, p[0].y, p[0].z, p[0].w}, p1[4] = {p[1].x, p[1].y, p[1].z, p[1].w};
+  const uint32_t p2[4] = {p[2].x, p[2].y, p[2].z, p[2].w}, p3[4] = {p[3].x, p[3].y, p[3].z, p[3].w};
+  const uint32_t p4[4] = {p[4].x, p[4].y, p[4].z, p[4].w}, p5[4] = {p[5].x, p[5].y, p[5].z, p[5].w};
+  uint32_t d0 = 0, d1 = 0;
+  int d2 = 0;
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     const uint32_t x = wv[t] ^ 0x88888888u;      // two's complement -> q + 8
-    const uint32_t be = x & 0x0F0F0F0Fu;          // codes of k+0, k+2, k+4, k+6
-    const uint32_t bo = (x >> 4) & 0x0F0F0F0Fu;   // codes of k+1, k+3, k+5, k+7
-    const uint32_t h[4] = {p[t].x, p[t].y, p[t].z, p[t].w};
-    const uint32_t lo[4] = {p[4 + t].x, p[4 + t].y, p[4 + t].z, p[4 + t].w};
-    asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(ih) : "r"(h[0]), "r"(be));
-    asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(ih) : "r"(h[1]), "r"(be));
-    asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(ih) : "r"(h[2]), "r"(bo));
-    asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(ih) : "r"(h[3]), "r"(bo));
-    asm("dp2a.lo.u32.u32 %0, %1, %2, %0;" : "+r"(il) : "r"(lo[0]), "r"(be));
-    asm("dp2a.hi.u32.u32 %0, %1, %2, %0;" : "+r"(il) : "r"(lo[1]), "r"(be));
-    asm("dp2a.lo.u32.u32 %0, %1, %2, %0;" : "+r"(il) : "r"(lo[2]), "r"(bo));
-    asm("dp2a.hi.u32.u32 %0, %1, %2, %0;" : "+r"(il) : "r"(lo[3]), "r"(bo));
+    const uint32_t be = x & 0x0F0F0F0Fu;          // codes of values 8t + 0, 2, 4, 6
+    const uint32_t bo = (x >> 4) & 0x0F0F0F0Fu;   // codes of values 8t + 1, 3, 5, 7
+    asm("dp4a.u32.u32 %0, %1, %2, %0;" : "+r"(d0) : "r"(p0[t]), "r"(be));
+    asm("dp4a.u32.u32 %0, %1, %2, %0;" : "+r"(d0) : "r"(p1[t]), "r"(bo));
+    asm("dp4a.u32.u32 %0, %1, %2, %0;" : "+r"(d1) : "r"(p2[t]), "r"(be));
+    asm("dp4a.u32.u32 %0, %1, %2, %0;" : "+r"(d1) : "r"(p3[t]), "r"(bo));
+    asm("dp4a.s32.u32 %0, %1, %2, %0;" : "+r"(d2) : "r"(p4[t]), "r"(be));
+    asm("dp4a.s32.u32 %0, %1, %2, %0;" : "+r"(d2) : "r"(p5[t]), "r"(bo));
   }
-  // sum y (q + 8) - 8 sum y = sum y q, per half, exactly in int32
-  return fmaf((float)(ih - ch), 65536.f, (float)((int)il - cl));
+  // sum y (q + 8) - 8 sum y = sum y q per plane, exactly in int32
+  const int lowmid = ((int)d1 - m.z) * 256 + ((int)d0 - m.w);
+  return fmaf((float)(d2 - m.y), 65536.f, (float)lowmid);
 }
 
 template <int WDT, int K>
@@ -234,163 +275,122 @@ struct Gemv {
   static constexpr int VPC = WDT == WINT4 ? 32 : (WDT == WBF16 ? 8 : 4);
   static constexpr int NCH = K / VPC;
   static constexpr int CPL = (NCH + 31) / 32;
-  static constexpr int SUBS = WDT == WINT4 ? 8 : VPC / 4;  // 16-byte pieces of a staged chunk
-  // int4 chunk metadata: activation scale, 8 * sum of high halves, 8 * sum of
-  // low halves (the nibbles are read as q + 8), padding
+  static constexpr int SUBS = WDT == WINT4 ? 6 : VPC / 4;  // 16-byte pieces of a staged chunk
   static constexpr int META = WDT == WINT4 ? 16 : 0;
   static constexpr int ACT_BYTES = NCH * SUBS * 16 + NCH * META;
   static constexpr int ROW_BYTES = WDT == WINT4 ? K / 2 : (WDT == WBF16 ? 2 * K : 4 * K);
-  static constexpr bool PIPE = CPL <= 2;  // registers allow loading the next task early
-  // int4 (and short rows) keep the activation in registers; long bf16/fp32
-  // rows read the staged chunk from shared memory per row instead (2 bytes
-  // of shared memory per weight byte, well inside its bandwidth)
-  static constexpr bool ACT_REGS = WDT == WINT4 || CPL <= 2;
+  static constexpr int SCALE_BYTES = WDT == WINT4 ? K / 64 * 2 : 0;
+  // rows per aligned group: A rows of scales are a multiple of 16 bytes
+  static constexpr int A = SCALE_BYTES == 0 ? 1
+                         : (SCALE_BYTES % 16 == 0 ? 1 : (SCALE_BYTES % 8 == 0 ? 2 : (SCALE_BYTES % 4 == 0 ? 4 : 8)));
+  // short rows may keep the activation chunks in registers (worth it when a
+  // warp dots many rows with one activation); otherwise they are read from
+  // shared memory per chunk
+  static constexpr bool ACT_REGS = CPL <= 2;
   static constexpr int AR = ACT_REGS ? CPL : 1;
   static_assert(K % VPC == 0, "K must be a multiple of the chunk");
-  static_assert(ACT_BYTES % 16 == 0, "staged vectors stay 16-byte aligned");
+  static_assert(WDT != WINT4 || K % 64 == 0, "int4 rows are whole scale groups");
+  static_assert(ACT_BYTES % 16 == 0 && ROW_BYTES % 16 == 0, "16-byte aligned rows and vectors");
 
   struct Act {
     uint4 v[AR][SUBS];
-    float s[AR];
-    int ch[AR], cl[AR];
-    const uint8_t* base;
+    int4 m[AR];
   };
-  struct Row {
-    uint4 w[CPL];
-    float s[CPL];
-  };
-
-  __device__ static __forceinline__ void load_row(Row& r, const uint8_t* w, const uint16_t* s,
-                                                  int lane) {
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      const int c = lane + 32 * j;
-      if (NCH % 32 == 0 || c < NCH) {
-        r.w[j] = ld_weight16(w + 16 * c);
-        if constexpr (WDT == WINT4) r.s[j] = bf16_to_f(ld_weight2(s + (c >> 1)));
-      }
-    }
-  }
 
   __device__ static __forceinline__ void load_act(Act& a, const uint8_t* base, int lane) {
-    a.base = base;
     if constexpr (ACT_REGS) {
 #pragma unroll
       for (int j = 0; j < CPL; ++j) {
         const int c = lane + 32 * j;
         if (NCH % 32 == 0 || c < NCH) {
 #pragma unroll
-          for (int t = 0; t < SUBS; ++t)
-            a.v[j][t] = *reinterpret_cast<const uint4*>(base + (t * NCH + c) * 16);
+          for (int t = 0; t < SUBS; ++t) a.v[j][t] = lds128(base + (t * NCH + c) * 16);
           if constexpr (WDT == WINT4) {
-            const int4 m = *reinterpret_cast<const int4*>(base + NCH * SUBS * 16 + c * 16);
-            a.s[j] = __int_as_float(m.x);
-            a.ch[j] = m.y;
-            a.cl[j] = m.z;
+            const uint4 m = lds128(base + NCH * SUBS * 16 + c * 16);
+            a.m[j] = make_int4((int)m.x, (int)m.y, (int)m.z, (int)m.w);
           }
         }
       }
     }
   }
 
-  __device__ static __forceinline__ uint4 act_piece(const Act& a, int j, int t, int c) {
-    if constexpr (ACT_REGS) return a.v[j][t];
-    else return *reinterpret_cast<const uint4*>(a.base + (t * NCH + c) * 16);
+  // lane-partial dot product of one weight chunk (16 bytes, group scale sc)
+  // with an activation chunk (pieces p, int4 metadata m)
+  __device__ static __forceinline__ float chunk(const uint4 w, float sc, const uint4 (&p)[SUBS], const int4 m,
+                                                float acc) {
+    if constexpr (WDT == WINT4) {
+      return fmaf(int4_chunk_dot(w, p, m), __int_as_float(m.x) * sc, acc);
+    } else if constexpr (WDT == WBF16) {
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+      const float av[8] = {__uint_as_float(p[0].x), __uint_as_float(p[0].y), __uint_as_float(p[0].z),
+                           __uint_as_float(p[0].w), __uint_as_float(p[1].x), __uint_as_float(p[1].y),
+                           __uint_as_float(p[1].z), __uint_as_float(p[1].w)};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        acc = fmaf(__uint_as_float(wv[t] << 16), av[2 * t], acc);
+        acc = fmaf(__uint_as_float(wv[t] & 0xFFFF0000u), av[2 * t + 1], acc);
+      }
+      return acc;
+    } else {
+      acc = fmaf(__uint_as_float(w.x), __uint_as_float(p[0].x), acc);
+      acc = fmaf(__uint_as_float(w.y), __uint_as_float(p[0].y), acc);
+      acc = fmaf(__uint_as_float(w.z), __uint_as_float(p[0].z), acc);
+      acc = fmaf(__uint_as_float(w.w), __uint_as_float(p[0].w), acc);
+      return acc;
+    }
   }
 
-  // lane-partial dot product (sum over the lane's chunks)
-  __device__ static __forceinline__ float dot(const Row& r, const Act& a, int lane) {
-    float acc = 0.f;
+  // Full dot products (warp-reduced, in every lane) of RP rows (codes at
+  // w[r], scales at s[r], shared memory) with one staged activation: from
+  // registers (REGS, after load_act) or read chunk by chunk from shared
+  // memory at `base`.  Each weight chunk is read where it is used.
+  template <int RP, bool REGS>
+  __device__ static __forceinline__ void dots(const uint8_t* const (&w)[2], const uint8_t* const (&s)[2],
+                                              const Act& a, const uint8_t* base, int lane, float& v0,
+                                              float& v1) {
+    static_assert(!REGS || ACT_REGS, "activation registers only for short rows");
+    float acc[2] = {0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < CPL; ++j) {
       const int c = lane + 32 * j;
       if (NCH % 32 == 0 || c < NCH) {
-        if constexpr (WDT == WINT4) {
-          acc = fmaf(int4_chunk_dot(r.w[j], a.v[j], a.ch[j], a.cl[j]), a.s[j] * r.s[j], acc);
-        } else if constexpr (WDT == WBF16) {
-          const uint32_t wv[4] = {r.w[j].x, r.w[j].y, r.w[j].z, r.w[j].w};
-          const uint4 a0 = act_piece(a, j, 0, c), a1 = act_piece(a, j, 1, c);
-          const float av[8] = {__uint_as_float(a0.x), __uint_as_float(a0.y), __uint_as_float(a0.z),
-                               __uint_as_float(a0.w), __uint_as_float(a1.x), __uint_as_float(a1.y),
-                               __uint_as_float(a1.z), __uint_as_float(a1.w)};
+        uint4 wv[2];
+        float sc[2] = {1.f, 1.f};
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            acc = fmaf(__uint_as_float(wv[t] << 16), av[2 * t], acc);
-            acc = fmaf(__uint_as_float(wv[t] & 0xFFFF0000u), av[2 * t + 1], acc);
-          }
+        for (int r = 0; r < RP; ++r) {
+          wv[r] = lds128(w[r] + 16 * c);
+          if constexpr (WDT == WINT4) sc[r] = bf16_to_f(lds16(s[r] + 2 * (c >> 1)));
+        }
+        if constexpr (REGS) {
+#pragma unroll
+          for (int r = 0; r < RP; ++r) acc[r] = chunk(wv[r], sc[r], a.v[j], a.m[j], acc[r]);
         } else {
-          const uint4 a0 = act_piece(a, j, 0, c);
-          acc = fmaf(__uint_as_float(r.w[j].x), __uint_as_float(a0.x), acc);
-          acc = fmaf(__uint_as_float(r.w[j].y), __uint_as_float(a0.y), acc);
-          acc = fmaf(__uint_as_float(r.w[j].z), __uint_as_float(a0.z), acc);
-          acc = fmaf(__uint_as_float(r.w[j].w), __uint_as_float(a0.w), acc);
+          uint4 p[SUBS];
+#pragma unroll
+          for (int t = 0; t < SUBS; ++t) p[t] = lds128(base + (t * NCH + c) * 16);
+          int4 m = make_int4(0, 0, 0, 0);
+          if constexpr (WDT == WINT4) {
+            const uint4 mm = lds128(base + NCH * SUBS * 16 + c * 16);
+            m = make_int4((int)mm.x, (int)mm.y, (int)mm.z, (int)mm.w);
+          }
+#pragma unroll
+          for (int r = 0; r < RP; ++r) acc[r] = chunk(wv[r], sc[r], p, m, acc[r]);
         }
       }
     }
-    return acc;
+    v0 = warp_sum(acc[0]);
+    v1 = RP > 1 ? warp_sum(acc[1]) : 0.f;
   }
-
-  // Dot products of two rows with one staged activation, the activation read
-  // chunk by chunk from shared memory (fewer live registers than load_act).
-  __device__ static __forceinline__ void dot2_smem(const Row& r0, const Row& r1, const uint8_t* base,
-                                                   int lane, float& v0, float& v1) {
-    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      const int c = lane + 32 * j;
-      if (NCH % 32 == 0 || c < NCH) {
-        if constexpr (WDT == WINT4) {
-          uint4 p[8];
-#pragma unroll
-          for (int t = 0; t < 8; ++t) p[t] = *reinterpret_cast<const uint4*>(base + (t * NCH + c) * 16);
-          const int4 m = *reinterpret_cast<const int4*>(base + NCH * SUBS * 16 + c * 16);
-          const float sa = __int_as_float(m.x);
-          acc0 = fmaf(int4_chunk_dot(r0.w[j], p, m.y, m.z), sa * r0.s[j], acc0);
-          acc1 = fmaf(int4_chunk_dot(r1.w[j], p, m.y, m.z), sa * r1.s[j], acc1);
-        } else {
-#pragma unroll
-          for (int t = 0; t < SUBS; ++t) {
-            const uint4 ap = *reinterpret_cast<const uint4*>(base + (t * NCH + c) * 16);
-            const float av[4] = {__uint_as_float(ap.x), __uint_as_float(ap.y), __uint_as_float(ap.z),
-                                 __uint_as_float(ap.w)};
-            if constexpr (WDT == WBF16) {
-              const uint32_t a0 = t == 0 ? r0.w[j].x : r0.w[j].z, b0 = t == 0 ? r0.w[j].y : r0.w[j].w;
-              const uint32_t a1 = t == 0 ? r1.w[j].x : r1.w[j].z, b1 = t == 0 ? r1.w[j].y : r1.w[j].w;
-              acc0 = fmaf(__uint_as_float(a0 << 16), av[0], acc0);
-              acc0 = fmaf(__uint_as_float(a0 & 0xFFFF0000u), av[1], acc0);
-              acc0 = fmaf(__uint_as_float(b0 << 16), av[2], acc0);
-              acc0 = fmaf(__uint_as_float(b0 & 0xFFFF0000u), av[3], acc0);
-              acc1 = fmaf(__uint_as_float(a1 << 16), av[0], acc1);
-              acc1 = fmaf(__uint_as_float(a1 & 0xFFFF0000u), av[1], acc1);
-              acc1 = fmaf(__uint_as_float(b1 << 16), av[2], acc1);
-              acc1 = fmaf(__uint_as_float(b1 & 0xFFFF0000u), av[3], acc1);
-            } else {
-              acc0 = fmaf(__uint_as_float(r0.w[j].x), av[0], acc0);
-              acc0 = fmaf(__uint_as_float(r0.w[j].y), av[1], acc0);
-              acc0 = fmaf(__uint_as_float(r0.w[j].z), av[2], acc0);
-              acc0 = fmaf(__uint_as_float(r0.w[j].w), av[3], acc0);
-              acc1 = fmaf(__uint_as_float(r1.w[j].x), av[0], acc1);
-              acc1 = fmaf(__uint_as_float(r1.w[j].y), av[1], acc1);
-              acc1 = fmaf(__uint_as_float(r1.w[j].z), av[2], acc1);
-              acc1 = fmaf(__uint_as_float(r1.w[j].w), av[3], acc1);
-            }
-          }
-        }
-      }
-    }
-    v0 = warp_sum(acc0);
-    v1 = warp_sum(acc1);
-  }
-
 };
 
-// Block-cooperative staging of `rows` activation vectors of K floats into the
-// staged form of Gemv<WDT, K> (vector r at dst + r * ACT_BYTES).  Thread t
-// loads float4 number t (coalesced: the block reads each vector as one
-// contiguous stream), optionally RMS-normalises the row (block reduction in a
-// fixed order, so every block gets the same scale) and multiplies by a
-// weight, then writes its part of the staged chunk; for int4 the 8 lanes
-// holding one 32-value chunk agree on its scale with shuffles.
+// Block-cooperative staging (the compute warps) of `rows` activation
+// vectors of K floats into the staged form of Gemv<WDT, K> (vector r at
+// dst + r * ACT_BYTES).  Thread t loads float4 number t (coalesced: the block
+// reads each vector as one contiguous stream), optionally RMS-normalises the
+// row (block reduction in a fixed order, so every block gets the same scale)
+// and multiplies by a weight, then writes its part of the staged chunk; for
+// int4 the 8 lanes holding one 32-value chunk agree on its scale and plane
+// sums with shuffles.
 //   LD(row, f4) -> float4 values 4*f4 .. 4*f4+3 of vector `row`
 //   WT(f4)      -> float4 weights (only with norm)
 //   red         -> shared scratch of kWarps * 4 floats
@@ -429,7 +429,7 @@ __device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, bool 
         ss[g] = warp_sum(ss[g]);
         if (lane == 0) red[wid * RG + g] = ss[g];
       }
-      __syncthreads();
+      csync();
 #pragma unroll
       for (int g = 0; g < RG; ++g) {
         float t = 0.f;
@@ -437,7 +437,7 @@ __device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, bool 
         rs[g] = rsqrtf(t / K + eps);
       }
       if (rscale && tid < nrg) rscale[r0 + tid] = rs[tid];
-      __syncthreads();
+      csync();
     }
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
@@ -448,137 +448,71 @@ __device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, bool 
       const bool live = it < nrg * NF4;
       const bool warp_live = WDT == WINT4 ? __any_sync(0xffffffffu, live) : live;
       if (warp_live) {
-      const int row = live ? it / NF4 : 0, f4 = live ? it % NF4 : 0;
-      float4 y = v[i];
-      if (norm && live) {
-        const float4 w = wt(f4);
-        float r = rs[0];
+        const int row = live ? it / NF4 : 0, f4 = live ? it % NF4 : 0;
+        float4 y = live ? v[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (norm && live) {
+          const float4 w = wt(f4);
+          float r = rs[0];
 #pragma unroll
-        for (int g = 1; g < RG; ++g) r = row == g ? rs[g] : r;
-        y = make_float4(y.x * r * w.x, y.y * r * w.y, y.z * r * w.z, y.w * r * w.w);
-      }
-      uint8_t* base = dst + (r0 + row) * Gv::ACT_BYTES;
-      if constexpr (WDT == WINT4) {
-        // chunk c = f4 / 8 (32 values) lives in lanes 8j .. 8j+7
-        float amax = live ? fmaxf(fmaxf(fabsf(y.x), fabsf(y.y)), fmaxf(fabsf(y.z), fabsf(y.w))) : 0.f;
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        // 30-bit fixed point: |q| <= 2^30, split q = 65536 * hi + lo
-        const float inv = amax > 0.f ? 1073741824.f / amax : 0.f;
-        const int q0 = __float2int_rn(y.x * inv), q1 = __float2int_rn(y.y * inv);
-        const int q2 = __float2int_rn(y.z * inv), q3 = __float2int_rn(y.w * inv);
-        const int h0 = q0 >> 16, h1 = q1 >> 16, h2 = q2 >> 16, h3 = q3 >> 16;
-        const int l0 = q0 & 0xFFFF, l1 = q1 & 0xFFFF, l2 = q2 & 0xFFFF, l3 = q3 & 0xFFFF;
-        int sh = h0 + h1 + h2 + h3, sl = l0 + l1 + l2 + l3;
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-          sh += __shfl_xor_sync(0xffffffffu, sh, o);
-          sl += __shfl_xor_sync(0xffffffffu, sl, o);
+          for (int g = 1; g < RG; ++g) r = row == g ? rs[g] : r;
+          y = make_float4(y.x * r * w.x, y.y * r * w.y, y.z * r * w.z, y.w * r * w.w);
         }
-        // word group t = (f4 % 8) / 2 holds values 8t .. 8t+7 of the chunk:
-        // dp2a operand order (0,2) (4,6) (1,3) (5,7); the even lane of the
-        // pair holds values 0-3, the odd lane 4-7
-        const uint32_t ha = (uint32_t)(h0 & 0xFFFF) | ((uint32_t)h2 << 16);
-        const uint32_t hb = (uint32_t)(h1 & 0xFFFF) | ((uint32_t)h3 << 16);
-        const uint32_t la = (uint32_t)l0 | ((uint32_t)l2 << 16);
-        const uint32_t lb = (uint32_t)l1 | ((uint32_t)l3 << 16);
-        const uint32_t oha = __shfl_xor_sync(0xffffffffu, ha, 1);
-        const uint32_t ohb = __shfl_xor_sync(0xffffffffu, hb, 1);
-        const uint32_t ola = __shfl_xor_sync(0xffffffffu, la, 1);
-        const uint32_t olb = __shfl_xor_sync(0xffffffffu, lb, 1);
-        const int c = f4 >> 3, t = (f4 & 7) >> 1;
-        if (live && (f4 & 1) == 0) {
-          *reinterpret_cast<uint4*>(base + (t * Gv::NCH + c) * 16) = make_uint4(ha, oha, hb, ohb);
-          *reinterpret_cast<uint4*>(base + ((4 + t) * Gv::NCH + c) * 16) = make_uint4(la, ola, lb, olb);
-          if (t == 0)
-            *reinterpret_cast<int4*>(base + Gv::NCH * Gv::SUBS * 16 + c * 16) =
-                make_int4(__float_as_int(amax * 9.3132257461547852e-10f), 8 * sh, 8 * sl, 0);
+        uint8_t* base = dst + (r0 + row) * Gv::ACT_BYTES;
+        if constexpr (WDT == WINT4) {
+          // chunk c = f4 / 8 (32 values) lives in lanes 8j .. 8j+7
+          float amax = fmaxf(fmaxf(fabsf(y.x), fabsf(y.y)), fmaxf(fabsf(y.z), fabsf(y.w)));
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          // 24-bit fixed point, |q| <= 2^23 - 1, split into byte planes
+          const float inv = amax > 0.f ? 8388607.f / amax : 0.f;
+          const float yv[4] = {y.x, y.y, y.z, y.w};
+          int q[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) q[e] = max(-8388607, min(8388607, __float2int_rn(yv[e] * inv)));
+          int s0 = 0, s1 = 0, s2 = 0;
+          uint32_t pk[3];  // per plane: bytes of values (0, 2) | (1, 3) << 16
+#pragma unroll
+          for (int pl = 0; pl < 3; ++pl) {
+            uint32_t b[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) b[e] = (uint32_t)(q[e] >> (8 * pl)) & 0xFFu;
+            pk[pl] = b[0] | (b[2] << 8) | (b[1] << 16) | (b[3] << 24);
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            s0 += q[e] & 0xFF;
+            s1 += (q[e] >> 8) & 0xFF;
+            s2 += q[e] >> 16;
+          }
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1) {
+            s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+          }
+          uint32_t opk[3];
+#pragma unroll
+          for (int pl = 0; pl < 3; ++pl) opk[pl] = __shfl_xor_sync(0xffffffffu, pk[pl], 1);
+          // word t = (f4 % 8) / 2 holds values 8t .. 8t+7 of the chunk: the
+          // even lane of the pair has values 0-3, the odd lane 4-7
+          const int c = f4 >> 3, t = (f4 & 7) >> 1;
+          if (live && (f4 & 1) == 0) {
+#pragma unroll
+            for (int pl = 0; pl < 3; ++pl) {
+              const uint32_t ev = (pk[pl] & 0xFFFFu) | (opk[pl] << 16);
+              const uint32_t od = (pk[pl] >> 16) | (opk[pl] & 0xFFFF0000u);
+              *reinterpret_cast<uint32_t*>(base + ((2 * pl) * Gv::NCH + c) * 16 + 4 * t) = ev;
+              *reinterpret_cast<uint32_t*>(base + ((2 * pl + 1) * Gv::NCH + c) * 16 + 4 * t) = od;
+            }
+            if (t == 0)
+              *reinterpret_cast<int4*>(base + Gv::NCH * Gv::SUBS * 16 + c * 16) =
+                  make_int4(__float_as_int(amax * (1.f / 8388607.f)), 8 * s2, 8 * s1, 8 * s0);
+          }
+        } else {
+          // chunk c holds VPC values = VPC/4 float4; sub t of chunk c at (t*NCH + c)*16
+          const int c = f4 / (Gv::VPC / 4), t = f4 % (Gv::VPC / 4);
+          if (live) *reinterpret_cast<float4*>(base + (t * Gv::NCH + c) * 16) = y;
         }
-      } else {
-        // chunk c holds VPC values = VPC/4 float4; sub t of chunk c at (t*NCH + c)*16
-        const int c = f4 / (Gv::VPC / 4), t = f4 % (Gv::VPC / 4);
-        *reinterpret_cast<float4*>(base + (t * Gv::NCH + c) * 16) = y;
-      }
-      }
-    }
-  }
-}
-
-// Block-level task runner.  Tasks t = warp, warp + 16, ... ; each task has RP
-// weight rows and a list of staged activations; the warp loads each row once
-// and forms its dot product with every activation of the task.  A task
-// object provides (all inlined, results returned by value):
-//   RowRef row(t, r)        row pointers of row r of task t
-//   ActRange acts(t)        activations: i-th is list ? list[start+i] : start+i
-//   void out(t, ai, i, v0, v1)  results for activation ai (i-th of the task), all lanes
-struct RowRef {
-  const uint8_t* w;
-  const uint16_t* s;
-};
-struct ActRange {
-  const uint8_t* list;
-  int start, count;
-};
-
-template <int WDT, int K, int RP, class T>
-__device__ __forceinline__ void run_tasks(int ntasks, const uint8_t* act_base, const T& task) {
-  using Gv = Gemv<WDT, K>;
-  const int lane = threadIdx.x & 31;
-  const int wid = threadIdx.x >> 5;
-  typename Gv::Act a;
-  int loaded = -1;
-  auto prefetch_rows_l2 = [&](int tf) {
-#pragma unroll
-    for (int r = 0; r < RP; ++r) {
-      const RowRef rr = task.row(tf, r);
-#pragma unroll
-      for (int j = 0; j < Gv::CPL; ++j) {
-        const int c = lane + 32 * j;
-        if (Gv::NCH % 32 == 0 || c < Gv::NCH) asm volatile("prefetch.global.L2 [%0];" ::"l"(rr.w + 16 * c));
-      }
-    }
-  };
-  if constexpr (Gv::PIPE && RP == 1) {
-    typename Gv::Row cur, nxt;
-    int t = wid;
-    if (t < ntasks) {
-      const RowRef rr = task.row(t, 0);
-      Gv::load_row(cur, rr.w, rr.s, lane);
-    }
-    for (; t < ntasks; t += kWarps) {
-      const int tn = t + kWarps;
-      if (tn < ntasks) {
-        const RowRef rr = task.row(tn, 0);
-        Gv::load_row(nxt, rr.w, rr.s, lane);
-      }
-      if (t + 4 * kWarps < ntasks) prefetch_rows_l2(t + 4 * kWarps);  // keep HBM busy further ahead
-      const ActRange ar = task.acts(t);
-      for (int i = 0; i < ar.count; ++i) {
-        const int ai = ar.list ? ar.list[ar.start + i] : ar.start + i;
-        if (ai != loaded) { Gv::load_act(a, act_base + ai * Gv::ACT_BYTES, lane); loaded = ai; }
-        const float v0 = warp_sum(Gv::dot(cur, a, lane));
-        task.out(t, ai, i, v0, 0.f);
-      }
-      cur = nxt;
-    }
-  } else {
-    // activations read from shared memory per chunk: no activation registers
-    // live across the task loop
-    typename Gv::Row row[2];
-    for (int t = wid; t < ntasks; t += kWarps) {
-      if (t + kWarps < ntasks) prefetch_rows_l2(t + kWarps);  // warm L2 for this warp's next task
-#pragma unroll
-      for (int r = 0; r < RP; ++r) {
-        const RowRef rr = task.row(t, r);
-        Gv::load_row(row[r], rr.w, rr.s, lane);
-      }
-      if (RP == 1) row[1] = row[0];
-      const ActRange ar = task.acts(t);
-      for (int i = 0; i < ar.count; ++i) {
-        const int ai = ar.list ? ar.list[ar.start + i] : ar.start + i;
-        float v0, v1;
-        Gv::dot2_smem(row[0], row[1], act_base + ai * Gv::ACT_BYTES, lane, v0, v1);
-        task.out(t, ai, i, v0, v1);
       }
     }
   }

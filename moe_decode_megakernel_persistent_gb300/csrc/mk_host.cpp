@@ -83,6 +83,8 @@ int validate_desc(const mk_model_desc* d, int* shape) {
   if (!d) return fail(MK_ERR_INVALID_ARG, "model description is NULL");
   if (d->n_layers < 1 || d->vocab < 1 || d->n_dense < 0 || d->n_dense > d->n_layers)
     return fail(MK_ERR_INVALID_ARG, "n_layers / vocab / n_dense out of range");
+  if (d->wdtype == MK_INT4_G64 && d->vocab % 8 != 0)
+    return fail(MK_ERR_UNSUPPORTED, "int4 lm_head needs a vocabulary that is a multiple of 8 rows");
   if (d->page_tokens != kPageTokens) return fail(MK_ERR_UNSUPPORTED, "page_tokens must be 128");
   if (d->max_batch < 1 || d->max_batch > kMaxBatch)
     return fail(MK_ERR_INVALID_ARG, "max_batch must be in [1, 16]");
@@ -199,6 +201,13 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
     a.pos[i] = p;
     a.cur_page[i] = q.pages[pi];
   }
+  // first position of each row's sequence that this launch writes: earlier
+  // positions are in the cache before the launch starts
+  for (int i = 0; i < n; ++i) {
+    a.new0[i] = a.pos[i];
+    for (int j = 0; j < n; ++j)
+      if (a.slot[j] == a.slot[i] && a.pos[j] < a.new0[i]) a.new0[i] = a.pos[j];
+  }
   attention_split(c, positions, n, &a.chunk, &a.n_units);
   if (a.n_units > c->max_units) {
     rollback();
@@ -232,7 +241,7 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
   // a skipped arrival is a one-shot request
   c->dbg_flags &= ~MK_DBG_SKIP_ARRIVAL;
   void* args[] = {&a};
-  cudaError_t e = cudaLaunchCooperativeKernel(c->kern.fn, dim3(c->grid), dim3(kThreads), args,
+  cudaError_t e = cudaLaunchCooperativeKernel(c->kern.fn, dim3(c->grid), dim3(kBlockThreads), args,
                                               (size_t)c->kern.smem_bytes, st);
   if (e != cudaSuccess) {
     rollback();
@@ -399,7 +408,7 @@ MK_API int mk_create(const mk_model_desc* d, const mk_weights* w, mk_ctx** out) 
     return fail(MK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
   }
   int nb = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, c->kern.fn, kThreads, c->kern.smem_bytes);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, c->kern.fn, kBlockThreads, c->kern.smem_bytes);
   if (e != cudaSuccess || nb < 1) {
     delete c;
     return fail(MK_ERR_UNSUPPORTED, "one block per SM cannot be resident (occupancy check)");
@@ -592,7 +601,7 @@ MK_API int mk_get_info(mk_ctx* c, mk_info* info) {
   info->device = c->device;
   info->num_sms = c->num_sms;
   info->grid = c->grid;
-  info->block_threads = kThreads;
+  info->block_threads = kBlockThreads;
   info->smem_bytes = c->kern.smem_bytes;
   info->n_pages = c->n_pages;
   info->free_pages = (int32_t)c->free_pages.size();

@@ -9,12 +9,17 @@ namespace mk {
 
 constexpr int kMaxBatch = 16;        // rows per launch
 constexpr int kPageTokens = 128;     // KV positions per page
-constexpr int kThreads = 512;        // threads per block (16 warps)
+// 15 compute warps + 1 weight-streaming warp: 16 warps keep 4 per scheduler
+// partition, so each thread may hold 128 registers (a 17th warp would cut
+// that to 96)
+constexpr int kThreads = 480;        // compute threads per block (15 warps)
 constexpr int kWarps = kThreads / 32;
+constexpr int kBlockThreads = kThreads + 32;  // plus one weight-streaming warp
+constexpr int kMaxStages = 16;       // shared-memory ring stages
 constexpr int kMaxUpd = 64;          // block-table updates carried by one launch
 constexpr int kMaxRowsPerBlock = 32; // hidden rows owned by one block (hidden / grid)
 constexpr int kMaxChunks = 64;       // attention chunks per (row, kv head): one per lane-pair of a warp
-constexpr int kSmemBytes = 200 * 1024;  // dynamic shared memory per block
+constexpr int kSmemBytes = 227 * 1024;  // dynamic shared memory per block (the sm_100 family maximum)
 
 // Linear-weight slots of a layer.
 enum Lin { WQ = 0, WK, WV, WO, GATE, UP, DOWN, EGATE, EUP, EDOWN, NLIN };
@@ -83,12 +88,13 @@ struct StepArgs {
   uint64_t spin_limit_ns;
   int32_t slot[kMaxBatch];
   int32_t pos[kMaxBatch];
+  int32_t new0[kMaxBatch];   // first position of the row's sequence written by this launch
   int32_t cur_page[kMaxBatch];
   PageUpd upd[kMaxUpd];
 };
 
 // Error sites recorded in err[1].
-enum ErrSite { SITE_BARRIER = 1, SITE_PAGE = 2, SITE_UNIT = 3, SITE_TOKEN = 4 };
+enum ErrSite { SITE_BARRIER = 1, SITE_PAGE = 2, SITE_UNIT = 3, SITE_TOKEN = 4, SITE_RING = 5, SITE_SMEM = 6 };
 
 // Kernel variants compiled into the library.
 enum ShapeId { SHAPE_FLINT = 0, SHAPE_TINY = 1, NSHAPE };

@@ -9,13 +9,23 @@
 //   P2  split attention: (row, kv head, chunk of positions) units, the last
 //       unit of a (row, kv head) merges all chunks (log-sum-exp)          | barrier
 //   P3  o_proj rows + residual; MoE layers also form this block's partial
-//       router logits, reduced by the last block to arrive                | barrier
+//       router logits                                                     | barrier
 //   P4  RMSNorm + softmax/top-k (every block), expert gate/up -> SiLU
 //       (dense layers: the SwiGLU gate/up)                                | barrier
 //   P5  down projection rows, weighted sum over the selected experts, residual
 //                                                                          | barrier
 // After the last layer: final RMSNorm, lm_head rows, per-block argmax, and
 // the last block to arrive reduces the argmax (no barrier needed).
+//
+// Data movement.  A block is 15 compute warps plus one streaming warp.  Every
+// weight row and every cached K/V row a block reads goes through a ring of
+// shared-memory stages filled by bulk copies (cp.async.bulk): the streaming
+// warp walks the block's whole schedule for the launch (layer by layer, phase
+// by phase, in the order the compute warps consume it) and issues each tile
+// as soon as a stage is free, so the next phase's weights are already in
+// shared memory when a grid barrier releases.  Only expert tiles wait, for
+// the layer's routing.  The compute warps wait on a stage's "full" mbarrier,
+// form their dot products from shared memory and release the stage.
 #include <cfloat>
 #include <climits>
 #include <type_traits>
@@ -23,12 +33,14 @@
 
 namespace mk {
 
-constexpr int kMaxEnt = kMaxBatch * 8; // (row, expert slot) entries
+constexpr int kMaxEnt = kMaxBatch * 8;  // (row, expert slot) entries
 
-// Per-launch, per-block context shared by the phases; it lives in shared
-// memory (inside Fixed) so the phases read it with shared-memory loads.
+// Per-launch, per-block context shared by the phases (in shared memory).
 struct Ctx {
-  uint8_t* act;    // staging area in shared memory
+  uint8_t* act;    // activation staging area
+  uint8_t* ring;   // weight ring stages
+  int ns;          // ring stages
+  int act_bytes;   // size of the staging area
   int G, bid, n;
   int r0, nr;      // hidden rows owned by this block
   float *tr_x, *tr_attn, *tr_rl, *tr_tk, *tr_fin;
@@ -39,6 +51,12 @@ struct Fixed {
   StepArgs args;   // copy of the launch arguments
   LayerW lw;       // the current layer's weight pointers
   Ctx ctx;
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint32_t kc;            // ring items consumed so far by the compute warps
+  volatile int route_gen; // l + 1 once layer l's routing tables are ready
+  volatile int abort;     // compute warps left the step early
+  volatile int ok_word;   // grid barrier outcome broadcast
   int tok[kMaxBatch];
   int topk_id[kMaxBatch][8];
   float topk_w[kMaxBatch][8];
@@ -48,16 +66,14 @@ struct Fixed {
   float best_v[kWarps][kMaxBatch];
   int best_i[kWarps][kMaxBatch];
   int unit_start[kMaxBatch + 1];
-  int upages[2][64];   // pool pages of this block's attention units (same for every layer)
+  int upages[2][64];      // pool pages of this block's attention units (streaming warp)
   float rnorm[kMaxBatch];
   int16_t ue_expert[64], ue_start[64], ue_len[64];
-  int16_t run_start[kMaxEnt], run_len[kMaxEnt], run_mat[kMaxEnt];
   uint8_t ent_b[kMaxEnt], ent_j[kMaxEnt];
   uint8_t ent_of[kMaxBatch][8];
-  int n_ue, n_runs, flag;
+  int n_ue, flag;
 };
 constexpr int kActOffset = (sizeof(Fixed) + 127) / 128 * 128;
-constexpr int kActBytes = kSmemBytes - kActOffset;
 
 __device__ __forceinline__ Fixed& fixed() {
   extern __shared__ __align__(128) uint8_t smem_dyn[];
@@ -81,28 +97,136 @@ struct Kv {
 #define MK_STAMP(c, l, p, k) \
   if ((c).tm && threadIdx.x == 0) (c).tm[1 + 16 * (l) + 3 * (p) + (k)] = globaltimer()
 
+// ---------------------------------------------------------------- ring, consumer side
+// Every compute thread calls acquire/release for every item, in order.
+template <int STAGE>
+__device__ __forceinline__ const uint8_t* ring_acquire(uint32_t k) {
+  Fixed& F = fixed();
+  const int s = (int)(k % (uint32_t)F.ctx.ns);
+  const uint32_t par = (k / (uint32_t)F.ctx.ns) & 1u;
+  mbar_wait(&F.full[s], par, &F.abort, F.args.sc.err, F.args.spin_limit_ns, (int)k);
+  return F.ctx.ring + (size_t)s * STAGE;
+}
+__device__ __forceinline__ void ring_release(uint32_t k) {
+  Fixed& F = fixed();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&F.empty[k % (uint32_t)F.ctx.ns]);
+}
+
+// ---------------------------------------------------------------- ring, producer side
+// Lane 0 of the streaming warp.  Item k goes to stage k % NS once the compute
+// warps released the stage's previous item (and that item's copies landed);
+// each run of contiguous bytes is one bulk copy counted on the stage's full
+// mbarrier, and the producer's own arrival closes the item.
+struct Producer {
+  uint32_t k = 0;
+  bool dead = false;
+  uint8_t* stage = nullptr;
+  uint64_t* bar = nullptr;
+
+  template <int STAGE>
+  __device__ __forceinline__ bool begin() {
+    Fixed& F = fixed();
+    if (dead) return false;
+    if (F.abort || *(volatile int32_t*)F.args.sc.err != 0) { dead = true; return false; }
+    const uint32_t ns = (uint32_t)F.ctx.ns;
+    const int s = (int)(k % ns);
+    const uint32_t round = k / ns;
+    if (round > 0) {
+      if (!mbar_wait(&F.empty[s], (round & 1u) ^ 1u, &F.abort, F.args.sc.err, F.args.spin_limit_ns, (int)k) ||
+          !mbar_wait(&F.full[s], (round - 1) & 1u, &F.abort, F.args.sc.err, F.args.spin_limit_ns, (int)k)) {
+        dead = true;
+        return false;
+      }
+    }
+    stage = F.ctx.ring + (size_t)s * STAGE;
+    bar = &F.full[s];
+    return true;
+  }
+  __device__ __forceinline__ void copy(uint32_t off, const void* src, uint32_t bytes) {
+    mbar_expect_tx(bar, bytes);
+    bulk_g2s(stage + off, src, bytes, bar);
+  }
+  __device__ __forceinline__ void end() {
+    mbar_arrive(bar);
+    ++k;
+  }
+  // Before the block exits: the last item of every stage has landed.
+  __device__ void drain() {
+    Fixed& F = fixed();
+    const uint32_t ns = (uint32_t)F.ctx.ns;
+    for (uint32_t s = 0; s < ns && s < k; ++s) {
+      const uint32_t last = s + ((k - 1 - s) / ns) * ns;
+      mbar_wait_drain(&F.full[s], (last / ns) & 1u, 100000000ull);
+    }
+  }
+};
+
+__device__ __forceinline__ uint2 lds64(const void* p) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p)));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
+  return v;
+}
+
+struct ActRange {
+  const uint8_t* list;   // staged index of the i-th activation: list ? list[start + i] : start + i
+  int start, count;
+};
+
 template <class S, int WDT>
 struct Model {
   static constexpr int AUX = WDT == WF32 ? WF32 : WBF16;
   static constexpr int H = S::H, NH = S::NH, NKV = S::NKV, HD = S::HD, E = S::E, TOPK = S::TOPK;
   static constexpr int FE = S::FE, FD = S::FD, QD = NH * HD, GQA = NH / NKV, HALF = HD / 2;
   static constexpr int DPL = HD / 32;
-  static constexpr int KSD = FD <= 2048 ? FD : (WDT == WBF16 ? 1024 : 2048);  // dense-down segment
-  static constexpr int NSEG = FD / KSD;
-  static_assert(FD % KSD == 0, "dense FFN splits into segments");
   using GH = Gemv<WDT, H>;
   using GQ = Gemv<WDT, QD>;
   using GE = Gemv<WDT, FE>;
-  using GS = Gemv<WDT, KSD>;
-  static_assert(kMaxBatch * GH::ACT_BYTES <= kActBytes, "staging area holds a full batch");
-  static_assert(kMaxBatch * GQ::ACT_BYTES <= kActBytes, "staging area holds a full batch");
-  static_assert((kWarps * GQA * (HD + 2) + GQA * HD) * 4 <= kActBytes, "attention combine + query buffers");
+  using GD = Gemv<WDT, FD>;
+
+  // ring stage: data bytes (+ int4 scales, 1/16 of the codes)
+  static constexpr int STD = WDT == WBF16 ? 32768 : 16384;
+  static constexpr int AUXB = WDT == WINT4 ? STD / 16 : 0;
+  static constexpr int STAGE = STD + AUXB;
+  __host__ __device__ static constexpr int cmax(int a, int b) { return a > b ? a : b; }
+  // task ranges and tiles start at multiples of A rows (16-byte aligned scales)
+  static constexpr int A_Q = GH::A;
+  static constexpr int A_H = cmax(GQ::A, cmax(GE::A, GD::A));
+  __host__ __device__ static constexpr int tmax(int rp, int rb, int sb, int al) {
+    int t = STD / (rp * rb);
+    if (sb) t = t < AUXB / (rp * sb) ? t : AUXB / (rp * sb);
+    return t - t % al;
+  }
+  static constexpr int T_QKV = tmax(2, GH::ROW_BYTES, GH::SCALE_BYTES, A_Q);
+  static constexpr int T_O = tmax(1, GQ::ROW_BYTES, GQ::SCALE_BYTES, A_H);
+  static constexpr int T_GU = tmax(2, GH::ROW_BYTES, GH::SCALE_BYTES, A_Q);
+  static constexpr int T_DN = tmax(1, GE::ROW_BYTES, GE::SCALE_BYTES, A_H);
+  static constexpr int T_DD = tmax(1, GD::ROW_BYTES, GD::SCALE_BYTES, A_H);
+  static constexpr int T_LM = tmax(1, GH::ROW_BYTES, GH::SCALE_BYTES, A_Q);
+  static_assert(T_QKV >= 1 && T_O >= 1 && T_GU >= 1 && T_DN >= 1 && T_DD >= 1 && T_LM >= 1, "tile sizes");
+  static constexpr int TU = STD / (4 * HD) / kWarps;  // positions per warp per stage
+  static constexpr int TT = TU * kWarps;              // cached positions per stage (K and V rows, bf16)
+  static_assert(TU >= 1, "a stage holds a position per warp");
+  static_assert(HALF % A_Q == 0 && FE % A_Q == 0 && FD % A_Q == 0 && H % A_H == 0, "aligned row groups");
   static_assert(TOPK <= 8 && E <= 64, "router tables");
 
-
-
+  static constexpr int NQP = NH * HALF, NKP = NKV * HALF, NP = NQP + 2 * NKP;
   static constexpr int PR = HD + 4;  // partial row: m, l, pad, pad, o[HD] (16-byte rows)
-  static constexpr int TU = 4;
+  static constexpr int ATT_BYTES = (kWarps * GQA * (HD + 2) + GQA * HD) * 4;
+
+  // Staging area for n rows: every phase's activations fit; the MoE down
+  // entries take what is left above 3 ring stages (rounds if they do not fit).
+  __host__ __device__ static constexpr int act_base_bytes(int n) {
+    return cmax(cmax(n * GH::ACT_BYTES, n * GQ::ACT_BYTES),
+                cmax(cmax(ATT_BYTES, GD::ACT_BYTES), n * GE::ACT_BYTES));
+  }
+  static_assert(kActOffset + act_base_bytes(kMaxBatch) + 2 * STAGE <= kSmemBytes,
+                "a full batch leaves at least two ring stages");
 
   __device__ static __forceinline__ void unit_of(const StepArgs& a, const int* unit_start, int u, int n,
                                                  int& b, int& g, int& ci, int& nch) {
@@ -114,85 +238,90 @@ struct Model {
     ci = rem % nch;
   }
 
-  static constexpr int NQP = NH * HALF, NKP = NKV * HALF, NP = NQP + 2 * NKP;
-
-  // Weight rows of QKV task p (a RoPE pair of q or k rows, or two v rows).
-  __device__ static __forceinline__ RowRef qkv_row(const LayerW& Lw, int p, int r) {
-    int m, row;
-    if (p < NQP) { m = WQ; row = (p / HALF) * HD + p % HALF + r * HALF; }
-    else if (p < NQP + NKP) { const int q = p - NQP; m = WK; row = (q / HALF) * HD + q % HALF + r * HALF; }
-    else { const int q = p - NQP - NKP; m = WV; row = (q / HALF) * HD + 2 * (q % HALF) + r; }
-    return {(const uint8_t*)Lw.w[m] + (size_t)row * GH::ROW_BYTES,
-            (const uint16_t*)Lw.s[m] + (size_t)row * (H / 64)};
+  // ---- the block's task ranges (identical for the streaming warp and the
+  // compute warps)
+  __device__ static __forceinline__ void qkv_range(const Ctx& c, int& p0, int& p1) {
+    split_range(NP / A_Q, c.G, c.bid, p0, p1);
+    p0 *= A_Q;
+    p1 *= A_Q;
+  }
+  __device__ static __forceinline__ void gu_range(const Ctx& c, int total, int& u0, int& u1) {
+    split_range(total / A_Q, c.G, c.bid, u0, u1);
+    u0 *= A_Q;
+    u1 *= A_Q;
+  }
+  // rounds of the MoE down projection: distinct experts [ua, ub) whose
+  // entries fit the staging area together
+  __device__ static __forceinline__ int moe_round_end(const Fixed& F, int ua, int cap) {
+    int ub = ua, cnt = 0;
+    while (ub < F.n_ue && cnt + F.ue_len[ub] <= cap) cnt += F.ue_len[ub++];
+    return ub > ua ? ub : ua + 1;
+  }
+  // ring positions of unit u: cached positions [t0, rt1) come through the
+  // ring, the ones this launch writes, [rt1, t1), are read from global memory
+  __device__ static __forceinline__ void unit_span(const StepArgs& a, int b, int ci, int& t0, int& rt1,
+                                                   int& t1) {
+    t0 = ci * a.chunk;
+    t1 = min(a.pos[b] + 1, t0 + a.chunk);
+    rt1 = min(t1, max(t0, a.new0[b]));
   }
 
-  // --- L2 warm-up (all threads of the block): bytes a block reads in a
-  // later phase are requested from HBM early, so that phase's loads find
-  // them in L2.
-  __device__ static void prefetch_rows(const void* w, const void* s, size_t row0, int rows, int row_bytes,
-                                       int scale_bytes) {
-    if (rows <= 0) return;
-    prefetch_l2_block((const uint8_t*)w + row0 * row_bytes, (size_t)rows * row_bytes);
-    if (WDT == WINT4) prefetch_l2_block((const uint8_t*)s + row0 * scale_bytes, (size_t)rows * scale_bytes);
-  }
-
-  // QKV rows and o_proj rows of layer l owned by this block.
-  __device__ static void prefetch_attn_weights(int l) {
-    const Ctx& c = fixed().ctx;
-    const LayerW& Lw = fixed().args.layers[l];  // (a later layer: read from global)
-    int p0, p1;
-    split_range(NP, c.G, c.bid, p0, p1);
-    // rows of consecutive tasks are consecutive within a head: merge them
-    for (int r = 0; r < 2; ++r) {
-      const uint8_t* run_w = nullptr; const uint16_t* run_s = nullptr;
-      int run_n = 0;
-      for (int p = p0; p <= p1; ++p) {
-        const uint8_t* w = nullptr; const uint16_t* s = nullptr;
-        if (p < p1) { const RowRef rr = qkv_row(Lw, p, r); w = rr.w; s = rr.s; }
-        if (run_n && p < p1 && w == run_w + (size_t)run_n * GH::ROW_BYTES) { ++run_n; continue; }
-        if (run_n) prefetch_rows(run_w, run_s, 0, run_n, GH::ROW_BYTES, H / 64 * 2);
-        run_w = w; run_s = s; run_n = p < p1 ? 1 : 0;
-      }
-    }
-    prefetch_rows(Lw.w[WO], Lw.s[WO], c.r0, c.nr, GQ::ROW_BYTES, QD / 64 * 2);
-  }
-
-  // Cached K/V of this block's attention units at layer l.  Pages come from
-  // the block table, or for a row's newest page from the launch arguments;
-  // out-of-range entries are skipped.
-  __device__ static void prefetch_kv(int l) {
+  // ---- generic GEMV over ring tiles.  Tasks [0, ntask) of the phase, T per
+  // ring item; task t runs on warp t % kWarps.  TK provides
+  //   ActRange acts(t) and void out(t, ai, i, v0, v1) (all lanes).
+  template <int K, int RP, int T, bool REGS, class TK>
+  __device__ static __forceinline__ void run_gemv(int ntask, const uint8_t* act_base, const TK& task) {
+    using Gv = Gemv<WDT, K>;
     Fixed& F = fixed();
-    const StepArgs& a = F.args;
-    const Ctx& c = F.ctx;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    (void)tid; (void)lane; (void)wid;
-    for (int u = c.bid; u < a.n_units; u += c.G) {
-      int b, g, ci, nch;
-      unit_of(a, fixed().unit_start, u, c.n, b, g, ci, nch);
-      const int t0 = ci * a.chunk, t1 = min(a.pos[b] + 1, t0 + a.chunk);
-      for (int pi = t0 / kPageTokens; pi <= (t1 - 1) / kPageTokens; ++pi) {
-        int page = pi == a.pos[b] / kPageTokens ? a.cur_page[b]
-                 : (pi < a.max_pages_per_seq ? __ldcg(a.block_table + a.slot[b] * a.max_pages_per_seq + pi) : -1);
-        if (page < 0 || page >= a.n_pages) continue;
-        const int s0 = max(t0, pi * kPageTokens) % kPageTokens;
-        const int s1 = (min(t1, (pi + 1) * kPageTokens) - 1) % kPageTokens + 1;
-        for (int kv = 0; kv < 2; ++kv)
-          prefetch_l2_block(a.kv + Kv<S>::offset(l, a.n_pages, page, kv, g, s0), (size_t)(s1 - s0) * HD * 2);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint32_t k = F.kc;
+    typename Gv::Act a;
+    int loaded = -1;
+#pragma unroll 1
+    for (int t0 = 0; t0 < ntask; t0 += T, ++k) {
+      const uint8_t* st = ring_acquire<STAGE>(k);
+      const int tn = min(T, ntask - t0);
+#pragma unroll 1
+      for (int j = ((wid - t0) % kWarps + kWarps) % kWarps; j < tn; j += kWarps) {
+        const int t = t0 + j;
+        const uint8_t* wr[2];
+        const uint8_t* sr[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int rr = r < RP ? r : 0;
+          wr[r] = st + (rr * T + j) * Gv::ROW_BYTES;
+          sr[r] = st + STD + (rr * T + j) * Gv::SCALE_BYTES;
+        }
+        const ActRange ar = task.acts(t);
+#pragma unroll 1
+        for (int i = 0; i < ar.count; ++i) {
+          const int ai = ar.list ? ar.list[ar.start + i] : ar.start + i;
+          const uint8_t* ab = act_base + ai * Gv::ACT_BYTES;
+          if constexpr (REGS) {
+            if (ai != loaded) { Gv::load_act(a, ab, lane); loaded = ai; }
+          }
+          float v0, v1;
+          Gv::template dots<RP, REGS>(wr, sr, a, ab, lane, v0, v1);
+          task.out(t, ai, i, v0, v1);
+        }
       }
+      ring_release(k);
     }
+    csync();
+    if (threadIdx.x == 0) F.kc = k;
+    csync();
   }
 
   // ---------------------------------------------------------------- P1
-  // RMSNorm of the residual (every block, redundantly) -> this block's rows of
-  // the QKV projection.  A task is a RoPE pair of q or k rows (i, i + HD/2)
-  // of one head, or two adjacent v rows, so the warp that forms a pair also
-  // rotates it and writes it: q to scratch, k and v as bf16 into the page.
+  // RMSNorm of the residual (every block, redundantly) -> this block's QKV
+  // tasks.  A task is a RoPE pair of rows (i, i + HD/2) of one q, k or v head,
+  // so the warp that forms a pair also rotates it and writes it: q to
+  // scratch, k and v as bf16 into the page.
   __device__ static __noinline__ void qkv(int l) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    (void)tid; (void)lane; (void)wid;
+    const int tid = threadIdx.x, lane = tid & 31;
     const LayerW& Lw = F.lw;
     const int n = c.n;
     if (l == 0 && c.bid == 0)
@@ -219,19 +348,14 @@ struct Model {
         const int b = i / c.nr, r = c.r0 + i % c.nr;
         a.sc.x[b * H + r] = ld_aux<AUX>(a.embed, (size_t)F.tok[b] * H + r);
       }
-    __syncthreads();
+    csync();
     MK_STAMP(c, l, 0, 0);
 
     int p0, p1;
-    split_range(NP, c.G, c.bid, p0, p1);
+    qkv_range(c, p0, p1);
     struct {
-      const StepArgs* a; const LayerW* Lw; int p0, l, lane;
-      __device__ __forceinline__ RowRef row(int t, int r) const {
-        return qkv_row(*Lw, p0 + t, r);
-      }
-      __device__ __forceinline__ ActRange acts(int) const {
-        return {nullptr, 0, a->n};
-      }
+      const StepArgs* a; int p0, l, lane;
+      __device__ __forceinline__ ActRange acts(int) const { return {nullptr, 0, a->n}; }
       __device__ __forceinline__ void out(int t, int b, int, float v0, float v1) const {
         if (lane != 0) return;
         const int p = p0 + t;
@@ -252,74 +376,116 @@ struct Model {
           }
         } else {
           const int q = p - NQP - NKP;
-          const int g = q / HALF, i2 = 2 * (q % HALF);
+          const int g = q / HALF, i = q % HALF;
           uint16_t* dst = a->kv + Kv<S>::offset(l, a->n_pages, a->cur_page[b], 1, g, pos % kPageTokens);
-          dst[i2] = f_to_bf16(v0);
-          dst[i2 + 1] = f_to_bf16(v1);
+          dst[i] = f_to_bf16(v0);
+          dst[i + HALF] = f_to_bf16(v1);
         }
       }
-    } task{&a, &Lw, p0, l, lane};
-    run_tasks<WDT, H, 2>(p1 - p0, c.act, task);
+    } task{&a, p0, l, lane};
+    run_gemv<H, 2, T_QKV, false>(p1 - p0, c.act, task);
+  }
+
+  // K/V rows of TU positions into registers (bf16 -> float), from shared
+  // memory (ring) or, for positions this launch wrote, from global memory at
+  // L2 (written by other blocks before the grid barrier).
+  template <bool GL>
+  __device__ static __forceinline__ void ld_kv(const uint16_t* p, float (&f)[DPL]) {
+    if constexpr (DPL == 4) {
+      const uint2 r = GL ? __ldcg(reinterpret_cast<const uint2*>(p)) : lds64(p);
+      f[0] = bf16_to_f(r.x & 0xffff); f[1] = bf16_to_f(r.x >> 16);
+      f[2] = bf16_to_f(r.y & 0xffff); f[3] = bf16_to_f(r.y >> 16);
+    } else {
+      const uint32_t r = GL ? __ldcg(reinterpret_cast<const unsigned int*>(p)) : lds32(p);
+      f[0] = bf16_to_f(r & 0xffff); f[1] = bf16_to_f(r >> 16);
+    }
+  }
+
+  // One online-softmax update of a warp's GQA heads with TU positions (K and
+  // V row pointers per position, `ok` false for padding positions).
+  template <bool GL>
+  __device__ static __forceinline__ void attend(const uint16_t* const (&kp)[TU], const uint16_t* const (&vp)[TU],
+                                                const bool (&ok)[TU], const float (&q)[GQA][DPL], float (&m)[GQA],
+                                                float (&lsum)[GQA], float (&o)[GQA][DPL], int lane) {
+    float kf[TU][DPL], vf[TU][DPL];
+#pragma unroll
+    for (int k = 0; k < TU; ++k) {
+      ld_kv<GL>(kp[k], kf[k]);
+      ld_kv<GL>(vp[k], vf[k]);
+    }
+    // scores of the TU positions for the GQA heads: lane partials, one
+    // transposing reduction for all of them, then broadcast back
+    constexpr int NV = TU * GQA;
+    constexpr int NB = NV == 32 ? 5 : NV == 16 ? 4 : NV == 8 ? 3 : NV == 4 ? 2 : NV == 2 ? 1 : 0;
+    static_assert((1 << NB) == NV, "TU * GQA is a power of two <= 32");
+    float sv[NV];
+#pragma unroll
+    for (int k = 0; k < TU; ++k)
+#pragma unroll
+      for (int i = 0; i < GQA; ++i) {
+        float acc = 0.f;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc = fmaf(q[i][d], kf[k][d], acc);
+        sv[k * GQA + i] = acc;
+      }
+    const float mine = warp_reduce_scatter<NV>(sv, lane);
+    float sc[TU][GQA];
+#pragma unroll
+    for (int idx = 0; idx < NV; ++idx) sc[idx / GQA][idx % GQA] = __shfl_sync(0xffffffffu, mine, bitrev<NB>(idx));
+#pragma unroll
+    for (int i = 0; i < GQA; ++i) {
+      float mn = m[i];
+#pragma unroll
+      for (int k = 0; k < TU; ++k) mn = ok[k] ? fmaxf(mn, sc[k][i]) : mn;
+      const float corr = mn == -INFINITY ? 1.f : __expf(m[i] - mn);
+      float psum = 0.f, p[TU];
+#pragma unroll
+      for (int k = 0; k < TU; ++k) {
+        p[k] = ok[k] ? __expf(sc[k][i] - mn) : 0.f;
+        psum += p[k];
+      }
+      lsum[i] = fmaf(lsum[i], corr, psum);
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) {
+        float acc = o[i][d] * corr;
+#pragma unroll
+        for (int k = 0; k < TU; ++k) acc = fmaf(p[k], vf[k][d], acc);
+        o[i][d] = acc;
+      }
+      m[i] = mn;
+    }
   }
 
   // ---------------------------------------------------------------- P2
   // Split attention over the paged cache.  Unit = (row, kv head, chunk of
-  // positions); each warp takes TU positions at a time (their K and V rows
-  // loaded together), keeps a running max, sum and weighted value (online
-  // softmax) for the GQA heads of the kv head; the warps are combined and
-  // the unit's partial (m, l, o) written.  The last unit of a (row, kv head)
-  // to finish copies all its chunk partials into shared memory and merges
-  // them in chunk order (log-sum-exp).
+  // positions).  Cached positions arrive through the ring, TT per stage (K
+  // rows, then V rows); warp w takes positions w, w + 15, ... of a stage and
+  // keeps a running max, sum and weighted value (online softmax) for the GQA
+  // heads of the kv head.  Positions this launch wrote are read from global
+  // memory.  The warps are combined and the unit's partial (m, l, o) written;
+  // the last unit of a (row, kv head) to finish merges all its chunks in
+  // chunk order (log-sum-exp).
   __device__ static __noinline__ void attention(int l) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    (void)tid; (void)lane; (void)wid;
     const int n = c.n;
     float* comb = reinterpret_cast<float*>(c.act);  // [warp][GQA][HD + 2]
     float* qs = comb + kWarps * GQA * (HD + 2);     // [GQA][HD] this unit's queries
     const float qscale = rsqrtf((float)HD);
-    if (l == 0) {
-      // the pool pages of this block's units, read once per launch (after the
-      // block table got this launch's new pages): every warp of every unit
-      // reading the table itself would queue on the same L2 lines
-      int k = 0;
-      for (int u = c.bid; u < a.n_units; u += c.G, ++k) {
-        int b, g, ci, nch;
-        unit_of(a, F.unit_start, u, n, b, g, ci, nch);
-        const int t0 = ci * a.chunk, t1 = min(a.pos[b] + 1, t0 + a.chunk);
-        const int p0 = t0 / kPageTokens, np = (t1 - 1) / kPageTokens - p0 + 1;
-        if (k >= 2 || np > 64) {
-          if (tid == 0) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, u);
-          continue;
-        }
-        for (int j = tid; j < np; j += kThreads) {
-          const int pi = p0 + j;
-          int page = pi < a.max_pages_per_seq ? __ldcg(a.block_table + a.slot[b] * a.max_pages_per_seq + pi) : -1;
-          if (page < 0 || page >= a.n_pages) {
-            set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_PAGE, pi);
-            page = 0;
-          }
-          F.upages[k][j] = page;
-        }
-      }
-      __syncthreads();
-    }
-    int k_unit = 0;
-    for (int u = c.bid; u < a.n_units; u += c.G, ++k_unit) {
+    uint32_t k = F.kc;
+#pragma unroll 1
+    for (int u = c.bid; u < a.n_units; u += c.G) {
       int b, g, ci, nch;
       unit_of(a, F.unit_start, u, n, b, g, ci, nch);
-      const int ctx = a.pos[b] + 1;
-      const int t0 = ci * a.chunk, t1 = min(ctx, t0 + a.chunk);
-      const int pbase = t0 / kPageTokens;
-      const int* upg = F.upages[min(k_unit, 1)];
+      int t0, rt1, t1;
+      unit_span(a, b, ci, t0, rt1, t1);
       // this unit's queries into shared memory once (coalesced), not per warp
       for (int v = tid; v < GQA * HD / 4; v += kThreads)
         reinterpret_cast<float4*>(qs)[v] =
             __ldcg(reinterpret_cast<const float4*>(a.sc.q + b * QD + g * GQA * HD) + v);
-      __syncthreads();
-
+      csync();
       float q[GQA][DPL];
 #pragma unroll
       for (int i = 0; i < GQA; ++i)
@@ -328,81 +494,52 @@ struct Model {
       float m[GQA], lsum[GQA], o[GQA][DPL];
 #pragma unroll
       for (int i = 0; i < GQA; ++i) {
-        m[i] = -INFINITY; lsum[i] = 0.f;
+        m[i] = -INFINITY;
+        lsum[i] = 0.f;
 #pragma unroll
         for (int d = 0; d < DPL; ++d) o[i][d] = 0.f;
       }
-      for (int tb = t0 + wid; tb < t1; tb += kWarps * TU) {
-        // TU positions per warp: all K/V loads issued before any is used;
-        // positions past the chunk are predicated off (no break: the loops
-        // stay fully unrolled and the arrays stay in registers)
-        float kf[TU][DPL], vf[TU][DPL];
+#pragma unroll 1
+      for (int tb = t0; tb < rt1; tb += TT, ++k) {
+        const uint8_t* st = ring_acquire<STAGE>(k);
+        const int nt = min(TT, rt1 - tb);
+        const uint16_t* kp[TU];
+        const uint16_t* vp[TU];
         bool ok[TU];
 #pragma unroll
-        for (int k = 0; k < TU; ++k) {
-          const int t = tb + k * kWarps;
-          ok[k] = t < t1;
-          const int tt = ok[k] ? t : t0;
-          const int page = upg[tt / kPageTokens - pbase];
-          const int slot = tt % kPageTokens;
-          const uint16_t* kp = a.kv + Kv<S>::offset(l, a.n_pages, page, 0, g, slot) + lane * DPL;
-          const uint16_t* vp = a.kv + Kv<S>::offset(l, a.n_pages, page, 1, g, slot) + lane * DPL;
-          if constexpr (DPL == 4) {
-            const uint2 kr = __ldcg(reinterpret_cast<const uint2*>(kp));
-            const uint2 vr = __ldcg(reinterpret_cast<const uint2*>(vp));
-            kf[k][0] = bf16_to_f(kr.x & 0xffff); kf[k][1] = bf16_to_f(kr.x >> 16);
-            kf[k][2] = bf16_to_f(kr.y & 0xffff); kf[k][3] = bf16_to_f(kr.y >> 16);
-            vf[k][0] = bf16_to_f(vr.x & 0xffff); vf[k][1] = bf16_to_f(vr.x >> 16);
-            vf[k][2] = bf16_to_f(vr.y & 0xffff); vf[k][3] = bf16_to_f(vr.y >> 16);
-          } else {
-            const uint32_t kr = __ldcg(reinterpret_cast<const unsigned int*>(kp));
-            const uint32_t vr = __ldcg(reinterpret_cast<const unsigned int*>(vp));
-            kf[k][0] = bf16_to_f(kr & 0xffff); kf[k][1] = bf16_to_f(kr >> 16);
-            vf[k][0] = bf16_to_f(vr & 0xffff); vf[k][1] = bf16_to_f(vr >> 16);
-          }
+        for (int i = 0; i < TU; ++i) {
+          const int j = wid + kWarps * i;
+          ok[i] = j < nt;
+          const int jj = ok[i] ? j : 0;
+          kp[i] = reinterpret_cast<const uint16_t*>(st + (size_t)jj * HD * 2) + lane * DPL;
+          vp[i] = reinterpret_cast<const uint16_t*>(st + (size_t)(TT + jj) * HD * 2) + lane * DPL;
         }
-        // scores of the TU positions for the GQA heads: lane partials, one
-        // transposing reduction for all of them, then broadcast back
-        constexpr int NV = TU * GQA;
-        constexpr int NB = NV == 32 ? 5 : NV == 16 ? 4 : NV == 8 ? 3 : NV == 4 ? 2 : NV == 2 ? 1 : 0;
-        float sv[NV];
+        attend<false>(kp, vp, ok, q, m, lsum, o, lane);
+        ring_release(k);
+      }
+#pragma unroll 1
+      for (int tb = rt1; tb < t1; tb += kWarps * TU) {
+        const uint16_t* kp[TU];
+        const uint16_t* vp[TU];
+        bool ok[TU];
 #pragma unroll
-        for (int k = 0; k < TU; ++k)
-#pragma unroll
-          for (int i = 0; i < GQA; ++i) {
-            float acc = 0.f;
-#pragma unroll
-            for (int d = 0; d < DPL; ++d) acc = fmaf(q[i][d], kf[k][d], acc);
-            sv[k * GQA + i] = acc;
+        for (int i = 0; i < TU; ++i) {
+          const int t = tb + wid + kWarps * i;
+          ok[i] = t < t1;
+          const int tt = ok[i] ? t : rt1;
+          const int pi = tt / kPageTokens;
+          int page = pi == a.pos[b] / kPageTokens
+                         ? a.cur_page[b]
+                         : (pi < a.max_pages_per_seq ? __ldcg(a.block_table + a.slot[b] * a.max_pages_per_seq + pi)
+                                                     : -1);
+          if (page < 0 || page >= a.n_pages) {
+            set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_PAGE, pi);
+            page = 0;
           }
-        const float mine = warp_reduce_scatter<NV>(sv, lane);
-        float sc[TU][GQA];
-#pragma unroll
-        for (int idx = 0; idx < NV; ++idx)
-          sc[idx / GQA][idx % GQA] = __shfl_sync(0xffffffffu, mine, bitrev<NB>(idx));
-        // one online-softmax update per head for the whole batch
-#pragma unroll
-        for (int i = 0; i < GQA; ++i) {
-          float mn = m[i];
-#pragma unroll
-          for (int k = 0; k < TU; ++k) mn = ok[k] ? fmaxf(mn, sc[k][i]) : mn;
-          const float corr = __expf(m[i] - mn);
-          float psum = 0.f, p[TU];
-#pragma unroll
-          for (int k = 0; k < TU; ++k) {
-            p[k] = ok[k] ? __expf(sc[k][i] - mn) : 0.f;
-            psum += p[k];
-          }
-          lsum[i] = fmaf(lsum[i], corr, psum);
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) {
-            float acc = o[i][d] * corr;
-#pragma unroll
-            for (int k = 0; k < TU; ++k) acc = fmaf(p[k], vf[k][d], acc);
-            o[i][d] = acc;
-          }
-          m[i] = mn;
+          kp[i] = a.kv + Kv<S>::offset(l, a.n_pages, page, 0, g, tt % kPageTokens) + lane * DPL;
+          vp[i] = a.kv + Kv<S>::offset(l, a.n_pages, page, 1, g, tt % kPageTokens) + lane * DPL;
         }
+        attend<true>(kp, vp, ok, q, m, lsum, o, lane);
       }
 #pragma unroll
       for (int i = 0; i < GQA; ++i) {
@@ -411,7 +548,7 @@ struct Model {
 #pragma unroll
         for (int d = 0; d < DPL; ++d) cw[2 + lane * DPL + d] = o[i][d];
       }
-      __syncthreads();
+      csync();
       if (u >= a.max_units) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, u);
       float* pu = a.sc.part + (size_t)min(u, a.max_units - 1) * GQA * PR;
       // factors exp(m_w - M) once per (warp, head), then a weighted sum per dim
@@ -422,13 +559,13 @@ struct Model {
         for (int w = 0; w < kWarps; ++w) M = fmaxf(M, comb[(w * GQA + tid) * (HD + 2)]);
         Ms[tid] = M;
       }
-      __syncthreads();
+      csync();
       if (tid < kWarps * GQA) {
         const int w = tid / GQA, i = tid % GQA;
         const float mw = comb[(w * GQA + i) * (HD + 2)];
         fac[tid] = mw == -INFINITY ? 0.f : __expf(mw - Ms[i]);
       }
-      __syncthreads();
+      csync();
       for (int idx = tid; idx < GQA * HD; idx += kThreads) {
         const int i = idx / HD, d = idx % HD;
         float L = 0.f, O = 0.f;
@@ -441,7 +578,7 @@ struct Model {
         if (d == 0) { pu[i * PR] = Ms[i]; pu[i * PR + 1] = L; }
         pu[i * PR + 4 + d] = O;
       }
-      __syncthreads();
+      csync();
       if (tid == 0) {
         // release this unit's partial, acquire the others' if it is the last
         int old;
@@ -449,72 +586,107 @@ struct Model {
                      : "=r"(old) : "l"(a.sc.merge_cnt + b * NKV + g) : "memory");
         F.flag = old == nch - 1;
       }
-      __syncthreads();
-      if (F.flag) {  // last unit of (b, g): log-sum-exp merge of its chunks
-        if (nch > kMaxChunks || nch * GQA > kThreads) {
-          if (tid == 0) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, nch);
-          __syncthreads();
-          continue;
-        }
-        const float* pb = a.sc.part + (size_t)(F.unit_start[b] + g * nch) * GQA * PR;
-        // one warp per head: M = max_c m_c, L = sum_c l_c exp(m_c - M), and the
-        // chunk factors exp(m_c - M) / L into shared memory
-        float* mfac = F.red;  // [nch][GQA]
-        if (wid < GQA) {
-          const int i = wid;
-          float mv[2], lv[2];
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int cc = lane + 32 * r;
-            mv[r] = cc < nch ? __ldcg(pb + (cc * GQA + i) * PR) : -INFINITY;
-            lv[r] = cc < nch ? __ldcg(pb + (cc * GQA + i) * PR + 1) : 0.f;
-          }
-          const float M = warp_max(fmaxf(mv[0], mv[1]));
-          float f[2];
-#pragma unroll
-          for (int r = 0; r < 2; ++r) f[r] = mv[r] == -INFINITY ? 0.f : __expf(mv[r] - M);
-          const float Linv = 1.f / warp_sum(fmaf(lv[0], f[0], lv[1] * f[1]));
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int cc = lane + 32 * r;
-            if (cc < nch) mfac[cc * GQA + i] = f[r] * Linv;
-          }
-        }
-        __syncthreads();
-        // weighted sum of the chunk outputs, read from L2 eight chunks at a time
-        for (int idx = tid; idx < GQA * HD; idx += kThreads) {
-          const int i = idx / HD, d = idx % HD;
-          float O = 0.f;
-          for (int c0 = 0; c0 < nch; c0 += 8) {
-            float ov[8];
-#pragma unroll
-            for (int u2 = 0; u2 < 8; ++u2)
-              ov[u2] = c0 + u2 < nch ? __ldcg(pb + ((c0 + u2) * GQA + i) * PR + 4 + d) : 0.f;
-#pragma unroll
-            for (int u2 = 0; u2 < 8; ++u2)
-              if (c0 + u2 < nch) O = fmaf(ov[u2], mfac[(c0 + u2) * GQA + i], O);
-          }
-          a.sc.attn[b * QD + (g * GQA + i) * HD + d] = O;
-          if (c.tr_attn) c.tr_attn[((size_t)l * n + b) * QD + (g * GQA + i) * HD + d] = O;
-        }
-        if (tid == 0) a.sc.merge_cnt[b * NKV + g] = 0;
-      }
-      __syncthreads();
+      csync();
+      if (F.flag) merge(l, b, g, nch);
+      csync();
     }
+    if (tid == 0) F.kc = k;
+    csync();
+  }
+
+  // Last unit of (b, g): log-sum-exp merge of its chunks into the attention
+  // output.
+  __device__ static __forceinline__ void merge(int l, int b, int g, int nch) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int n = c.n;
+    if (nch > kMaxChunks || nch * GQA > kThreads) {
+      if (tid == 0) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, nch);
+      return;
+    }
+    const float* pb = a.sc.part + (size_t)(F.unit_start[b] + g * nch) * GQA * PR;
+    // one warp per head: M = max_c m_c, L = sum_c l_c exp(m_c - M), and the
+    // chunk factors exp(m_c - M) / L into shared memory
+    float* mfac = F.red;  // [nch][GQA]
+    if (wid < GQA) {
+      const int i = wid;
+      float mv[2], lv[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int cc = lane + 32 * r;
+        mv[r] = cc < nch ? __ldcg(pb + (cc * GQA + i) * PR) : -INFINITY;
+        lv[r] = cc < nch ? __ldcg(pb + (cc * GQA + i) * PR + 1) : 0.f;
+      }
+      const float M = warp_max(fmaxf(mv[0], mv[1]));
+      float f[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) f[r] = mv[r] == -INFINITY ? 0.f : __expf(mv[r] - M);
+      const float Linv = 1.f / warp_sum(fmaf(lv[0], f[0], lv[1] * f[1]));
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int cc = lane + 32 * r;
+        if (cc < nch) mfac[cc * GQA + i] = f[r] * Linv;
+      }
+    }
+    csync();
+    // weighted sum of the chunk outputs: float4 output o = (head, 4 dims) is
+    // summed by NG thread groups over chunks grp, grp + NG, ... (all of a
+    // group's loads in flight together), then the groups in a fixed order
+    constexpr int NOUT4 = GQA * HD / 4;
+    constexpr int NG = kThreads / NOUT4;
+    constexpr int BATCH = 12;
+    static_assert(NG >= 1, "one float4 output per thread at least");
+    float4* gsum = reinterpret_cast<float4*>(c.act);  // [NG][NOUT4] (the combine area is free now)
+    if (tid < NG * NOUT4) {
+      const int grp = tid / NOUT4, o = tid % NOUT4, i = o / (HD / 4), d4 = o % (HD / 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c0 = grp; c0 < nch; c0 += NG * BATCH) {
+        float4 ov[BATCH];
+#pragma unroll
+        for (int u2 = 0; u2 < BATCH; ++u2) {
+          const int cc = c0 + u2 * NG;
+          ov[u2] = cc < nch ? __ldcg(reinterpret_cast<const float4*>(pb + (cc * GQA + i) * PR + 4) + d4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u2 = 0; u2 < BATCH; ++u2) {
+          const int cc = c0 + u2 * NG;
+          const float f = cc < nch ? mfac[cc * GQA + i] : 0.f;
+          acc.x = fmaf(ov[u2].x, f, acc.x);
+          acc.y = fmaf(ov[u2].y, f, acc.y);
+          acc.z = fmaf(ov[u2].z, f, acc.z);
+          acc.w = fmaf(ov[u2].w, f, acc.w);
+        }
+      }
+      gsum[grp * NOUT4 + o] = acc;
+    }
+    csync();
+    if (tid < NOUT4) {
+      const int i = tid / (HD / 4), d4 = tid % (HD / 4);
+      float4 o = gsum[tid];
+      for (int grp = 1; grp < NG; ++grp) {
+        const float4 v = gsum[grp * NOUT4 + tid];
+        o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w;
+      }
+      const size_t off = (size_t)(g * GQA + i) * HD + 4 * d4;
+      *reinterpret_cast<float4*>(a.sc.attn + b * QD + off) = o;
+      if (c.tr_attn) *reinterpret_cast<float4*>(c.tr_attn + ((size_t)l * n + b) * QD + off) = o;
+    }
+    if (tid == 0) a.sc.merge_cnt[b * NKV + g] = 0;
   }
 
   // ---------------------------------------------------------------- P3
   // o_proj rows of this block + residual.  In MoE layers the block also forms
   // its partial router logits: the post-attention RMSNorm is one scalar per
   // row times w2, so logits = rsqrt(mean(h^2) + eps) * sum_blocks(partials);
-  // the scalar is applied in P4.  The last block to finish adds the
-  // partials in block order (deterministic).
+  // the scalar is applied in P4.
   __device__ static __noinline__ void oproj(int l) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    (void)tid; (void)lane; (void)wid;
+    const int tid = threadIdx.x, lane = tid & 31;
     const LayerW& Lw = F.lw;
     const int n = c.n;
     {
@@ -523,27 +695,20 @@ struct Model {
           c.act, n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(at + r * QD) + f4); },
           false, 0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
     }
-    __syncthreads();
+    csync();
     MK_STAMP(c, l, 2, 0);
     struct {
-      const StepArgs* a; const LayerW* Lw; Fixed* F; int r0, lane;
-      __device__ __forceinline__ RowRef row(int t, int) const {
-        return {(const uint8_t*)Lw->w[WO] + (size_t)(r0 + t) * GQ::ROW_BYTES,
-                (const uint16_t*)Lw->s[WO] + (size_t)(r0 + t) * (QD / 64)};
-      }
-      __device__ __forceinline__ ActRange acts(int) const {
-        return {nullptr, 0, a->n};
-      }
-      __device__ __forceinline__ void out(int t, int b, int, float v0, float v1) const {
+      const StepArgs* a; Fixed* F; int r0, lane;
+      __device__ __forceinline__ ActRange acts(int) const { return {nullptr, 0, a->n}; }
+      __device__ __forceinline__ void out(int t, int b, int, float v0, float) const {
         if (lane != 0) return;
         const float hv = __ldcg(a->sc.x + b * H + r0 + t) + v0;
         a->sc.h[b * H + r0 + t] = hv;
         F->hs[b][t] = hv;
       }
-    } task{&a, &Lw, &F, c.r0, lane};
-    run_tasks<WDT, QD, 1>(c.nr, c.act, task);
+    } task{&a, &F, c.r0, lane};
+    run_gemv<QD, 1, T_O, false>(c.nr, c.act, task);
     if (l < a.n_dense) return;
-    __syncthreads();
     for (int idx = tid; idx < n * E; idx += kThreads) {
       const int b = idx / E, e = idx % E;
       float s = 0.f;
@@ -559,16 +724,15 @@ struct Model {
   // Routing, then the post-attention RMSNorm.  The router logits of a row are
   // rsqrt(mean(h^2) + eps) times the block-summed partials of P3; that factor
   // is positive and common to the row, so the top-k selection (ties -> lower
-  // expert id) is made from the partials before the norm is known.  The
-  // selected experts' weights are then requested from HBM while the norm is
-  // computed, and the softmax weights (renormalised over the selection) are
-  // formed from the scaled logits.  Dense layers only norm.
+  // expert id) is made from the partials before the norm is known, and the
+  // streaming warp is told at once so the experts' weights start moving while
+  // the norm is computed.  The softmax weights (renormalised over the
+  // selection) are formed from the scaled logits.  Dense layers only norm.
   __device__ static __noinline__ void route(int l) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    (void)tid; (void)lane; (void)wid;
     const LayerW& Lw = F.lw;
     const bool moe = l >= a.n_dense;
     const int n = c.n;
@@ -582,7 +746,7 @@ struct Model {
           lg[j] = e < E ? __ldcg(a.sc.rlogit + b * E + e) : -INFINITY;
         }
 #pragma unroll
-        for (int k = 0; k < TOPK; ++k) {
+        for (int kk = 0; kk < TOPK; ++kk) {
           float bv = -INFINITY;
           int be = INT_MAX;
 #pragma unroll
@@ -596,13 +760,13 @@ struct Model {
             const int oe = __shfl_xor_sync(0xffffffffu, be, o);
             if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
           }
-          if (lane == 0) { F.topk_id[b][k] = be; F.topk_w[b][k] = bv; }  // partial logit for now
+          if (lane == 0) { F.topk_id[b][kk] = be; F.topk_w[b][kk] = bv; }  // partial logit for now
 #pragma unroll
           for (int j = 0; j < EJ; ++j)
             if (lane + 32 * j == be) lg[j] = -INFINITY;
         }
       }
-      __syncthreads();
+      csync();
       if (wid == 0) {
         // entries sorted by (expert, row, slot); one run of rows per distinct expert
         int base = 0, nue = 0;
@@ -611,7 +775,7 @@ struct Model {
           const int e = lane + 32 * j;
           int cnt = 0;
           for (int b = 0; b < n; ++b)
-            for (int k = 0; k < TOPK; ++k) cnt += F.topk_id[b][k] == e;
+            for (int kk = 0; kk < TOPK; ++kk) cnt += F.topk_id[b][kk] == e;
           const int has = cnt > 0;
           int incl = cnt, hincl = has;
 #pragma unroll
@@ -628,11 +792,11 @@ struct Model {
             F.ue_len[ue] = (int16_t)cnt;
             int pos = start;
             for (int b = 0; b < n; ++b)
-              for (int k = 0; k < TOPK; ++k)
-                if (F.topk_id[b][k] == e) {
+              for (int kk = 0; kk < TOPK; ++kk)
+                if (F.topk_id[b][kk] == e) {
                   F.ent_b[pos] = (uint8_t)b;
-                  F.ent_j[pos] = (uint8_t)k;
-                  F.ent_of[b][k] = (uint8_t)pos;
+                  F.ent_j[pos] = (uint8_t)kk;
+                  F.ent_of[b][kk] = (uint8_t)pos;
                   ++pos;
                 }
           }
@@ -641,7 +805,11 @@ struct Model {
         }
         if (lane == 0) F.n_ue = nue;
       }
-      __syncthreads();
+      csync();
+      if (tid == 0) {
+        __threadfence_block();
+        F.route_gen = l + 1;
+      }
     }
     {
       const void* nw = Lw.ffn_norm;
@@ -650,7 +818,7 @@ struct Model {
           c.act, n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(hp + r * H) + f4); },
           true, a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, F.rnorm);
     }
-    __syncthreads();
+    csync();
     MK_STAMP(c, l, 3, 0);
     if (!moe) return;
     for (int b = wid; b < n; b += kWarps) {
@@ -663,81 +831,35 @@ struct Model {
         const float top = r * F.topk_w[b][0];
         float wk[TOPK], wsum = 0.f;
 #pragma unroll
-        for (int k = 0; k < TOPK; ++k) {
-          wk[k] = expf(r * F.topk_w[b][k] - top);
-          wsum += wk[k];
+        for (int kk = 0; kk < TOPK; ++kk) {
+          wk[kk] = expf(r * F.topk_w[b][kk] - top);
+          wsum += wk[kk];
         }
 #pragma unroll
-        for (int k = 0; k < TOPK; ++k) {
-          F.topk_w[b][k] = wk[k] / wsum;
+        for (int kk = 0; kk < TOPK; ++kk) {
+          F.topk_w[b][kk] = wk[kk] / wsum;
           if (c.tr_tk && c.bid == 0) {
-            c.tr_tk[((size_t)l * n + b) * 2 * TOPK + k] = (float)F.topk_id[b][k];
-            c.tr_tk[((size_t)l * n + b) * 2 * TOPK + TOPK + k] = wk[k] / wsum;
+            c.tr_tk[((size_t)l * n + b) * 2 * TOPK + kk] = (float)F.topk_id[b][kk];
+            c.tr_tk[((size_t)l * n + b) * 2 * TOPK + TOPK + kk] = wk[kk] / wsum;
           }
         }
       }
     }
   }
 
-  // After routing (all threads): this block's gate/up and down rows of layer l,
-  // then the attention weights and cached K/V of layer l + 1 (or the start of
-  // its lm_head rows after the last layer).
-  __device__ static void prefetch_ffn_and_next(int l) {
-    Fixed& F = fixed();
-    const StepArgs& a = F.args;
-    const Ctx& c = F.ctx;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    (void)tid; (void)lane; (void)wid;
-    const LayerW& Lw = F.lw;
-    if (l >= a.n_dense) {
-      int u0, u1;
-      split_range(F.n_ue * FE, c.G, c.bid, u0, u1);
-      for (int ue = u0 / FE; ue < F.n_ue && ue * FE < u1; ++ue) {
-        const int e = F.ue_expert[ue];
-        const int f0 = max(u0, ue * FE) - ue * FE, f1 = min(u1, (ue + 1) * FE) - ue * FE;
-        for (int m = EGATE; m <= EUP; ++m)
-          prefetch_rows(Lw.w[m], Lw.s[m], (size_t)e * FE + f0, f1 - f0, GH::ROW_BYTES, H / 64 * 2);
-      }
-      for (int ue = 0; ue < F.n_ue; ++ue)
-        prefetch_rows(Lw.w[EDOWN], Lw.s[EDOWN], (size_t)F.ue_expert[ue] * H + c.r0, c.nr, GE::ROW_BYTES,
-                      FE / 64 * 2);
-    } else {
-      int f0, f1;
-      split_range(FD, c.G, c.bid, f0, f1);
-      for (int m = GATE; m <= UP; ++m) prefetch_rows(Lw.w[m], Lw.s[m], f0, f1 - f0, GH::ROW_BYTES, H / 64 * 2);
-      prefetch_rows(Lw.w[DOWN], Lw.s[DOWN], c.r0, c.nr, NSEG * GS::ROW_BYTES, FD / 64 * 2);
-    }
-    if (l + 1 < a.n_layers) {
-      prefetch_attn_weights(l + 1);
-      prefetch_kv(l + 1);
-    } else if (a.out_first < c.n) {
-      int v0, v1;
-      split_range(a.vocab, c.G, c.bid, v0, v1);
-      prefetch_rows(a.lm_head, a.lm_head_s, v0, min(v1 - v0, 128), GH::ROW_BYTES, H / 64 * 2);
-    }
-  }
-
   // ---------------------------------------------------------------- P4b
-  // Gate/up rows -> silu(gate) * up.  MoE: units (distinct expert, ffn row),
+  // Gate/up rows -> silu(gate) * up.  MoE: tasks (distinct expert, ffn row),
   // each computed for every row routed to that expert.  Dense: ffn rows.
   __device__ static __noinline__ void gateup(int l) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    (void)tid; (void)lane; (void)wid;
-    const LayerW& Lw = F.lw;
+    const int lane = threadIdx.x & 31;
     if (l >= a.n_dense) {
       int u0, u1;
-      split_range(F.n_ue * FE, c.G, c.bid, u0, u1);
+      gu_range(c, F.n_ue * FE, u0, u1);
       struct {
-        const StepArgs* a; const LayerW* Lw; Fixed* F; int u0, lane;
-        __device__ __forceinline__ RowRef row(int t, int r) const {
-          const int u = u0 + t, e = F->ue_expert[u / FE], f = u % FE;
-          const size_t rr = (size_t)e * FE + f;
-          return {(const uint8_t*)Lw->w[r ? EUP : EGATE] + rr * GH::ROW_BYTES,
-                  (const uint16_t*)Lw->s[r ? EUP : EGATE] + rr * (H / 64)};
-        }
+        const StepArgs* a; Fixed* F; int u0, lane;
         __device__ __forceinline__ ActRange acts(int t) const {
           const int ue = (u0 + t) / FE;
           return {F->ent_b, F->ue_start[ue], F->ue_len[ue]};
@@ -748,110 +870,101 @@ struct Model {
           const int j = F->ent_j[F->ue_start[u / FE] + i];
           a->sc.act[(b * TOPK + j) * FE + f] = silu(v0) * v1;
         }
-      } task{&a, &Lw, &F, u0, lane};
-      run_tasks<WDT, H, 2>(u1 - u0, c.act, task);
+      } task{&a, &F, u0, lane};
+      run_gemv<H, 2, T_GU, false>(u1 - u0, c.act, task);
     } else {
       int f0, f1;
-      split_range(FD, c.G, c.bid, f0, f1);
+      gu_range(c, FD, f0, f1);
       struct {
-        const StepArgs* a; const LayerW* Lw; int f0, lane;
-        __device__ __forceinline__ RowRef row(int t, int r) const {
-          return {(const uint8_t*)Lw->w[r ? UP : GATE] + (size_t)(f0 + t) * GH::ROW_BYTES,
-                  (const uint16_t*)Lw->s[r ? UP : GATE] + (size_t)(f0 + t) * (H / 64)};
-        }
-        __device__ __forceinline__ ActRange acts(int) const {
-          return {nullptr, 0, a->n};
-        }
+        const StepArgs* a; int f0, lane;
+        __device__ __forceinline__ ActRange acts(int) const { return {nullptr, 0, a->n}; }
         __device__ __forceinline__ void out(int t, int b, int, float v0, float v1) const {
           if (lane == 0) a->sc.dact[b * FD + f0 + t] = silu(v0) * v1;
         }
-      } task{&a, &Lw, f0, lane};
-      run_tasks<WDT, H, 2>(f1 - f0, c.act, task);
+      } task{&a, f0, lane};
+      run_gemv<H, 2, T_GU, false>(f1 - f0, c.act, task);
     }
   }
 
   // ---------------------------------------------------------------- P5
-  // Down projection of this block's hidden rows.  Activation vectors
-  // ("entries": (row, expert slot) in MoE layers, (segment, row) in dense
-  // layers) are staged in rounds that fit the staging area; entries sharing
-  // one weight matrix form a run, so each weight row is read once per run.
-  // The weighted sum over experts is taken in slot order, then the residual.
+  // Down projection of this block's hidden rows.  MoE: the (row, expert slot)
+  // activation vectors are staged in rounds of whole experts that fit the
+  // staging area; a tile holds this block's rows of one or more experts'
+  // matrices, each row is dotted with every entry of its expert.  Dense: the
+  // batch rows are staged in rounds, the full-width rows of the block are
+  // streamed once per round.  Then the weighted sum over experts in slot
+  // order and the residual.
   template <bool MOE>
   __device__ static __noinline__ void down(int l) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    (void)tid; (void)lane; (void)wid;
-    const LayerW& Lw = F.lw;
-    using GD = typename std::conditional<MOE, GE, GS>::type;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int n = c.n, nr = c.nr;
-    const int nent = MOE ? n * TOPK : n * NSEG;
-    const int cap = kActBytes / GD::ACT_BYTES;
-    for (int base = 0; base < nent; base += cap) {
-      const int cnt = min(cap, nent - base);
-      {
-        const float* act = a.sc.act;
-        const float* dact = a.sc.dact;
-        const Fixed* Fp = &F;
-        stage_block<WDT, MOE ? FE : KSD>(
-            c.act, cnt,
-            [&](int r, int f4) -> float4 {
-              const int en = base + r;
-              const float* src = MOE ? act + (Fp->ent_b[en] * TOPK + Fp->ent_j[en]) * FE
-                                     : dact + (en % n) * FD + (en / n) * KSD;
-              return __ldcg(reinterpret_cast<const float4*>(src) + f4);
-            },
-            false, 0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
-      }
-      if (tid == 0) {
-        int nrun = 0;
-        for (int en = base; en < base + cnt; ++en) {
-          const int mat = MOE ? F.topk_id[F.ent_b[en]][F.ent_j[en]] : en / n;
-          if (nrun == 0 || F.run_mat[nrun - 1] != mat) {
-            F.run_mat[nrun] = (int16_t)mat;
-            F.run_start[nrun] = (int16_t)(en - base);
-            F.run_len[nrun] = 0;
-            ++nrun;
+    if constexpr (MOE) {
+      const int cap = c.act_bytes / GE::ACT_BYTES;
+#pragma unroll 1
+      for (int ua = 0; ua < F.n_ue;) {
+        const int ub = moe_round_end(F, ua, cap);
+        const int e0 = F.ue_start[ua], ecnt = F.ue_start[ub - 1] + F.ue_len[ub - 1] - e0;
+        {
+          const float* act = a.sc.act;
+          const Fixed* Fp = &F;
+          stage_block<WDT, FE>(
+              c.act, ecnt,
+              [&](int r, int f4) -> float4 {
+                const int en = e0 + r;
+                const float* src = act + (Fp->ent_b[en] * TOPK + Fp->ent_j[en]) * FE;
+                return __ldcg(reinterpret_cast<const float4*>(src) + f4);
+              },
+              false, 0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
+        }
+        csync();
+        MK_STAMP(c, l, 4, 0);
+        struct {
+          Fixed* F; int ua, nr, e0, lane;
+          __device__ __forceinline__ ActRange acts(int t) const {
+            const int ue = ua + t / nr;
+            return {nullptr, F->ue_start[ue] - e0, F->ue_len[ue]};
           }
-          ++F.run_len[nrun - 1];
-        }
-        F.n_runs = nrun;
-      }
-      __syncthreads();
-      MK_STAMP(c, l, 4, 0);
-      struct {
-        const LayerW* Lw; Fixed* F; int r0, nr, base, lane;
-        __device__ __forceinline__ RowRef row(int t, int) const {
-          const int run = t / nr, rr = t % nr, mat = F->run_mat[run];
-          if (MOE) {
-            const size_t row = (size_t)mat * H + r0 + rr;
-            return {(const uint8_t*)Lw->w[EDOWN] + row * GD::ROW_BYTES,
-                    (const uint16_t*)Lw->s[EDOWN] + row * (FE / 64)};
-          } else {
-            const size_t row = (size_t)(r0 + rr);
-            return {(const uint8_t*)Lw->w[DOWN] + (row * NSEG + mat) * GD::ROW_BYTES,
-                    (const uint16_t*)Lw->s[DOWN] + row * (FD / 64) + mat * (KSD / 64)};
+          __device__ __forceinline__ void out(int t, int ai, int, float v0, float) const {
+            if (lane == 0) F->dots[e0 + ai][t % nr] = v0;
           }
+        } task{&F, ua, nr, e0, lane};
+        run_gemv<FE, 1, T_DN, false>((ub - ua) * nr, c.act, task);
+        ua = ub;
+      }
+    } else {
+      const int cap = c.act_bytes / GD::ACT_BYTES;
+#pragma unroll 1
+      for (int ba = 0; ba < n; ba += cap) {
+        const int cnt = min(cap, n - ba);
+        {
+          const float* dact = a.sc.dact;
+          stage_block<WDT, FD>(
+              c.act, cnt,
+              [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(dact + (ba + r) * FD) + f4); },
+              false, 0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
         }
-        __device__ __forceinline__ ActRange acts(int t) const {
-          const int run = t / nr;
-          return {nullptr, F->run_start[run], F->run_len[run]};
-        }
-        __device__ __forceinline__ void out(int t, int ai, int, float v0, float v1) const {
-          if (lane == 0) F->dots[base + ai][t % nr] = v0;
-        }
-      } task{&Lw, &F, c.r0, nr, base, lane};
-      run_tasks<WDT, MOE ? FE : KSD, 1>(F.n_runs * nr, c.act, task);
-      __syncthreads();
+        csync();
+        MK_STAMP(c, l, 4, 0);
+        struct {
+          Fixed* F; int ba, cnt, lane;
+          __device__ __forceinline__ ActRange acts(int) const { return {nullptr, 0, cnt}; }
+          __device__ __forceinline__ void out(int t, int ai, int, float v0, float) const {
+            if (lane == 0) F->dots[ba + ai][t] = v0;
+          }
+        } task{&F, ba, cnt, lane};
+        run_gemv<FD, 1, T_DD, false>(nr, c.act, task);
+      }
     }
     for (int idx = tid; idx < n * nr; idx += kThreads) {
       const int b = idx / nr, rr = idx % nr;
       float s = 0.f;
       if (MOE)
-        for (int k = 0; k < TOPK; ++k) s = fmaf(F.topk_w[b][k], F.dots[F.ent_of[b][k]][rr], s);
+        for (int kk = 0; kk < TOPK; ++kk) s = fmaf(F.topk_w[b][kk], F.dots[F.ent_of[b][kk]][rr], s);
       else
-        for (int sg = 0; sg < NSEG; ++sg) s += F.dots[sg * n + b][rr];
+        s = F.dots[b][rr];
       const float xv = __ldcg(a.sc.h + b * H + c.r0 + rr) + s;
       a.sc.x[b * H + c.r0 + rr] = xv;
       if (c.tr_x) c.tr_x[((size_t)l * n + b) * H + c.r0 + rr] = xv;
@@ -867,7 +980,6 @@ struct Model {
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    (void)tid; (void)lane; (void)wid;
     const int n = c.n;
     {
       const void* nw = a.final_norm;
@@ -881,19 +993,13 @@ struct Model {
       F.best_v[i / kMaxBatch][i % kMaxBatch] = -INFINITY;
       F.best_i[i / kMaxBatch][i % kMaxBatch] = INT_MAX;
     }
-    __syncthreads();
+    csync();
     int v0, v1;
-    split_range(a.vocab, c.G, c.bid, v0, v1);
+    gu_range(c, a.vocab, v0, v1);
     struct {
       const StepArgs* a; Fixed* F; float* tr; int vr0, lane, wid;
-      __device__ __forceinline__ RowRef row(int t, int) const {
-        return {(const uint8_t*)a->lm_head + (size_t)(vr0 + t) * GH::ROW_BYTES,
-                (const uint16_t*)a->lm_head_s + (size_t)(vr0 + t) * (H / 64)};
-      }
-      __device__ __forceinline__ ActRange acts(int) const {
-        return {nullptr, a->out_first, a->n - a->out_first};
-      }
-      __device__ __forceinline__ void out(int t, int b, int, float v0, float v1) const {
+      __device__ __forceinline__ ActRange acts(int) const { return {nullptr, a->out_first, a->n - a->out_first}; }
+      __device__ __forceinline__ void out(int t, int b, int, float v0, float) const {
         if (lane != 0) return;
         const int tok = vr0 + t;
         // a warp visits its rows in increasing order: '>' keeps the lowest id
@@ -901,8 +1007,7 @@ struct Model {
         if (tr) tr[(size_t)b * a->vocab + tok] = v0;
       }
     } task{&a, &F, c.tr_fin, v0, lane, wid};
-    run_tasks<WDT, H, 1>(v1 - v0, c.act, task);
-    __syncthreads();
+    run_gemv<H, 1, T_LM, GH::ACT_REGS>(v1 - v0, c.act, task);
     if (tid < n) {
       float bv = -INFINITY;
       int bi = INT_MAX;
@@ -914,12 +1019,12 @@ struct Model {
       a.sc.amax_v[c.bid * kMaxBatch + tid] = bv;
       a.sc.amax_i[c.bid * kMaxBatch + tid] = bi;
     }
-    __syncthreads();
+    csync();
     if (tid == 0) {
       __threadfence();
       F.flag = atomicAdd(a.sc.sync + 96, 1u) == (uint32_t)(c.G - 1);
     }
-    __syncthreads();
+    csync();
     if (!F.flag) return;
     __threadfence();
     for (int b = a.out_first + wid; b < n; b += kWarps) {
@@ -940,10 +1045,222 @@ struct Model {
     }
     if (tid == 0) a.sc.sync[96] = 0;
   }
+
+  // ---------------------------------------------------------------- streaming warp
+  // One run of `cnt` consecutive rows (codes at w0, scales at s0) into
+  // segment `seg` of a tile of T tasks, starting at task j.
+  __device__ static __forceinline__ void put_run(Producer& p, int seg, int T, int j, int cnt, const void* w0,
+                                                 const void* s0, int rb, int sb) {
+    p.copy((uint32_t)((seg * T + j) * rb), w0, (uint32_t)(cnt * rb));
+    if (sb) p.copy((uint32_t)(STD + (seg * T + j) * sb), s0, (uint32_t)(cnt * sb));
+  }
+
+  // Pool pages of this block's attention units (positions before new0 only,
+  // the same for every layer), read once per launch by the whole streaming
+  // warp.
+  __device__ static __forceinline__ void load_unit_pages() {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int lane = threadIdx.x & 31;
+    int k = 0;
+    for (int u = c.bid; u < a.n_units; u += c.G, ++k) {
+      int b, g, ci, nch;
+      unit_of(a, F.unit_start, u, c.n, b, g, ci, nch);
+      int t0, rt1, t1;
+      unit_span(a, b, ci, t0, rt1, t1);
+      if (rt1 <= t0) continue;
+      const int p0 = t0 / kPageTokens, np = (rt1 - 1) / kPageTokens - p0 + 1;
+      if (k >= 2 || np > 64) {
+        if (lane == 0) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, u);
+        continue;
+      }
+      for (int j = lane; j < np; j += 32) {
+        const int pi = p0 + j;
+        int page = pi < a.max_pages_per_seq ? __ldcg(a.block_table + a.slot[b] * a.max_pages_per_seq + pi) : -1;
+        if (page < 0 || page >= a.n_pages) {
+          set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_PAGE, pi);
+          page = 0;
+        }
+        F.upages[k][j] = page;
+      }
+    }
+    __syncwarp();
+  }
+
+  // The block's schedule of ring items for the whole launch, in the order the
+  // compute warps consume them (lane 0 of the streaming warp).  Runs of rows
+  // contiguous in memory are known from the layouts: a QKV run ends at a head
+  // boundary, an expert run at an expert boundary.
+  __device__ static __noinline__ void produce(Producer& p) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int n = c.n;
+    constexpr int RBH = GH::ROW_BYTES, SBH = GH::SCALE_BYTES;
+#pragma unroll 1
+    for (int l = 0; l < a.n_layers; ++l) {
+      const LayerW Lg = a.layers[l];  // one batch of loads per layer
+      {  // P1: pair tasks [p0, p1); a run stays inside one head of one matrix
+        int p0, p1;
+        qkv_range(c, p0, p1);
+#pragma unroll 1
+        for (int ta = p0; ta < p1; ta += T_QKV) {
+          if (!p.template begin<STAGE>()) return;
+          const int tb = min(p1, ta + T_QKV);
+#pragma unroll 1
+          for (int q0 = ta; q0 < tb;) {
+            const int q1 = min(tb, (q0 / HALF + 1) * HALF);
+            int m, qq;
+            if (q0 < NQP) { m = WQ; qq = q0; }
+            else if (q0 < NQP + NKP) { m = WK; qq = q0 - NQP; }
+            else { m = WV; qq = q0 - NQP - NKP; }
+            const size_t row = (size_t)(qq / HALF) * HD + qq % HALF;
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+              put_run(p, r, T_QKV, q0 - ta, q1 - q0, (const uint8_t*)Lg.w[m] + (row + r * HALF) * RBH,
+                      (const uint8_t*)Lg.s[m] + (row + r * HALF) * SBH, RBH, SBH);
+            q0 = q1;
+          }
+          p.end();
+        }
+      }
+      {  // P2: cached K/V of this block's units
+        int k = 0;
+#pragma unroll 1
+        for (int u = c.bid; u < a.n_units; u += c.G, ++k) {
+          int b, g, ci, nch;
+          unit_of(a, F.unit_start, u, n, b, g, ci, nch);
+          int t0, rt1, t1;
+          unit_span(a, b, ci, t0, rt1, t1);
+          const int pbase = t0 / kPageTokens;
+#pragma unroll 1
+          for (int tb = t0; tb < rt1; tb += TT) {
+            if (!p.template begin<STAGE>()) return;
+            const int nt = min(TT, rt1 - tb);
+#pragma unroll 1
+            for (int j = 0; j < nt;) {
+              const int t = tb + j, slot = t % kPageTokens;
+              const int run = min(nt - j, kPageTokens - slot);
+              const int page = F.upages[min(k, 1)][t / kPageTokens - pbase];
+#pragma unroll
+              for (int kv = 0; kv < 2; ++kv)
+                p.copy((uint32_t)((kv * TT + j) * HD * 2), a.kv + Kv<S>::offset(l, a.n_pages, page, kv, g, slot),
+                       (uint32_t)(run * HD * 2));
+              j += run;
+            }
+            p.end();
+          }
+        }
+      }
+      // P3: o_proj rows [r0, r0 + nr), one run
+#pragma unroll 1
+      for (int t0 = 0; t0 < c.nr; t0 += T_O) {
+        if (!p.template begin<STAGE>()) return;
+        const size_t row = (size_t)(c.r0 + t0);
+        put_run(p, 0, T_O, 0, min(T_O, c.nr - t0), (const uint8_t*)Lg.w[WO] + row * GQ::ROW_BYTES,
+                (const uint8_t*)Lg.s[WO] + row * GQ::SCALE_BYTES, GQ::ROW_BYTES, GQ::SCALE_BYTES);
+        p.end();
+      }
+      if (l >= a.n_dense) {
+        // P4/P5 need the layer's routing
+        {
+          const uint64_t t_start = globaltimer();
+          uint32_t i = 0;
+          while (F.route_gen < l + 1) {
+            if ((++i & 15u) == 0) {
+              if (F.abort || *(volatile int32_t*)a.sc.err != 0) return;
+              if (globaltimer() - t_start > a.spin_limit_ns) {
+                set_error(a.sc.err, MK_ERR_BARRIER_TIMEOUT, SITE_RING, l);
+                return;
+              }
+            }
+          }
+          __threadfence_block();
+        }
+        int u0, u1;
+        gu_range(c, F.n_ue * FE, u0, u1);
+#pragma unroll 1
+        for (int ta = u0; ta < u1; ta += T_GU) {
+          if (!p.template begin<STAGE>()) return;
+          const int tb = min(u1, ta + T_GU);
+#pragma unroll 1
+          for (int q0 = ta; q0 < tb;) {  // a run stays inside one expert
+            const int q1 = min(tb, (q0 / FE + 1) * FE);
+            const size_t row = (size_t)F.ue_expert[q0 / FE] * FE + q0 % FE;
+            put_run(p, 0, T_GU, q0 - ta, q1 - q0, (const uint8_t*)Lg.w[EGATE] + row * RBH,
+                    (const uint8_t*)Lg.s[EGATE] + row * SBH, RBH, SBH);
+            put_run(p, 1, T_GU, q0 - ta, q1 - q0, (const uint8_t*)Lg.w[EUP] + row * RBH,
+                    (const uint8_t*)Lg.s[EUP] + row * SBH, RBH, SBH);
+            q0 = q1;
+          }
+          p.end();
+        }
+        const int cap = c.act_bytes / GE::ACT_BYTES;
+        const int nr = c.nr;
+#pragma unroll 1
+        for (int ua = 0; ua < F.n_ue;) {
+          const int ub = moe_round_end(F, ua, cap);
+          const int ntask = (ub - ua) * nr;
+#pragma unroll 1
+          for (int ta = 0; ta < ntask; ta += T_DN) {
+            if (!p.template begin<STAGE>()) return;
+            const int tb = min(ntask, ta + T_DN);
+#pragma unroll 1
+            for (int q0 = ta; q0 < tb;) {  // a run stays inside one expert
+              const int q1 = min(tb, (q0 / nr + 1) * nr);
+              const size_t row = (size_t)F.ue_expert[ua + q0 / nr] * H + c.r0 + q0 % nr;
+              put_run(p, 0, T_DN, q0 - ta, q1 - q0, (const uint8_t*)Lg.w[EDOWN] + row * GE::ROW_BYTES,
+                      (const uint8_t*)Lg.s[EDOWN] + row * GE::SCALE_BYTES, GE::ROW_BYTES, GE::SCALE_BYTES);
+              q0 = q1;
+            }
+            p.end();
+          }
+          ua = ub;
+        }
+      } else {
+        int f0, f1;
+        gu_range(c, FD, f0, f1);
+#pragma unroll 1
+        for (int t0 = f0; t0 < f1; t0 += T_GU) {
+          if (!p.template begin<STAGE>()) return;
+          const int cnt = min(T_GU, f1 - t0);
+          put_run(p, 0, T_GU, 0, cnt, (const uint8_t*)Lg.w[GATE] + (size_t)t0 * RBH,
+                  (const uint8_t*)Lg.s[GATE] + (size_t)t0 * SBH, RBH, SBH);
+          put_run(p, 1, T_GU, 0, cnt, (const uint8_t*)Lg.w[UP] + (size_t)t0 * RBH,
+                  (const uint8_t*)Lg.s[UP] + (size_t)t0 * SBH, RBH, SBH);
+          p.end();
+        }
+        const int cap = c.act_bytes / GD::ACT_BYTES;
+#pragma unroll 1
+        for (int ba = 0; ba < n; ba += cap) {
+#pragma unroll 1
+          for (int t0 = 0; t0 < c.nr; t0 += T_DD) {
+            if (!p.template begin<STAGE>()) return;
+            const size_t row = (size_t)(c.r0 + t0);
+            put_run(p, 0, T_DD, 0, min(T_DD, c.nr - t0), (const uint8_t*)Lg.w[DOWN] + row * GD::ROW_BYTES,
+                    (const uint8_t*)Lg.s[DOWN] + row * GD::SCALE_BYTES, GD::ROW_BYTES, GD::SCALE_BYTES);
+            p.end();
+          }
+        }
+      }
+    }
+    if (a.out_first < n) {
+      int v0, v1;
+      gu_range(c, a.vocab, v0, v1);
+#pragma unroll 1
+      for (int t0 = v0; t0 < v1; t0 += T_LM) {
+        if (!p.template begin<STAGE>()) return;
+        put_run(p, 0, T_LM, 0, min(T_LM, v1 - t0), (const uint8_t*)a.lm_head + (size_t)t0 * RBH,
+                (const uint8_t*)a.lm_head_s + (size_t)t0 * SBH, RBH, SBH);
+        p.end();
+      }
+    }
+  }
 };
 
 template <class S, int WDT>
-__global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepArgs a) {
+__global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_constant__ StepArgs a) {
   using M = Model<S, WDT>;
   extern __shared__ __align__(128) uint8_t smem[];
   Fixed& F = *reinterpret_cast<Fixed*>(smem);
@@ -953,7 +1270,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     const uint32_t* src = reinterpret_cast<const uint32_t*>(&a);
     uint32_t* dst = reinterpret_cast<uint32_t*>(&F.args);
     static_assert(sizeof(StepArgs) % 4 == 0, "word copy");
-    for (int i = tid; i < (int)(sizeof(StepArgs) / 4); i += kThreads) dst[i] = src[i];
+    for (int i = tid; i < (int)(sizeof(StepArgs) / 4); i += kBlockThreads) dst[i] = src[i];
   }
   const int n = a.n;
   if (tid == 0) {
@@ -963,9 +1280,18 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     c.bid = blockIdx.x;
     c.n = n;
     int r0, r1;
-    split_range(S::H, c.G, c.bid, r0, r1);
-    c.r0 = r0;
-    c.nr = r1 - r0;
+    split_range(S::H / M::A_H, c.G, c.bid, r0, r1);
+    c.r0 = r0 * M::A_H;
+    c.nr = (r1 - r0) * M::A_H;
+    // staging area, then the ring in what is left
+    const int avail = kSmemBytes - kActOffset;
+    int act = M::act_base_bytes(n);
+    const int want = n * S::TOPK * M::GE::ACT_BYTES;
+    if (want > act) act = max(act, min(want, avail - 3 * M::STAGE));
+    act = (act + 127) / 128 * 128;
+    c.act_bytes = act;
+    c.ring = smem + kActOffset + act;
+    c.ns = min(kMaxStages, (avail - act) / M::STAGE);
     c.tr_x = a.trace;
     c.tr_attn = a.trace ? c.tr_x + (size_t)a.n_layers * n * S::H : nullptr;
     c.tr_rl = a.trace ? c.tr_attn + (size_t)a.n_layers * n * M::QD : nullptr;
@@ -979,6 +1305,15 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
       acc += S::NKV * ((a.pos[b] + 1 + a.chunk - 1) / a.chunk);
     }
     F.unit_start[n] = acc;
+    F.kc = 0;
+    F.route_gen = 0;
+    F.abort = 0;
+    for (int s = 0; s < c.ns; ++s) {
+      mbar_init(&F.full[s], 1);
+      mbar_init(&F.empty[s], kWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (c.ns < 2) set_error(a.sc.err, MK_ERR_UNSUPPORTED, SITE_SMEM, c.ns);
   }
   // token ids (device memory; may be the previous step's output)
   if (tid < n) {
@@ -991,45 +1326,65 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
   }
   __syncthreads();
   const Ctx& c = F.ctx;
+  Producer prod;
 
-  uint32_t nbar = 0;
-  if (c.tm && tid == 0) c.tm[0] = globaltimer();
-  for (int l = 0; l < a.n_layers; ++l) {
-    {  // this layer's weight pointers into shared memory (read by every task)
+  if (tid >= kThreads) {
+    // streaming warp
+    if (c.ns >= 2) {
+      M::load_unit_pages();
+      if (tid == kThreads) M::produce(prod);
+    }
+    __syncwarp();
+  } else {
+    bool ok = c.ns >= 2;
+    uint32_t nbar = 0;
+    if (c.tm && tid == 0) c.tm[0] = globaltimer();
+    // the layer's norm / router pointers in shared memory; layer l + 1's are
+    // fetched once layer l's routing has used them, during gate/up
+    auto load_lw = [&](int l) {
       const uint32_t* src = reinterpret_cast<const uint32_t*>(a.layers + l);
       uint32_t* dst = reinterpret_cast<uint32_t*>(&F.lw);
       for (int i = tid; i < (int)(sizeof(LayerW) / 4); i += kThreads) dst[i] = __ldg(src + i);
-      __syncthreads();
+    };
+    load_lw(0);
+    csync();
+    for (int l = 0; ok && l < a.n_layers; ++l) {
+      M::qkv(l);
+      MK_STAMP(c, l, 0, 1);
+      if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
+      MK_STAMP(c, l, 0, 2);
+      M::attention(l);
+      MK_STAMP(c, l, 1, 1);
+      if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
+      MK_STAMP(c, l, 1, 2);
+      M::oproj(l);
+      MK_STAMP(c, l, 2, 1);
+      if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
+      MK_STAMP(c, l, 2, 2);
+      M::route(l);
+      csync();
+      if (l + 1 < a.n_layers) load_lw(l + 1);
+      M::gateup(l);
+      MK_STAMP(c, l, 3, 1);
+      if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
+      MK_STAMP(c, l, 3, 2);
+      if (l >= a.n_dense) M::template down<true>(l);
+      else M::template down<false>(l);
+      MK_STAMP(c, l, 4, 1);
+      if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
+      MK_STAMP(c, l, 4, 2);
     }
-    M::qkv(l);
-    MK_STAMP(c, l, 0, 1);
-    if (!grid_barrier(a, nbar)) goto done;
-    MK_STAMP(c, l, 0, 2);
-    M::attention(l);
-    MK_STAMP(c, l, 1, 1);
-    if (!grid_barrier(a, nbar)) goto done;
-    MK_STAMP(c, l, 1, 2);
-    M::oproj(l);
-    MK_STAMP(c, l, 2, 1);
-    if (!grid_barrier(a, nbar)) goto done;
-    MK_STAMP(c, l, 2, 2);
-    M::route(l);
-    __syncthreads();
-    M::gateup(l);
-    MK_STAMP(c, l, 3, 1);
-    if (!grid_barrier(a, nbar)) goto done;
-    MK_STAMP(c, l, 3, 2);
-    if (l >= a.n_dense) M::template down<true>(l);
-    else M::template down<false>(l);
-    MK_STAMP(c, l, 4, 1);
-    if (!grid_barrier(a, nbar)) goto done;
-    MK_STAMP(c, l, 4, 2);
+    if (ok && a.out_first < n) M::lm_head();
+    if (c.tm && tid == 0) c.tm[1 + 16 * a.n_layers] = globaltimer();
+    csync();
+    if (tid == 0 && !ok) F.abort = 1;
   }
-  if (a.out_first < n) M::lm_head();
-  if (c.tm && tid == 0) c.tm[1 + 16 * a.n_layers] = globaltimer();
-
-done:
   __syncthreads();
+  // every copy the streaming warp issued has landed before the block ends
+  if (tid >= kThreads) {
+    if (tid == kThreads) prod.drain();
+    __syncwarp();
+  }
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(a.sc.sync + 32, 1u) == (uint32_t)(c.G - 1)) {

@@ -147,6 +147,7 @@ extern "C" MK_API int mk_decode_step_static(
   for (int i = 0; i < n; ++i) {
     a.slot[i] = slots_host[i];
     a.pos[i] = positions_host[i];
+    a.new0[i] = positions_host[i];  // one row per sequence
     a.cur_page[i] = pages_host[i];
     a.upd[a.n_upd++] = PageUpd{slots_host[i], positions_host[i] / kPageTokens, pages_host[i]};
   }
@@ -181,7 +182,7 @@ extern "C" MK_API int mk_decode_step_static(
     e = cudaMemcpyAsync(base + off_layers, layers, sizeof(LayerW) * d->n_layers, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return host_fail(MK_ERR_CUDA, cudaGetErrorString(e));
   void* args[] = {&a};
-  e = cudaLaunchCooperativeKernel(kern.fn, dim3(grid), dim3(kThreads), args, (size_t)kern.smem_bytes, st);
+  e = cudaLaunchCooperativeKernel(kern.fn, dim3(grid), dim3(kBlockThreads), args, (size_t)kern.smem_bytes, st);
   if (e != cudaSuccess)
     return host_fail(MK_ERR_CUDA, (std::string("cudaLaunchCooperativeKernel: ") + cudaGetErrorString(e)).c_str());
   if (status_dev) {
