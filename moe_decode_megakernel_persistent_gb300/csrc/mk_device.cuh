@@ -385,43 +385,57 @@ struct Gemv {
 
 // Block-cooperative staging (the compute warps) of `rows` activation
 // vectors of K floats into the staged form of Gemv<WDT, K> (vector r at
-// dst + r * ACT_BYTES).  Thread t loads float4 number t (coalesced: the block
-// reads each vector as one contiguous stream), optionally RMS-normalises the
-// row (block reduction in a fixed order, so every block gets the same scale)
-// and multiplies by a weight, then writes its part of the staged chunk; for
-// int4 the 8 lanes holding one 32-value chunk agree on its scale and plane
-// sums with shuffles.
+// dst + r * ACT_BYTES).  A thread takes one 8-value word of a vector (two
+// float4, coalesced: the block reads each vector as one contiguous stream)
+// and, with norm, the matching norm weights in the same round trip;
+// optionally RMS-normalises the row (block reduction in a fixed order, so
+// every block gets the same scale), then writes its part of the staged
+// chunk.  For int4 the 4 threads holding one 32-value chunk agree on its
+// scale and plane sums with shuffles.
 //   LD(row, f4) -> float4 values 4*f4 .. 4*f4+3 of vector `row`
 //   WT(f4)      -> float4 weights (only with norm)
 //   red         -> shared scratch of kWarps * 4 floats
 //   rscale      -> if non-null, receives each row's RMS scale (shared memory)
-template <int WDT, int K, class LD, class WT>
-__device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, bool norm, float eps, WT wt,
-                                            float* red, float* rscale) {
+template <int WDT, int K, bool NORM, int RG, class LD, class WT>
+__device__ __noinline__ void stage_rows(uint8_t* dst, int rows, LD ld, float eps, WT wt, float* red,
+                                           float* rscale) {
   using Gv = Gemv<WDT, K>;
-  constexpr int NF4 = K / 4;
+  constexpr int NW = K / 8;                      // 8-value words per vector
   static_assert(K % 32 == 0, "vectors are whole chunks");
+  const bool norm = NORM;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  constexpr int RG = 4;                          // rows per pass
-  constexpr int PER = (RG * NF4 + kThreads - 1) / kThreads;
+  constexpr int PER = (RG * NW + kThreads - 1) / kThreads;  // RG rows per pass
   for (int r0 = 0; r0 < rows; r0 += RG) {
     const int nrg = min(RG, rows - r0);
-    float4 v[PER];
+    float4 va[PER], vb[PER], wa[NORM ? PER : 1], wb[NORM ? PER : 1];
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int it = tid + i * kThreads;
-      if (it < nrg * NF4) v[i] = ld(r0 + it / NF4, it % NF4);
+      if (it < nrg * NW) {
+        const int row = it / NW, w = it % NW;
+        va[i] = ld(r0 + row, 2 * w);
+        vb[i] = ld(r0 + row, 2 * w + 1);
+        if constexpr (NORM) {
+          wa[i] = wt(2 * w);
+          wb[i] = wt(2 * w + 1);
+        }
+      }
     }
-    float rs[RG] = {1.f, 1.f, 1.f, 1.f};
+    float rs[RG];
+#pragma unroll
+    for (int g = 0; g < RG; ++g) rs[g] = 1.f;
     if (norm) {
-      float ss[RG] = {0.f, 0.f, 0.f, 0.f};
+      float ss[RG];
+#pragma unroll
+      for (int g = 0; g < RG; ++g) ss[g] = 0.f;
 #pragma unroll
       for (int i = 0; i < PER; ++i) {
         const int it = tid + i * kThreads;
-        if (it < nrg * NF4) {
-          const float q = v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+        if (it < nrg * NW) {
+          const float q = va[i].x * va[i].x + va[i].y * va[i].y + va[i].z * va[i].z + va[i].w * va[i].w +
+                          vb[i].x * vb[i].x + vb[i].y * vb[i].y + vb[i].z * vb[i].z + vb[i].w * vb[i].w;
 #pragma unroll
-          for (int g = 0; g < RG; ++g) ss[g] += (it / NF4 == g) ? q : 0.f;
+          for (int g = 0; g < RG; ++g) ss[g] += (it / NW == g) ? q : 0.f;
         }
       }
 #pragma unroll
@@ -442,80 +456,92 @@ __device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, bool 
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int it = tid + i * kThreads;
-      // int4 chunks span 8 consecutive lanes, so the whole warp takes part in
-      // the shuffles; lanes past the end are predicated off (no continue: the
-      // loop stays unrolled and v[] stays in registers)
-      const bool live = it < nrg * NF4;
+      // int4 chunks span 4 consecutive threads, so the whole warp takes part
+      // in the shuffles; threads past the end are predicated off (no
+      // continue: the loop stays unrolled and the arrays stay in registers)
+      const bool live = it < nrg * NW;
       const bool warp_live = WDT == WINT4 ? __any_sync(0xffffffffu, live) : live;
       if (warp_live) {
-        const int row = live ? it / NF4 : 0, f4 = live ? it % NF4 : 0;
-        float4 y = live ? v[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-        if (norm && live) {
-          const float4 w = wt(f4);
+        const int row = live ? it / NW : 0, w = live ? it % NW : 0;
+        float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (live) {
           float r = rs[0];
 #pragma unroll
           for (int g = 1; g < RG; ++g) r = row == g ? rs[g] : r;
-          y = make_float4(y.x * r * w.x, y.y * r * w.y, y.z * r * w.z, y.w * r * w.w);
+          float4 ma = make_float4(1.f, 1.f, 1.f, 1.f), mb = ma;
+          if constexpr (NORM) {
+            ma = make_float4(r * wa[i].x, r * wa[i].y, r * wa[i].z, r * wa[i].w);
+            mb = make_float4(r * wb[i].x, r * wb[i].y, r * wb[i].z, r * wb[i].w);
+          }
+          y[0] = va[i].x * ma.x; y[1] = va[i].y * ma.y; y[2] = va[i].z * ma.z; y[3] = va[i].w * ma.w;
+          y[4] = vb[i].x * mb.x; y[5] = vb[i].y * mb.y; y[6] = vb[i].z * mb.z; y[7] = vb[i].w * mb.w;
         }
         uint8_t* base = dst + (r0 + row) * Gv::ACT_BYTES;
         if constexpr (WDT == WINT4) {
-          // chunk c = f4 / 8 (32 values) lives in lanes 8j .. 8j+7
-          float amax = fmaxf(fmaxf(fabsf(y.x), fabsf(y.y)), fmaxf(fabsf(y.z), fabsf(y.w)));
+          // chunk c = w / 4 (32 values) lives in threads 4j .. 4j+3; word t of
+          // the chunk holds values 8t .. 8t+7
+          float amax = 0.f;
 #pragma unroll
-          for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(y[e]));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
           // 24-bit fixed point, |q| <= 2^23 - 1, split into byte planes
-          const float inv = amax > 0.f ? 8388607.f / amax : 0.f;
-          const float yv[4] = {y.x, y.y, y.z, y.w};
-          int q[4];
+          const float inv = amax > 0.f ? __fdividef(8388607.f, amax) : 0.f;
+          int q[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) q[e] = max(-8388607, min(8388607, __float2int_rn(yv[e] * inv)));
-          int s0 = 0, s1 = 0, s2 = 0;
-          uint32_t pk[3];  // per plane: bytes of values (0, 2) | (1, 3) << 16
+          for (int e = 0; e < 8; ++e) q[e] = max(-8388607, min(8388607, __float2int_rn(y[e] * inv)));
+          int s01 = 0, s2 = 0;  // low + (middle << 16), high
 #pragma unroll
-          for (int pl = 0; pl < 3; ++pl) {
-            uint32_t b[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) b[e] = (uint32_t)(q[e] >> (8 * pl)) & 0xFFu;
-            pk[pl] = b[0] | (b[2] << 8) | (b[1] << 16) | (b[3] << 24);
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            s0 += q[e] & 0xFF;
-            s1 += (q[e] >> 8) & 0xFF;
+          for (int e = 0; e < 8; ++e) {
+            s01 += (q[e] & 0xFF) + (((q[e] >> 8) & 0xFF) << 16);
             s2 += q[e] >> 16;
           }
-#pragma unroll
-          for (int o = 1; o < 8; o <<= 1) {
-            s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-            s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-          }
-          uint32_t opk[3];
-#pragma unroll
-          for (int pl = 0; pl < 3; ++pl) opk[pl] = __shfl_xor_sync(0xffffffffu, pk[pl], 1);
-          // word t = (f4 % 8) / 2 holds values 8t .. 8t+7 of the chunk: the
-          // even lane of the pair has values 0-3, the odd lane 4-7
-          const int c = f4 >> 3, t = (f4 & 7) >> 1;
-          if (live && (f4 & 1) == 0) {
+          s01 += __shfl_xor_sync(0xffffffffu, s01, 1);
+          s2 += __shfl_xor_sync(0xffffffffu, s2, 1);
+          s01 += __shfl_xor_sync(0xffffffffu, s01, 2);
+          s2 += __shfl_xor_sync(0xffffffffu, s2, 2);
+          const int c = w >> 2, t = w & 3;
+          if (live) {
 #pragma unroll
             for (int pl = 0; pl < 3; ++pl) {
-              const uint32_t ev = (pk[pl] & 0xFFFFu) | (opk[pl] << 16);
-              const uint32_t od = (pk[pl] >> 16) | (opk[pl] & 0xFFFF0000u);
+              uint32_t b[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) b[e] = (uint32_t)(q[e] >> (8 * pl)) & 0xFFu;
+              const uint32_t ev = b[0] | (b[2] << 8) | (b[4] << 16) | (b[6] << 24);
+              const uint32_t od = b[1] | (b[3] << 8) | (b[5] << 16) | (b[7] << 24);
               *reinterpret_cast<uint32_t*>(base + ((2 * pl) * Gv::NCH + c) * 16 + 4 * t) = ev;
               *reinterpret_cast<uint32_t*>(base + ((2 * pl + 1) * Gv::NCH + c) * 16 + 4 * t) = od;
             }
             if (t == 0)
               *reinterpret_cast<int4*>(base + Gv::NCH * Gv::SUBS * 16 + c * 16) =
-                  make_int4(__float_as_int(amax * (1.f / 8388607.f)), 8 * s2, 8 * s1, 8 * s0);
+                  make_int4(__float_as_int(amax * (1.f / 8388607.f)), 8 * s2, 8 * (s01 >> 16), 8 * (s01 & 0xFFFF));
           }
-        } else {
+        } else if (live) {
           // chunk c holds VPC values = VPC/4 float4; sub t of chunk c at (t*NCH + c)*16
-          const int c = f4 / (Gv::VPC / 4), t = f4 % (Gv::VPC / 4);
-          if (live) *reinterpret_cast<float4*>(base + (t * Gv::NCH + c) * 16) = y;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int f4 = 2 * w + h;
+            const int c = f4 / (Gv::VPC / 4), t = f4 % (Gv::VPC / 4);
+            *reinterpret_cast<float4*>(base + (t * Gv::NCH + c) * 16) =
+                make_float4(y[4 * h], y[4 * h + 1], y[4 * h + 2], y[4 * h + 3]);
+          }
         }
       }
     }
   }
+}
+
+// Staging entry: one row per pass for a single row (fewest registers);
+// otherwise four rows per pass with a norm (one load round trip and one norm
+// reduction for four rows) and, without one, as many rows as fit two words
+// per thread.
+template <int WDT, int K, bool NORM, class LD, class WT>
+__device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, float eps, WT wt, float* red,
+                                            float* rscale) {
+  // without a norm, as many rows per pass as two words per thread cover
+  constexpr int RGM = NORM ? 4 : ((2 * kThreads) / (K / 8) > 1 ? (2 * kThreads) / (K / 8) : 1);
+  if (rows == 1) stage_rows<WDT, K, NORM, 1>(dst, rows, ld, eps, wt, red, rscale);
+  else stage_rows<WDT, K, NORM, RGM>(dst, rows, ld, eps, wt, red, rscale);
 }
 
 __device__ __forceinline__ void split_range(int n, int parts, int idx, int& lo, int& hi) {

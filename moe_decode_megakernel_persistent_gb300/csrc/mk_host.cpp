@@ -398,7 +398,7 @@ MK_API int mk_create(const mk_model_desc* d, const mk_weights* w, mk_ctx** out) 
   }
   c->num_sms = prop.multiProcessorCount;
   c->grid = c->num_sms;
-  if ((d->hidden + c->grid - 1) / c->grid > kMaxRowsPerBlock) {
+  if ((d->hidden / 4 + c->grid - 1) / c->grid * 4 > kMaxRowsPerBlock) {
     delete c;
     return fail(MK_ERR_UNSUPPORTED, "too few SMs for the compiled per-block row budget");
   }
@@ -569,10 +569,12 @@ MK_API int mk_sync(mk_ctx* c, void* stream) {
   MK_CUDA(cudaMemcpy(err, c->sc.err, sizeof(err), cudaMemcpyDeviceToHost));
   if (err[0] != 0) {
     MK_CUDA(cudaMemset(c->sc.err, 0, sizeof(err)));
-    static const char* sites[] = {"?", "grid barrier", "page table", "attention unit", "token id"};
-    const int site = err[1] >= 1 && err[1] <= 4 ? err[1] : 0;
+    static const char* sites[] = {"?", "grid barrier", "page table", "attention unit", "token id",
+                                  "weight ring", "shared-memory plan"};
+    const int site = err[1] >= 1 && err[1] <= 6 ? err[1] : 0;
     return fail(err[0], std::string("device reported error ") + std::to_string(err[0]) + " at " +
-                            sites[site] + " (detail " + std::to_string(err[2]) + ")");
+                            sites[site] + " (site " + std::to_string(err[1]) + ", detail " +
+                            std::to_string(err[2]) + ", " + std::to_string(err[3]) + ")");
   }
   return MK_OK;
 }

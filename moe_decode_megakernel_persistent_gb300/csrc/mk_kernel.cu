@@ -54,6 +54,7 @@ struct Fixed {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint32_t kc;            // ring items consumed so far by the compute warps
+  uint32_t prod_k;        // ring items issued by the streaming warp (for the exit drain)
   volatile int route_gen; // l + 1 once layer l's routing tables are ready
   volatile int abort;     // compute warps left the step early
   volatile int ok_word;   // grid barrier outcome broadcast
@@ -62,6 +63,7 @@ struct Fixed {
   float topk_w[kMaxBatch][8];
   float dots[kMaxEnt][kMaxRowsPerBlock];
   float hs[kMaxBatch][kMaxRowsPerBlock];
+  uint32_t nslw[kMaxRowsPerBlock];  // raw slice of the post-attention norm weights
   float red[kThreads];
   float best_v[kWarps][kMaxBatch];
   int best_i[kWarps][kMaxBatch];
@@ -71,6 +73,7 @@ struct Fixed {
   int16_t ue_expert[64], ue_start[64], ue_len[64];
   uint8_t ent_b[kMaxEnt], ent_j[kMaxEnt];
   uint8_t ent_of[kMaxBatch][8];
+  uint8_t efirst[kMaxEnt];
   int n_ue, flag;
 };
 constexpr int kActOffset = (sizeof(Fixed) + 127) / 128 * 128;
@@ -128,7 +131,9 @@ struct Producer {
   __device__ __forceinline__ bool begin() {
     Fixed& F = fixed();
     if (dead) return false;
-    if (F.abort || *(volatile int32_t*)F.args.sc.err != 0) { dead = true; return false; }
+    // the shared abort flag only: a global error-word read here would cost an
+    // L2 round trip per item (the waits below poll it while they spin)
+    if (F.abort) { dead = true; return false; }
     const uint32_t ns = (uint32_t)F.ctx.ns;
     const int s = (int)(k % ns);
     const uint32_t round = k / ns;
@@ -196,7 +201,9 @@ struct Model {
   __host__ __device__ static constexpr int cmax(int a, int b) { return a > b ? a : b; }
   // task ranges and tiles start at multiples of A rows (16-byte aligned scales)
   static constexpr int A_Q = GH::A;
-  static constexpr int A_H = cmax(GQ::A, cmax(GE::A, GD::A));
+  // hidden rows go to blocks in groups of at least 2, so a block's slice of
+  // a bf16 row (router, norm) starts and ends on a 4-byte boundary
+  static constexpr int A_H = cmax(2, cmax(GQ::A, cmax(GE::A, GD::A)));
   __host__ __device__ static constexpr int tmax(int rp, int rb, int sb, int al) {
     int t = STD / (rp * rb);
     if (sb) t = t < AUXB / (rp * sb) ? t : AUXB / (rp * sb);
@@ -267,9 +274,11 @@ struct Model {
   }
 
   // ---- generic GEMV over ring tiles.  Tasks [0, ntask) of the phase, T per
-  // ring item; task t runs on warp t % kWarps.  TK provides
+  // ring item; task t runs on warp t % kWarps, or (CONTIG) each warp takes a
+  // contiguous block of a tile's tasks (tasks sharing an activation stay on
+  // one warp, whose activation registers then reload rarely).  TK provides
   //   ActRange acts(t) and void out(t, ai, i, v0, v1) (all lanes).
-  template <int K, int RP, int T, bool REGS, class TK>
+  template <int K, int RP, int T, bool REGS, bool CONTIG, class TK>
   __device__ static __forceinline__ void run_gemv(int ntask, const uint8_t* act_base, const TK& task) {
     using Gv = Gemv<WDT, K>;
     Fixed& F = fixed();
@@ -281,8 +290,11 @@ struct Model {
     for (int t0 = 0; t0 < ntask; t0 += T, ++k) {
       const uint8_t* st = ring_acquire<STAGE>(k);
       const int tn = min(T, ntask - t0);
+      const int per = (tn + kWarps - 1) / kWarps;
+      const int j_first = CONTIG ? wid * per : ((wid - t0) % kWarps + kWarps) % kWarps;
+      const int j_end = CONTIG ? min(tn, j_first + per) : tn;
 #pragma unroll 1
-      for (int j = ((wid - t0) % kWarps + kWarps) % kWarps; j < tn; j += kWarps) {
+      for (int j = j_first; j < j_end; j += CONTIG ? 1 : kWarps) {
         const int t = t0 + j;
         const uint8_t* wr[2];
         const uint8_t* sr[2];
@@ -312,6 +324,34 @@ struct Model {
     csync();
   }
 
+  // This block's slice of the layer's router weights (E rows x nr columns)
+  // and of its post-attention norm, copied into shared memory with
+  // asynchronous 4-byte copies (F.dots holds the router slice: it is free
+  // from P1 to P3).  The slices are 4-byte aligned: r0 and nr are multiples
+  // of A_H >= 2.
+  __device__ static __forceinline__ void fetch_router_slice(const LayerW& Lw) {
+    Fixed& F = fixed();
+    const Ctx& c = F.ctx;
+    constexpr int VPW = AUX == WF32 ? 1 : 2;  // values per 4-byte word
+    const int words = c.nr / VPW;
+    uint32_t* rs = reinterpret_cast<uint32_t*>(&F.dots[0][0]);
+    const uint8_t* rb = reinterpret_cast<const uint8_t*>(Lw.router);
+    constexpr int VB = AUX == WF32 ? 4 : 2;
+    for (int idx = threadIdx.x; idx < (E + 1) * words; idx += kThreads) {
+      const int e = idx / words, w = idx % words;
+      const uint8_t* src = e < E ? rb + ((size_t)e * H + c.r0) * VB + 4 * w
+                                 : reinterpret_cast<const uint8_t*>(Lw.ffn_norm) + (size_t)c.r0 * VB + 4 * w;
+      uint32_t* dst = e < E ? rs + e * kMaxRowsPerBlock + w : F.nslw + w;
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  // value t of a raw slice row (bf16 pairs or fp32 words)
+  __device__ static __forceinline__ float slice_val(const uint32_t* row, int t) {
+    if constexpr (AUX == WF32) return __uint_as_float(row[t]);
+    else return bf16_to_f((row[t >> 1] >> (16 * (t & 1))) & 0xFFFFu);
+  }
+
   // ---------------------------------------------------------------- P1
   // RMSNorm of the residual (every block, redundantly) -> this block's QKV
   // tasks.  A task is a RoPE pair of rows (i, i + HD/2) of one q, k or v head,
@@ -329,19 +369,20 @@ struct Model {
         a.block_table[a.upd[i].slot * a.max_pages_per_seq + a.upd[i].index] = a.upd[i].page;
     if (c.bid == 0 && l >= a.n_dense)  // router logits are accumulated in P3
       for (int i = tid; i < n * E; i += kThreads) a.sc.rlogit[i] = 0.f;
+    if (l >= a.n_dense) fetch_router_slice(Lw);
     {
       const void* nw = Lw.attn_norm;
       const void* embed = a.embed;
       const float* x = a.sc.x;
       const int* tok = F.tok;
       const bool first = l == 0;
-      stage_block<WDT, H>(
+      stage_block<WDT, H, true>(
           c.act, n,
           [&](int r, int f4) -> float4 {
             return first ? ld_aux4<AUX>(embed, (size_t)tok[r] * (H / 4) + f4)
                          : __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4);
           },
-          true, a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
+          a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
     }
     if (l == 0)  // residual rows this block reads back in P3
       for (int i = tid; i < n * c.nr; i += kThreads) {
@@ -383,7 +424,7 @@ struct Model {
         }
       }
     } task{&a, p0, l, lane};
-    run_gemv<H, 2, T_QKV, false>(p1 - p0, c.act, task);
+    run_gemv<H, 2, T_QKV, false, false>(p1 - p0, c.act, task);
   }
 
   // K/V rows of TU positions into registers (bf16 -> float), from shared
@@ -401,18 +442,21 @@ struct Model {
     }
   }
 
-  // One online-softmax update of a warp's GQA heads with TU positions (K and
-  // V row pointers per position, `ok` false for padding positions).
+  // K and V rows of TU positions into registers.
   template <bool GL>
-  __device__ static __forceinline__ void attend(const uint16_t* const (&kp)[TU], const uint16_t* const (&vp)[TU],
-                                                const bool (&ok)[TU], const float (&q)[GQA][DPL], float (&m)[GQA],
-                                                float (&lsum)[GQA], float (&o)[GQA][DPL], int lane) {
-    float kf[TU][DPL], vf[TU][DPL];
+  __device__ static __forceinline__ void ld_tokens(const uint16_t* const (&kp)[TU], const uint16_t* const (&vp)[TU],
+                                                   float (&kf)[TU][DPL], float (&vf)[TU][DPL]) {
 #pragma unroll
     for (int k = 0; k < TU; ++k) {
       ld_kv<GL>(kp[k], kf[k]);
       ld_kv<GL>(vp[k], vf[k]);
     }
+  }
+  // One online-softmax update of a warp's GQA heads with TU positions
+  // (`ok` false for padding positions).
+  __device__ static __forceinline__ void attend(const float (&kf)[TU][DPL], const float (&vf)[TU][DPL],
+                                                const bool (&ok)[TU], const float (&q)[GQA][DPL], float (&m)[GQA],
+                                                float (&lsum)[GQA], float (&o)[GQA][DPL], int lane) {
     // scores of the TU positions for the GQA heads: lane partials, one
     // transposing reduction for all of them, then broadcast back
     constexpr int NV = TU * GQA;
@@ -499,29 +543,9 @@ struct Model {
 #pragma unroll
         for (int d = 0; d < DPL; ++d) o[i][d] = 0.f;
       }
-#pragma unroll 1
-      for (int tb = t0; tb < rt1; tb += TT, ++k) {
-        const uint8_t* st = ring_acquire<STAGE>(k);
-        const int nt = min(TT, rt1 - tb);
-        const uint16_t* kp[TU];
-        const uint16_t* vp[TU];
-        bool ok[TU];
-#pragma unroll
-        for (int i = 0; i < TU; ++i) {
-          const int j = wid + kWarps * i;
-          ok[i] = j < nt;
-          const int jj = ok[i] ? j : 0;
-          kp[i] = reinterpret_cast<const uint16_t*>(st + (size_t)jj * HD * 2) + lane * DPL;
-          vp[i] = reinterpret_cast<const uint16_t*>(st + (size_t)(TT + jj) * HD * 2) + lane * DPL;
-        }
-        attend<false>(kp, vp, ok, q, m, lsum, o, lane);
-        ring_release(k);
-      }
-#pragma unroll 1
-      for (int tb = rt1; tb < t1; tb += kWarps * TU) {
-        const uint16_t* kp[TU];
-        const uint16_t* vp[TU];
-        bool ok[TU];
+      // positions this launch wrote (global memory): the first batch is
+      // requested now, so its latency overlaps the ring tiles
+      auto new_tokens = [&](int tb, const uint16_t* (&kp)[TU], const uint16_t* (&vp)[TU], bool (&ok)[TU]) {
 #pragma unroll
         for (int i = 0; i < TU; ++i) {
           const int t = tb + wid + kWarps * i;
@@ -539,7 +563,45 @@ struct Model {
           kp[i] = a.kv + Kv<S>::offset(l, a.n_pages, page, 0, g, tt % kPageTokens) + lane * DPL;
           vp[i] = a.kv + Kv<S>::offset(l, a.n_pages, page, 1, g, tt % kPageTokens) + lane * DPL;
         }
-        attend<true>(kp, vp, ok, q, m, lsum, o, lane);
+      };
+      float nkf[TU][DPL], nvf[TU][DPL];
+      bool nok[TU];
+      if (rt1 < t1) {
+        const uint16_t* kp[TU];
+        const uint16_t* vp[TU];
+        new_tokens(rt1, kp, vp, nok);
+        ld_tokens<true>(kp, vp, nkf, nvf);
+      }
+#pragma unroll 1
+      for (int tb = t0; tb < rt1; tb += TT, ++k) {
+        const uint8_t* st = ring_acquire<STAGE>(k);
+        const int nt = min(TT, rt1 - tb);
+        const uint16_t* kp[TU];
+        const uint16_t* vp[TU];
+        bool ok[TU];
+#pragma unroll
+        for (int i = 0; i < TU; ++i) {
+          const int j = wid + kWarps * i;
+          ok[i] = j < nt;
+          const int jj = ok[i] ? j : 0;
+          kp[i] = reinterpret_cast<const uint16_t*>(st + (size_t)jj * HD * 2) + lane * DPL;
+          vp[i] = reinterpret_cast<const uint16_t*>(st + (size_t)(TT + jj) * HD * 2) + lane * DPL;
+        }
+        float kf[TU][DPL], vf[TU][DPL];
+        ld_tokens<false>(kp, vp, kf, vf);
+        attend(kf, vf, ok, q, m, lsum, o, lane);
+        ring_release(k);
+      }
+      if (rt1 < t1) attend(nkf, nvf, nok, q, m, lsum, o, lane);
+#pragma unroll 1
+      for (int tb = rt1 + kWarps * TU; tb < t1; tb += kWarps * TU) {
+        const uint16_t* kp[TU];
+        const uint16_t* vp[TU];
+        bool ok[TU];
+        new_tokens(tb, kp, vp, ok);
+        float kf[TU][DPL], vf[TU][DPL];
+        ld_tokens<true>(kp, vp, kf, vf);
+        attend(kf, vf, ok, q, m, lsum, o, lane);
       }
 #pragma unroll
       for (int i = 0; i < GQA; ++i) {
@@ -596,7 +658,7 @@ struct Model {
 
   // Last unit of (b, g): log-sum-exp merge of its chunks into the attention
   // output.
-  __device__ static __forceinline__ void merge(int l, int b, int g, int nch) {
+  __device__ static __noinline__ void merge(int l, int b, int g, int nch) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
@@ -607,6 +669,24 @@ struct Model {
       return;
     }
     const float* pb = a.sc.part + (size_t)(F.unit_start[b] + g * nch) * GQA * PR;
+    // float4 output o = (head, 4 dims) is summed by NG thread groups over
+    // chunks grp, grp + NG, ...; the first batch of chunk outputs is requested
+    // together with the (m, l) pairs, so the merge costs one L2 round trip
+    constexpr int NOUT4 = GQA * HD / 4;
+    constexpr int NG = kThreads / NOUT4;
+    constexpr int BATCH = 12;
+    static_assert(NG >= 1, "one float4 output per thread at least");
+    const bool sum_thread = tid < NG * NOUT4;
+    const int grp = tid / NOUT4, o4 = tid % NOUT4, hi = o4 / (HD / 4), d4 = o4 % (HD / 4);
+    float4 ov[BATCH];
+    if (sum_thread) {
+#pragma unroll
+      for (int u2 = 0; u2 < BATCH; ++u2) {
+        const int cc = grp + u2 * NG;
+        ov[u2] = cc < nch ? __ldcg(reinterpret_cast<const float4*>(pb + (cc * GQA + hi) * PR + 4) + d4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
     // one warp per head: M = max_c m_c, L = sum_c l_c exp(m_c - M), and the
     // chunk factors exp(m_c - M) / L into shared memory
     float* mfac = F.red;  // [nch][GQA]
@@ -631,46 +711,38 @@ struct Model {
       }
     }
     csync();
-    // weighted sum of the chunk outputs: float4 output o = (head, 4 dims) is
-    // summed by NG thread groups over chunks grp, grp + NG, ... (all of a
-    // group's loads in flight together), then the groups in a fixed order
-    constexpr int NOUT4 = GQA * HD / 4;
-    constexpr int NG = kThreads / NOUT4;
-    constexpr int BATCH = 12;
-    static_assert(NG >= 1, "one float4 output per thread at least");
     float4* gsum = reinterpret_cast<float4*>(c.act);  // [NG][NOUT4] (the combine area is free now)
-    if (tid < NG * NOUT4) {
-      const int grp = tid / NOUT4, o = tid % NOUT4, i = o / (HD / 4), d4 = o % (HD / 4);
+    if (sum_thread) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c0 = grp; c0 < nch; c0 += NG * BATCH) {
-        float4 ov[BATCH];
+      for (int c0 = grp;; c0 += NG * BATCH) {
 #pragma unroll
         for (int u2 = 0; u2 < BATCH; ++u2) {
           const int cc = c0 + u2 * NG;
-          ov[u2] = cc < nch ? __ldcg(reinterpret_cast<const float4*>(pb + (cc * GQA + i) * PR + 4) + d4)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u2 = 0; u2 < BATCH; ++u2) {
-          const int cc = c0 + u2 * NG;
-          const float f = cc < nch ? mfac[cc * GQA + i] : 0.f;
+          const float f = cc < nch ? mfac[cc * GQA + hi] : 0.f;
           acc.x = fmaf(ov[u2].x, f, acc.x);
           acc.y = fmaf(ov[u2].y, f, acc.y);
           acc.z = fmaf(ov[u2].z, f, acc.z);
           acc.w = fmaf(ov[u2].w, f, acc.w);
         }
+        if (c0 + NG * BATCH >= nch) break;
+#pragma unroll
+        for (int u2 = 0; u2 < BATCH; ++u2) {  // further chunks (long contexts)
+          const int cc = c0 + NG * BATCH + u2 * NG;
+          ov[u2] = cc < nch ? __ldcg(reinterpret_cast<const float4*>(pb + (cc * GQA + hi) * PR + 4) + d4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
-      gsum[grp * NOUT4 + o] = acc;
+      gsum[grp * NOUT4 + o4] = acc;
     }
     csync();
     if (tid < NOUT4) {
-      const int i = tid / (HD / 4), d4 = tid % (HD / 4);
+      const int i = tid / (HD / 4), dd = tid % (HD / 4);
       float4 o = gsum[tid];
-      for (int grp = 1; grp < NG; ++grp) {
-        const float4 v = gsum[grp * NOUT4 + tid];
+      for (int gg = 1; gg < NG; ++gg) {
+        const float4 v = gsum[gg * NOUT4 + tid];
         o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w;
       }
-      const size_t off = (size_t)(g * GQA + i) * HD + 4 * d4;
+      const size_t off = (size_t)(g * GQA + i) * HD + 4 * dd;
       *reinterpret_cast<float4*>(a.sc.attn + b * QD + off) = o;
       if (c.tr_attn) *reinterpret_cast<float4*>(c.tr_attn + ((size_t)l * n + b) * QD + off) = o;
     }
@@ -691,9 +763,9 @@ struct Model {
     const int n = c.n;
     {
       const float* at = a.sc.attn;
-      stage_block<WDT, QD>(
+      stage_block<WDT, QD, false>(
           c.act, n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(at + r * QD) + f4); },
-          false, 0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
+          0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
     }
     csync();
     MK_STAMP(c, l, 2, 0);
@@ -707,13 +779,17 @@ struct Model {
         F->hs[b][t] = hv;
       }
     } task{&a, &F, c.r0, lane};
-    run_gemv<QD, 1, T_O, false>(c.nr, c.act, task);
+    run_gemv<QD, 1, T_O, false, false>(c.nr, c.act, task);
     if (l < a.n_dense) return;
+    // the router / norm slices requested in P1 have landed
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    csync();
+    const uint32_t* rs = reinterpret_cast<const uint32_t*>(&F.dots[0][0]);
     for (int idx = tid; idx < n * E; idx += kThreads) {
       const int b = idx / E, e = idx % E;
       float s = 0.f;
       for (int t = 0; t < c.nr; ++t)
-        s = fmaf(F.hs[b][t] * ld_aux<AUX>(Lw.ffn_norm, c.r0 + t), ld_aux<AUX>(Lw.router, e * H + c.r0 + t), s);
+        s = fmaf(F.hs[b][t] * slice_val(F.nslw, t), slice_val(rs + e * kMaxRowsPerBlock, t), s);
       // every block adds its partial; after the grid barrier all blocks read
       // the same totals (the order of the additions may differ run to run)
       atomicAdd(a.sc.rlogit + b * E + e, s);
@@ -736,74 +812,65 @@ struct Model {
     const LayerW& Lw = F.lw;
     const bool moe = l >= a.n_dense;
     const int n = c.n;
-    constexpr int EJ = (E + 31) / 32;
     if (moe) {
-      for (int b = wid; b < n; b += kWarps) {
-        float lg[EJ];
-#pragma unroll
-        for (int j = 0; j < EJ; ++j) {
-          const int e = lane + 32 * j;
-          lg[j] = e < E ? __ldcg(a.sc.rlogit + b * E + e) : -INFINITY;
+      // partial logits into shared memory (F.dots is free between P3 and P5)
+      float* lg = &F.dots[0][0];
+      for (int i = tid; i < n * E; i += kThreads) lg[i] = __ldcg(a.sc.rlogit + i);
+      for (int i = tid; i < n * TOPK; i += kThreads) F.topk_id[i / TOPK][i % TOPK] = i % TOPK;  // valid ids
+      if (tid == 0) F.n_ue = 0;
+      csync();
+      // rank of each (row, expert) = experts with a larger partial logit, ties
+      // to the lower id; the selection is the ranks below k (the same set and
+      // order as k rounds of argmax)
+      for (int i = tid; i < n * E; i += kThreads) {
+        const int b = i / E, e = i % E;
+        const float v = lg[i];
+        int rank = 0;
+#pragma unroll 8
+        for (int e2 = 0; e2 < E; ++e2) {
+          const float w = lg[b * E + e2];
+          rank += (w > v) || (w == v && e2 < e);
         }
-#pragma unroll
-        for (int kk = 0; kk < TOPK; ++kk) {
-          float bv = -INFINITY;
-          int be = INT_MAX;
-#pragma unroll
-          for (int j = 0; j < EJ; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E && (lg[j] > bv || (lg[j] == bv && e < be))) { bv = lg[j]; be = e; }
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-          }
-          if (lane == 0) { F.topk_id[b][kk] = be; F.topk_w[b][kk] = bv; }  // partial logit for now
-#pragma unroll
-          for (int j = 0; j < EJ; ++j)
-            if (lane + 32 * j == be) lg[j] = -INFINITY;
+        if (rank < TOPK) {
+          F.topk_id[b][rank] = e;
+          F.topk_w[b][rank] = v;  // partial logit for now
         }
       }
       csync();
-      if (wid == 0) {
-        // entries sorted by (expert, row, slot); one run of rows per distinct expert
-        int base = 0, nue = 0;
-#pragma unroll
-        for (int j = 0; j < EJ; ++j) {
-          const int e = lane + 32 * j;
-          int cnt = 0;
-          for (int b = 0; b < n; ++b)
-            for (int kk = 0; kk < TOPK; ++kk) cnt += F.topk_id[b][kk] == e;
-          const int has = cnt > 0;
-          int incl = cnt, hincl = has;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            const int hy = __shfl_up_sync(0xffffffffu, hincl, o);
-            if (lane >= o) { incl += y; hincl += hy; }
-          }
-          const int start = base + incl - cnt;
-          const int ue = nue + hincl - has;
-          if (has) {
-            F.ue_expert[ue] = (int16_t)e;
-            F.ue_start[ue] = (int16_t)start;
-            F.ue_len[ue] = (int16_t)cnt;
-            int pos = start;
-            for (int b = 0; b < n; ++b)
-              for (int kk = 0; kk < TOPK; ++kk)
-                if (F.topk_id[b][kk] == e) {
-                  F.ent_b[pos] = (uint8_t)b;
-                  F.ent_j[pos] = (uint8_t)kk;
-                  F.ent_of[b][kk] = (uint8_t)pos;
-                  ++pos;
-                }
-          }
-          base += __shfl_sync(0xffffffffu, incl, 31);
-          nue += __shfl_sync(0xffffffffu, hincl, 31);
+      // entries (row, slot) sorted by (expert, row, slot); one run of entries
+      // per distinct expert
+      const int N = n * TOPK;
+      int my_e = 0, my_pos = 0;
+      bool my_first = false;
+      if (tid < N) {
+        const int b = tid / TOPK, k = tid % TOPK;
+        my_e = F.topk_id[b][k];
+        int pos = 0;
+        bool first = true;
+        for (int j = 0; j < N; ++j) {
+          const int e2 = F.topk_id[j / TOPK][j % TOPK];
+          pos += (e2 < my_e) || (e2 == my_e && j < tid);
+          first = first && !(e2 == my_e && j < tid);
         }
-        if (lane == 0) F.n_ue = nue;
+        F.ent_b[pos] = (uint8_t)b;
+        F.ent_j[pos] = (uint8_t)k;
+        F.ent_of[b][k] = (uint8_t)pos;
+        F.efirst[tid] = first;
+        my_pos = pos;
+        my_first = first;
+      }
+      csync();
+      if (my_first) {
+        int ue = 0, len = 0;
+        for (int j = 0; j < N; ++j) {
+          const int e2 = F.topk_id[j / TOPK][j % TOPK];
+          ue += F.efirst[j] && e2 < my_e;
+          len += e2 == my_e;
+        }
+        F.ue_expert[ue] = (int16_t)my_e;
+        F.ue_start[ue] = (int16_t)my_pos;
+        F.ue_len[ue] = (int16_t)len;
+        atomicMax(&F.n_ue, ue + 1);
       }
       csync();
       if (tid == 0) {
@@ -814,9 +881,9 @@ struct Model {
     {
       const void* nw = Lw.ffn_norm;
       const float* hp = a.sc.h;
-      stage_block<WDT, H>(
+      stage_block<WDT, H, true>(
           c.act, n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(hp + r * H) + f4); },
-          true, a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, F.rnorm);
+          a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, F.rnorm);
     }
     csync();
     MK_STAMP(c, l, 3, 0);
@@ -871,7 +938,7 @@ struct Model {
           a->sc.act[(b * TOPK + j) * FE + f] = silu(v0) * v1;
         }
       } task{&a, &F, u0, lane};
-      run_gemv<H, 2, T_GU, false>(u1 - u0, c.act, task);
+      run_gemv<H, 2, T_GU, false, false>(u1 - u0, c.act, task);
     } else {
       int f0, f1;
       gu_range(c, FD, f0, f1);
@@ -882,7 +949,7 @@ struct Model {
           if (lane == 0) a->sc.dact[b * FD + f0 + t] = silu(v0) * v1;
         }
       } task{&a, f0, lane};
-      run_gemv<H, 2, T_GU, false>(f1 - f0, c.act, task);
+      run_gemv<H, 2, T_GU, false, false>(f1 - f0, c.act, task);
     }
   }
 
@@ -910,14 +977,14 @@ struct Model {
         {
           const float* act = a.sc.act;
           const Fixed* Fp = &F;
-          stage_block<WDT, FE>(
+          stage_block<WDT, FE, false>(
               c.act, ecnt,
               [&](int r, int f4) -> float4 {
                 const int en = e0 + r;
                 const float* src = act + (Fp->ent_b[en] * TOPK + Fp->ent_j[en]) * FE;
                 return __ldcg(reinterpret_cast<const float4*>(src) + f4);
               },
-              false, 0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
+              0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
         }
         csync();
         MK_STAMP(c, l, 4, 0);
@@ -931,7 +998,7 @@ struct Model {
             if (lane == 0) F->dots[e0 + ai][t % nr] = v0;
           }
         } task{&F, ua, nr, e0, lane};
-        run_gemv<FE, 1, T_DN, false>((ub - ua) * nr, c.act, task);
+        run_gemv<FE, 1, T_DN, GE::ACT_REGS, true>((ub - ua) * nr, c.act, task);
         ua = ub;
       }
     } else {
@@ -941,10 +1008,10 @@ struct Model {
         const int cnt = min(cap, n - ba);
         {
           const float* dact = a.sc.dact;
-          stage_block<WDT, FD>(
+          stage_block<WDT, FD, false>(
               c.act, cnt,
               [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(dact + (ba + r) * FD) + f4); },
-              false, 0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
+              0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
         }
         csync();
         MK_STAMP(c, l, 4, 0);
@@ -955,7 +1022,7 @@ struct Model {
             if (lane == 0) F->dots[ba + ai][t] = v0;
           }
         } task{&F, ba, cnt, lane};
-        run_gemv<FD, 1, T_DD, false>(nr, c.act, task);
+        run_gemv<FD, 1, T_DD, false, false>(nr, c.act, task);
       }
     }
     for (int idx = tid; idx < n * nr; idx += kThreads) {
@@ -984,10 +1051,10 @@ struct Model {
     {
       const void* nw = a.final_norm;
       const float* x = a.sc.x + a.out_first * H;
-      stage_block<WDT, H>(
+      stage_block<WDT, H, true>(
           c.act + a.out_first * GH::ACT_BYTES, n - a.out_first,
           [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4); },
-          true, a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
+          a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
     }
     for (int i = tid; i < kWarps * kMaxBatch; i += kThreads) {
       F.best_v[i / kMaxBatch][i % kMaxBatch] = -INFINITY;
@@ -1007,7 +1074,7 @@ struct Model {
         if (tr) tr[(size_t)b * a->vocab + tok] = v0;
       }
     } task{&a, &F, c.tr_fin, v0, lane, wid};
-    run_gemv<H, 1, T_LM, GH::ACT_REGS>(v1 - v0, c.act, task);
+    run_gemv<H, 1, T_LM, GH::ACT_REGS, false>(v1 - v0, c.act, task);
     if (tid < n) {
       float bv = -INFINITY;
       int bi = INT_MAX;
@@ -1092,7 +1159,12 @@ struct Model {
   // compute warps consume them (lane 0 of the streaming warp).  Runs of rows
   // contiguous in memory are known from the layouts: a QKV run ends at a head
   // boundary, an expert run at an expert boundary.
-  __device__ static __noinline__ void produce(Producer& p) {
+  __device__ static __noinline__ void produce() {
+    Producer p;  // registers of the streaming lane; the item count goes to F.prod_k
+    run_schedule(p);
+    fixed().prod_k = p.k;
+  }
+  __device__ static __forceinline__ void run_schedule(Producer& p) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
@@ -1306,6 +1378,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     }
     F.unit_start[n] = acc;
     F.kc = 0;
+    F.prod_k = 0;
     F.route_gen = 0;
     F.abort = 0;
     for (int s = 0; s < c.ns; ++s) {
@@ -1326,13 +1399,12 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
   }
   __syncthreads();
   const Ctx& c = F.ctx;
-  Producer prod;
 
   if (tid >= kThreads) {
     // streaming warp
     if (c.ns >= 2) {
       M::load_unit_pages();
-      if (tid == kThreads) M::produce(prod);
+      if (tid == kThreads) M::produce();
     }
     __syncwarp();
   } else {
@@ -1382,7 +1454,11 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
   __syncthreads();
   // every copy the streaming warp issued has landed before the block ends
   if (tid >= kThreads) {
-    if (tid == kThreads) prod.drain();
+    if (tid == kThreads) {
+      Producer prod;
+      prod.k = F.prod_k;
+      prod.drain();
+    }
     __syncwarp();
   }
   if (tid == 0) {

@@ -120,7 +120,7 @@ extern "C" MK_API int mk_decode_step_static(
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return host_fail(MK_ERR_CUDA, cudaGetErrorString(e));
   if (dev >= kMaxDevices) return host_fail(MK_ERR_UNSUPPORTED, "device ordinal >= 64");
-  if ((d->hidden + sms - 1) / sms > kMaxRowsPerBlock)
+  if ((d->hidden / 4 + sms - 1) / sms * 4 > kMaxRowsPerBlock)
     return host_fail(MK_ERR_UNSUPPORTED, "too few SMs for the compiled per-block row budget");
 
   // layout of the static array: RoPE table | layer table | kernel scratch
