@@ -435,6 +435,34 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(v, 5), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_profile_case(args):
+    """A short run for an ncu capture of the decode launch at the bench's
+    full size: prefill of the workload's prompt (ceil(prompt / 16) launches),
+    then --steps decode launches; nothing else (no CPU baseline, no e2e)."""
+    import torch
+    import synth
+    from synth import prompts as SP
+    from synth import weights as SW
+    from moe_decode_megakernel_persistent_gb300 import _build
+    from moe_decode_megakernel_persistent_gb300.engine import Engine
+
+    _build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = synth.CONFIGS[args.config]
+    m = w.model
+    weights = SW.model_torch(m, dev)
+    prompt_len = w.prompt_len
+    max_ctx = prompt_len + args.steps + 16
+    eng = Engine(m, weights, n_pages=(max_ctx + 127) // 128 + 2, max_ctx=max_ctx, max_seqs=2)
+    prompt = torch.from_numpy(SP.prompt_tokens(m.seed, m.vocab, prompt_len)).to(dev)
+    tok = eng.prefill(0, prompt)
+    for i in range(args.steps):
+        eng.decode_step([0], tok, [prompt_len + i], tok)
+    eng.sync()
+    print(json.dumps({"profile_case": w.name, "prefill_launches": (prompt_len + 15) // 16,
+                      "decode_launches": args.steps}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -444,7 +472,14 @@ def main():
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="prefill + --steps decode launches only (for an ncu capture)")
     args = ap.parse_args()
+    if args.profile_case:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        run_profile_case(args)
+        return
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
