@@ -234,8 +234,10 @@ def run_ours(args, rank, world):
     gen_s = time.time() - t0
     prompt_len = w.prompt_len
     max_ctx = prompt_len + K + 2 * args.e2e_steps + W + 64
-    pages = 3 * ((max_ctx + 127) // 128) + 8
-    eng = Engine(m, weights, n_pages=pages, max_ctx=max_ctx, max_seqs=4)
+    B16, P16 = 16, 256
+    ctx16 = P16 + W + 1 + args.batch16_steps + 16
+    pages = 3 * ((max_ctx + 127) // 128) + 8 + B16 * ((ctx16 + 127) // 128)
+    eng = Engine(m, weights, n_pages=pages, max_ctx=max_ctx, max_seqs=4 + B16)
     stream = torch.cuda.current_stream()
 
     # warm-up sequence: a short prompt and W decode steps
@@ -293,6 +295,55 @@ def run_ours(args, rank, world):
     e2e_s = time.perf_counter() - t0
     eng.sync()
 
+    # batch 16: sixteen sequences with 256-token prompts decoded together, one
+    # launch per step for all of them
+    b16 = None
+    if args.batch16_steps > 0:
+        K16 = args.batch16_steps
+        ids = list(range(4, 4 + B16))
+        toks16 = torch.empty(B16, dtype=torch.int32, device=dev)
+        for j, sid in enumerate(ids):
+            p16 = torch.from_numpy(SP.prompt_tokens(m.seed, m.vocab, P16, seq=100 + j)).to(dev)
+            eng.prefill(sid, p16, out=toks16[j:j + 1])
+        pos = P16
+        for i in range(W):
+            eng.decode_step(ids, toks16, [pos] * B16, toks16)
+            pos += 1
+        # distinct experts per MoE layer, counted on one traced step
+        eng.enable_trace(B16)
+        eng.decode_step(ids, toks16, [pos] * B16, toks16)
+        eng.sync()
+        pos += 1
+        tk = eng.split_trace(B16)["topk"][m.n_dense:, :, :m.top_k].cpu().numpy().astype(int)
+        distinct = float(np.mean([len(np.unique(tk[l])) for l in range(tk.shape[0])]))
+        eng.disable_trace()
+        clocks16 = ClockSampler(torch.cuda.current_device())
+        clocks16.start()
+        time.sleep(0.3)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(K16):
+            eng.decode_step(ids, toks16, [pos + i] * B16, toks16)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        clk16 = clocks16.stop()
+        eng.sync()
+        ms16, _ = aggregate_over_ranks(e0.elapsed_time(e1), K16, dev)
+        bytes16 = sum(step_bytes(m, [pos + i + 1] * B16, distinct) for i in range(K16)) / K16
+        ach16 = bytes16 / (ms16 / K16 * 1e-3) / 1e9
+        b16 = {"value": round(world * B16 * K16 / (ms16 / 1e3), 2), "unit": "tok/s",
+               "ms_per_step": round(ms16 / K16, 4), "steps": K16, "sequences": B16,
+               "prompt": P16, "context": [pos + 1, pos + K16],
+               "distinct_experts_per_layer": round(distinct, 2),
+               "roofline": {"bound": "hbm", "achieved": round(ach16, 1),
+                            "frac": round(ach16 / load_peaks()[0]["hbm_gbs"], 4),
+                            "bytes_per_step": int(bytes16)},
+               "clocks": clk16}
+
     ctxs = [prompt_len + i + 1 for i in range(K)]
     bytes_avg = sum(step_bytes(m, [c], m.top_k) for c in ctxs) / K
     peaks, peak_kind = load_peaks()
@@ -328,6 +379,8 @@ def run_ours(args, rank, world):
         "clocks": clk,
         "setup_s": {"weights": round(gen_s, 1), "prefill": round(prefill_s, 3)},
     }
+    if b16 is not None:
+        out["batch16"] = b16
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(m, weights)
     eng.close()
@@ -472,6 +525,8 @@ def main():
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch16-steps", type=int, default=32,
+                    help="timed decode steps of the 16-sequence batch (0 = skip)")
     ap.add_argument("--profile-case", action="store_true",
                     help="prefill + --steps decode launches only (for an ncu capture)")
     args = ap.parse_args()

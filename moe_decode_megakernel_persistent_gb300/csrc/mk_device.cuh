@@ -396,7 +396,11 @@ struct Gemv {
 //   WT(f4)      -> float4 weights (only with norm)
 //   red         -> shared scratch of kWarps * 4 floats
 //   rscale      -> if non-null, receives each row's RMS scale (shared memory)
-template <int WDT, int K, bool NORM, int RG, class LD, class WT>
+// Row stride of the plain fp32 staging used by the tensor-core path (16
+// bytes of padding keep the rows of 8 columns on distinct banks).
+__host__ __device__ constexpr int plain_stride(int K) { return K * 4 + 16; }
+
+template <int WDT, int K, bool NORM, int RG, bool PLAIN, class LD, class WT>
 __device__ __noinline__ void stage_rows(uint8_t* dst, int rows, LD ld, float eps, WT wt, float* red,
                                            float* rscale) {
   using Gv = Gemv<WDT, K>;
@@ -460,7 +464,7 @@ __device__ __noinline__ void stage_rows(uint8_t* dst, int rows, LD ld, float eps
       // in the shuffles; threads past the end are predicated off (no
       // continue: the loop stays unrolled and the arrays stay in registers)
       const bool live = it < nrg * NW;
-      const bool warp_live = WDT == WINT4 ? __any_sync(0xffffffffu, live) : live;
+      const bool warp_live = (WDT == WINT4 && !PLAIN) ? __any_sync(0xffffffffu, live) : live;
       if (warp_live) {
         const int row = live ? it / NW : 0, w = live ? it % NW : 0;
         float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -476,8 +480,13 @@ __device__ __noinline__ void stage_rows(uint8_t* dst, int rows, LD ld, float eps
           y[0] = va[i].x * ma.x; y[1] = va[i].y * ma.y; y[2] = va[i].z * ma.z; y[3] = va[i].w * ma.w;
           y[4] = vb[i].x * mb.x; y[5] = vb[i].y * mb.y; y[6] = vb[i].z * mb.z; y[7] = vb[i].w * mb.w;
         }
-        uint8_t* base = dst + (r0 + row) * Gv::ACT_BYTES;
-        if constexpr (WDT == WINT4) {
+        uint8_t* base = dst + (r0 + row) * (PLAIN ? plain_stride(K) : Gv::ACT_BYTES);
+        if constexpr (PLAIN) {
+          if (live) {
+            *reinterpret_cast<float4*>(base + 32 * w) = make_float4(y[0], y[1], y[2], y[3]);
+            *reinterpret_cast<float4*>(base + 32 * w + 16) = make_float4(y[4], y[5], y[6], y[7]);
+          }
+        } else if constexpr (WDT == WINT4) {
           // chunk c = w / 4 (32 values) lives in threads 4j .. 4j+3; word t of
           // the chunk holds values 8t .. 8t+7
           float amax = 0.f;
@@ -531,17 +540,19 @@ __device__ __noinline__ void stage_rows(uint8_t* dst, int rows, LD ld, float eps
   }
 }
 
-// Staging entry: one row per pass for a single row (fewest registers);
-// otherwise four rows per pass with a norm (one load round trip and one norm
-// reduction for four rows) and, without one, as many rows as fit two words
-// per thread.
+// Staging entry: the plain fp32 rows of the tensor-core path (plain), or
+// the GEMV engine's staged form: one row per pass for a single row (fewest
+// registers); otherwise four rows per pass with a norm (one load round trip
+// and one norm reduction for four rows) and, without one, as many rows as fit
+// two words per thread.
 template <int WDT, int K, bool NORM, class LD, class WT>
-__device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, float eps, WT wt, float* red,
-                                            float* rscale) {
+__device__ __forceinline__ void stage_block(uint8_t* dst, int rows, bool plain, LD ld, float eps, WT wt,
+                                            float* red, float* rscale) {
   // without a norm, as many rows per pass as two words per thread cover
   constexpr int RGM = NORM ? 4 : ((2 * kThreads) / (K / 8) > 1 ? (2 * kThreads) / (K / 8) : 1);
-  if (rows == 1) stage_rows<WDT, K, NORM, 1>(dst, rows, ld, eps, wt, red, rscale);
-  else stage_rows<WDT, K, NORM, RGM>(dst, rows, ld, eps, wt, red, rscale);
+  if (plain) stage_rows<WDT, K, NORM, RGM, true>(dst, rows, ld, eps, wt, red, rscale);
+  else if (rows == 1) stage_rows<WDT, K, NORM, 1, false>(dst, rows, ld, eps, wt, red, rscale);
+  else stage_rows<WDT, K, NORM, RGM, false>(dst, rows, ld, eps, wt, red, rscale);
 }
 
 __device__ __forceinline__ void split_range(int n, int parts, int idx, int& lo, int& hi) {

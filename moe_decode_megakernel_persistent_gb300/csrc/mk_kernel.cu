@@ -34,6 +34,7 @@
 namespace mk {
 
 constexpr int kMaxEnt = kMaxBatch * 8;  // (row, expert slot) entries
+constexpr int kMmaUnits = 8;            // tensor-core units per pass (shared accumulators)
 
 // Per-launch, per-block context shared by the phases (in shared memory).
 struct Ctx {
@@ -43,6 +44,7 @@ struct Ctx {
   int act_bytes;   // size of the staging area
   int G, bid, n;
   int r0, nr;      // hidden rows owned by this block
+  bool tc;         // tensor-core GEMV (plain fp32 staging) for this launch
   float *tr_x, *tr_attn, *tr_rl, *tr_tk, *tr_fin;
   uint64_t* tm;    // timing stamps (block 0, thread 0 only) or null
 };
@@ -65,8 +67,9 @@ struct Fixed {
   float hs[kMaxBatch][kMaxRowsPerBlock];
   uint32_t nslw[kMaxRowsPerBlock];  // raw slice of the post-attention norm weights
   float red[kThreads];
-  float best_v[kWarps][kMaxBatch];
-  int best_i[kWarps][kMaxBatch];
+  unsigned long long best_key[kMaxBatch];  // lm_head argmax per row (argmax_key)
+  float mma_acc[2 * kMmaUnits * 128];      // tensor-core path: per-unit partial sums (two sets)
+  uint32_t mma_flip;                       // which set the next pass uses
   int unit_start[kMaxBatch + 1];
   int upages[2][64];      // pool pages of this block's attention units (streaming warp)
   float rnorm[kMaxBatch];
@@ -84,6 +87,20 @@ __device__ __forceinline__ Fixed& fixed() {
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.f + expf(-x)); }
+
+// Argmax as one 64-bit maximum: the logit's bits mapped to an unsigned order
+// (negative values flipped) above the complemented token id, so the larger
+// logit wins and, on equal logits, the lower token id.  Key 0 = no candidate.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int tok) {
+  const uint32_t b = __float_as_uint(v);
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)tok);
+}
+__device__ __forceinline__ float key_value(unsigned long long k) {
+  const uint32_t ord = (uint32_t)(k >> 32);
+  return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+}
+__device__ __forceinline__ int key_token(unsigned long long k) { return (int)(0xFFFFFFFFu - (uint32_t)k); }
 
 template <class S>
 struct Kv {
@@ -228,11 +245,15 @@ struct Model {
 
   // Staging area for n rows: every phase's activations fit; the MoE down
   // entries take what is left above 3 ring stages (rounds if they do not fit).
-  __host__ __device__ static constexpr int act_base_bytes(int n) {
-    return cmax(cmax(n * GH::ACT_BYTES, n * GQ::ACT_BYTES),
-                cmax(cmax(ATT_BYTES, GD::ACT_BYTES), n * GE::ACT_BYTES));
+  static constexpr bool TC = WDT != WF32;  // the tensor-core path serves launches of 2+ rows
+  // (the tensor-core path stages plain fp32 rows for the dense projections;
+  // the expert phases keep the GEMV engine's staged form)
+  __host__ __device__ static constexpr int act_base_bytes(int n, bool tc) {
+    return cmax(tc ? cmax(cmax(n * plain_stride(H), n * plain_stride(QD)), plain_stride(FD)) : 0,
+                cmax(cmax(n * GH::ACT_BYTES, n * GQ::ACT_BYTES),
+                     cmax(cmax(ATT_BYTES, GD::ACT_BYTES), n * GE::ACT_BYTES)));
   }
-  static_assert(kActOffset + act_base_bytes(kMaxBatch) + 2 * STAGE <= kSmemBytes,
+  static_assert(kActOffset + act_base_bytes(kMaxBatch, TC) + 2 * STAGE <= kSmemBytes,
                 "a full batch leaves at least two ring stages");
 
   __device__ static __forceinline__ void unit_of(const StepArgs& a, const int* unit_start, int u, int n,
@@ -259,6 +280,11 @@ struct Model {
   }
   // rounds of the MoE down projection: distinct experts [ua, ub) whose
   // entries fit the staging area together
+  // staged bytes per MoE down entry / per dense down row in this launch
+  __device__ static __forceinline__ int moe_entry_bytes(const Ctx&) { return GE::ACT_BYTES; }
+  __device__ static __forceinline__ int dense_entry_bytes(const Ctx& c) {
+    return c.tc ? plain_stride(FD) : GD::ACT_BYTES;
+  }
   __device__ static __forceinline__ int moe_round_end(const Fixed& F, int ua, int cap) {
     int ub = ua, cnt = 0;
     while (ub < F.n_ue && cnt + F.ue_len[ub] <= cap) cnt += F.ue_len[ub++];
@@ -277,9 +303,16 @@ struct Model {
   // ring item; task t runs on warp t % kWarps, or (CONTIG) each warp takes a
   // contiguous block of a tile's tasks (tasks sharing an activation stay on
   // one warp, whose activation registers then reload rarely).  TK provides
-  //   ActRange acts(t) and void out(t, ai, i, v0, v1) (all lanes).
-  template <int K, int RP, int T, bool REGS, bool CONTIG, class TK>
+  //   ActRange acts(t) and void put(t, ai, i, v0, v1) (one lane writes the
+  //   results of task t for activation ai, the i-th of the task's list).
+  template <int K, int RP, int T, bool REGS, bool CONTIG, bool MMA, class TK>
   __device__ static __forceinline__ void run_gemv(int ntask, const uint8_t* act_base, const TK& task) {
+    if constexpr (TC && MMA) {
+      if (fixed().ctx.tc) {
+        run_mma<K, RP, T>(ntask, act_base, task);
+        return;
+      }
+    }
     using Gv = Gemv<WDT, K>;
     Fixed& F = fixed();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -314,7 +347,7 @@ struct Model {
           }
           float v0, v1;
           Gv::template dots<RP, REGS>(wr, sr, a, ab, lane, v0, v1);
-          task.out(t, ai, i, v0, v1);
+          if (lane == 0) task.put(t, ai, i, v0, v1);
         }
       }
       ring_release(k);
@@ -352,6 +385,206 @@ struct Model {
     else return bf16_to_f((row[t >> 1] >> (16 * (t & 1))) & 0xFFFFu);
   }
 
+  // ---- tensor-core GEMV (launches of 2+ rows).  A ring tile is cut into
+  // m-tiles of 16 weight rows (RP == 2: 8 tasks, rows g and g + 8 are the two
+  // rows of task g; RP == 1: 16 tasks) and, per run of tasks sharing one
+  // activation list, n-tiles of 8 activations.  mma.sync m16n8k16, bf16 in,
+  // fp32 accumulate: int4 codes are widened to bf16 exactly in registers; each
+  // activation (plain fp32 staging) is split into three bf16 parts
+  // hi + mid + lo (24 significant bits), all multiplied into one accumulator.
+  // K is split over the warps in 64-value groups (the int4 scale group: a
+  // group's sum is scaled before it is added); the warps' partials meet in
+  // shared memory.  Within a group, thread q of a quad takes the values
+  // 16q .. 16q+15 of weights and activations alike (the order of k inside an
+  // mma is free as long as A and B agree on it).
+  __device__ static __forceinline__ uint32_t nib_pair_bf16(uint32_t E, uint32_t O, int i) {
+    // byte i of E / O (codes q + 8) -> bf16x2 {q_lo, q_hi}: (128 + c) - 136
+    uint32_t r;
+    const uint32_t sel = (uint32_t)i | ((uint32_t)i << 4) | ((uint32_t)(4 + i) << 8) | ((uint32_t)(4 + i) << 12);
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(E), "r"(O), "r"(sel));
+    r = (r & 0x00FF00FFu) | 0x43004300u;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(r), "r"(0x3F803F80u), "r"(0xC308C308u));
+    return r;
+  }
+  __device__ static __forceinline__ void split3(float x0, float x1, uint32_t& h, uint32_t& m, uint32_t& l) {
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(x1), "f"(x0));
+    const float r0 = x0 - __uint_as_float(h << 16), r1 = x1 - __uint_as_float(h & 0xFFFF0000u);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(m) : "f"(r1), "f"(r0));
+    const float s0 = r0 - __uint_as_float(m << 16), s1 = r1 - __uint_as_float(m & 0xFFFF0000u);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(l) : "f"(s1), "f"(s0));
+  }
+  __device__ static __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                  uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+  static __device__ __forceinline__ bool same_acts(const ActRange& x, const ActRange& y) {
+    return x.list == y.list && x.start == y.start && x.count == y.count;
+  }
+
+  template <int K, int RP, int T, class TK>
+  __device__ static __forceinline__ void run_mma(int ntask, const uint8_t* act_base, const TK& task) {
+    using Gv = Gemv<WDT, K>;
+    constexpr int NGR = K / 64;
+    constexpr int MT = RP == 2 ? 8 : 16;
+    constexpr int RB = Gv::ROW_BYTES, SB = Gv::SCALE_BYTES, AS = plain_stride(K);
+    static_assert(K % 64 == 0, "whole 64-value groups");
+    Fixed& F = fixed();
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, q = lane & 3;
+    uint32_t k = F.kc;
+    uint32_t flip = F.mma_flip;  // every thread advances its own copy identically
+#pragma unroll 1
+    for (int t0 = 0; t0 < ntask; t0 += T, ++k) {
+      const uint8_t* st = ring_acquire<STAGE>(k);
+      const int tn = min(T, ntask - t0);
+#pragma unroll 1
+      for (int base = 0;; base += kMmaUnits) {
+        // accumulators of this pass (two sets used alternately; the output
+        // step zeroes what it reads, so no separate clearing pass)
+        float* accs = F.mma_acc + (flip & 1) * (kMmaUnits * 128);
+        // walk the tile's units (m-tile, run of tasks, n-tile); units
+        // [base, base + kMmaUnits) are computed in this pass
+        int u = 0;
+#pragma unroll 1
+        for (int ta = 0; ta < tn; ta += MT) {
+          const int tb = min(tn, ta + MT);
+#pragma unroll 1
+          for (int sa = ta; sa < tb;) {
+            const ActRange ar = task.acts(t0 + sa);
+            int sb = sa + 1;
+            while (sb < tb && same_acts(task.acts(t0 + sb), ar)) ++sb;
+#pragma unroll 1
+            for (int c0 = 0; c0 < ar.count; c0 += 8, ++u) {
+              if (u < base || u >= base + kMmaUnits) continue;
+              // rows of this lane: task rows rho0 = g, rho1 = g + 8 of the m-tile
+              int j0, j1, seg1;
+              if (RP == 2) { j0 = ta + g; j1 = j0; seg1 = 1; }
+              else { j0 = ta + g; j1 = ta + 8 + g; seg1 = 0; }
+              j0 = j0 < tb ? j0 : ta;
+              j1 = j1 < tb ? j1 : ta;
+              const uint8_t* w0 = st + (size_t)j0 * RB;
+              const uint8_t* w1 = st + (size_t)(seg1 * T + j1) * RB;
+              const uint8_t* s0p = st + STD + (size_t)j0 * SB;
+              const uint8_t* s1p = st + STD + (size_t)(seg1 * T + j1) * SB;
+              // this lane's activation column
+              const int col = c0 + g;
+              const bool cv = col < ar.count;
+              const int ai = cv ? (ar.list ? ar.list[ar.start + col] : ar.start + col) : 0;
+              const uint8_t* xa = act_base + (size_t)ai * AS;
+              float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+              for (int G = wid; G < NGR; G += kWarps) {
+                float xv[16];
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4) {
+                  const uint4 r = cv ? lds128(xa + (64 * G + 16 * q + 4 * v4) * 4) : make_uint4(0u, 0u, 0u, 0u);
+                  xv[4 * v4] = __uint_as_float(r.x); xv[4 * v4 + 1] = __uint_as_float(r.y);
+                  xv[4 * v4 + 2] = __uint_as_float(r.z); xv[4 * v4 + 3] = __uint_as_float(r.w);
+                }
+                uint32_t aw[2][8];  // per row: bf16x2 words for steps 0..3 (2 per step)
+                if constexpr (WDT == WINT4) {
+#pragma unroll
+                  for (int r = 0; r < 2; ++r) {
+                    const uint2 wv = lds64((r ? w1 : w0) + 32 * G + 8 * q);
+                    const uint32_t x2[2] = {wv.x, wv.y};
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                      const uint32_t y = x2[h] ^ 0x88888888u;
+                      const uint32_t E = y & 0x0F0F0F0Fu, O = (y >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+                      for (int bi = 0; bi < 4; ++bi) aw[r][4 * h + bi] = nib_pair_bf16(E, O, bi);
+                    }
+                  }
+                } else {
+#pragma unroll
+                  for (int r = 0; r < 2; ++r) {
+                    const uint4 lo = lds128((r ? w1 : w0) + 128 * G + 32 * q);
+                    const uint4 hi = lds128((r ? w1 : w0) + 128 * G + 32 * q + 16);
+                    aw[r][0] = lo.x; aw[r][1] = lo.y; aw[r][2] = lo.z; aw[r][3] = lo.w;
+                    aw[r][4] = hi.x; aw[r][5] = hi.y; aw[r][6] = hi.z; aw[r][7] = hi.w;
+                  }
+                }
+                float cg[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int sstep = 0; sstep < 4; ++sstep) {
+                  uint32_t bh0, bm0, bl0, bh1, bm1, bl1;
+                  split3(xv[4 * sstep], xv[4 * sstep + 1], bh0, bm0, bl0);
+                  split3(xv[4 * sstep + 2], xv[4 * sstep + 3], bh1, bm1, bl1);
+                  const uint32_t a0 = aw[0][2 * sstep], a2 = aw[0][2 * sstep + 1];
+                  const uint32_t a1 = aw[1][2 * sstep], a3 = aw[1][2 * sstep + 1];
+                  mma16816(cg, a0, a1, a2, a3, bh0, bh1);
+                  mma16816(cg, a0, a1, a2, a3, bm0, bm1);
+                  mma16816(cg, a0, a1, a2, a3, bl0, bl1);
+                }
+                if constexpr (WDT == WINT4) {
+                  const float sc0 = bf16_to_f(lds16(s0p + 2 * G)), sc1 = bf16_to_f(lds16(s1p + 2 * G));
+                  acc[0] = fmaf(cg[0], sc0, acc[0]);
+                  acc[1] = fmaf(cg[1], sc0, acc[1]);
+                  acc[2] = fmaf(cg[2], sc1, acc[2]);
+                  acc[3] = fmaf(cg[3], sc1, acc[3]);
+                } else {
+#pragma unroll
+                  for (int r = 0; r < 4; ++r) acc[r] += cg[r];
+                }
+              }
+#pragma unroll
+              for (int r = 0; r < 4; ++r) atomicAdd(&accs[((u - base) * 32 + lane) * 4 + r], acc[r]);
+            }
+            sa = sb;
+          }
+        }
+        const int n_units = u;
+        csync();
+        // results: warp w writes unit base + w (lane: rows g / g + 8, columns 2q, 2q + 1)
+        u = 0;
+#pragma unroll 1
+        for (int ta = 0; ta < tn; ta += MT) {
+          const int tb = min(tn, ta + MT);
+#pragma unroll 1
+          for (int sa = ta; sa < tb;) {
+            const ActRange ar = task.acts(t0 + sa);
+            int sb = sa + 1;
+            while (sb < tb && same_acts(task.acts(t0 + sb), ar)) ++sb;
+#pragma unroll 1
+            for (int c0 = 0; c0 < ar.count; c0 += 8, ++u) {
+              if (u - base != wid) continue;
+              float* r4 = &accs[((u - base) * 32 + lane) * 4];
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                const int col = c0 + 2 * q + cc;
+                if (col >= ar.count) continue;
+                const int ai = ar.list ? ar.list[ar.start + col] : ar.start + col;
+                if (RP == 2) {
+                  const int j = ta + g;
+                  if (j >= sa && j < sb) task.put(t0 + j, ai, col, r4[cc], r4[2 + cc]);
+                } else {
+                  const int ja = ta + g, jb = ta + 8 + g;
+                  if (ja >= sa && ja < sb) task.put(t0 + ja, ai, col, r4[cc], 0.f);
+                  if (jb >= sa && jb < sb) task.put(t0 + jb, ai, col, r4[2 + cc], 0.f);
+                }
+              }
+              r4[0] = 0.f; r4[1] = 0.f; r4[2] = 0.f; r4[3] = 0.f;
+            }
+            sa = sb;
+          }
+        }
+        ++flip;
+        if (base + kMmaUnits >= n_units) break;
+        csync();
+      }
+      ring_release(k);
+    }
+    csync();
+    if (threadIdx.x == 0) {
+      F.kc = k;
+      F.mma_flip = flip;
+    }
+    csync();
+  }
+
   // ---------------------------------------------------------------- P1
   // RMSNorm of the residual (every block, redundantly) -> this block's QKV
   // tasks.  A task is a RoPE pair of rows (i, i + HD/2) of one q, k or v head,
@@ -377,7 +610,7 @@ struct Model {
       const int* tok = F.tok;
       const bool first = l == 0;
       stage_block<WDT, H, true>(
-          c.act, n,
+          c.act, n, c.tc,
           [&](int r, int f4) -> float4 {
             return first ? ld_aux4<AUX>(embed, (size_t)tok[r] * (H / 4) + f4)
                          : __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4);
@@ -397,8 +630,7 @@ struct Model {
     struct {
       const StepArgs* a; int p0, l, lane;
       __device__ __forceinline__ ActRange acts(int) const { return {nullptr, 0, a->n}; }
-      __device__ __forceinline__ void out(int t, int b, int, float v0, float v1) const {
-        if (lane != 0) return;
+      __device__ __forceinline__ void put(int t, int b, int, float v0, float v1) const {
         const int p = p0 + t;
         const int pos = a->pos[b];
         if (p < NQP + NKP) {
@@ -424,7 +656,7 @@ struct Model {
         }
       }
     } task{&a, p0, l, lane};
-    run_gemv<H, 2, T_QKV, false, false>(p1 - p0, c.act, task);
+    run_gemv<H, 2, T_QKV, false, false, true>(p1 - p0, c.act, task);
   }
 
   // K/V rows of TU positions into registers (bf16 -> float), from shared
@@ -764,7 +996,7 @@ struct Model {
     {
       const float* at = a.sc.attn;
       stage_block<WDT, QD, false>(
-          c.act, n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(at + r * QD) + f4); },
+          c.act, n, c.tc, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(at + r * QD) + f4); },
           0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
     }
     csync();
@@ -772,14 +1004,13 @@ struct Model {
     struct {
       const StepArgs* a; Fixed* F; int r0, lane;
       __device__ __forceinline__ ActRange acts(int) const { return {nullptr, 0, a->n}; }
-      __device__ __forceinline__ void out(int t, int b, int, float v0, float) const {
-        if (lane != 0) return;
+      __device__ __forceinline__ void put(int t, int b, int, float v0, float) const {
         const float hv = __ldcg(a->sc.x + b * H + r0 + t) + v0;
         a->sc.h[b * H + r0 + t] = hv;
         F->hs[b][t] = hv;
       }
     } task{&a, &F, c.r0, lane};
-    run_gemv<QD, 1, T_O, false, false>(c.nr, c.act, task);
+    run_gemv<QD, 1, T_O, false, false, true>(c.nr, c.act, task);
     if (l < a.n_dense) return;
     // the router / norm slices requested in P1 have landed
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -882,7 +1113,7 @@ struct Model {
       const void* nw = Lw.ffn_norm;
       const float* hp = a.sc.h;
       stage_block<WDT, H, true>(
-          c.act, n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(hp + r * H) + f4); },
+          c.act, n, c.tc && !moe, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(hp + r * H) + f4); },
           a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, F.rnorm);
     }
     csync();
@@ -931,25 +1162,24 @@ struct Model {
           const int ue = (u0 + t) / FE;
           return {F->ent_b, F->ue_start[ue], F->ue_len[ue]};
         }
-        __device__ __forceinline__ void out(int t, int b, int i, float v0, float v1) const {
-          if (lane != 0) return;
+        __device__ __forceinline__ void put(int t, int b, int i, float v0, float v1) const {
           const int u = u0 + t, f = u % FE;
           const int j = F->ent_j[F->ue_start[u / FE] + i];
           a->sc.act[(b * TOPK + j) * FE + f] = silu(v0) * v1;
         }
       } task{&a, &F, u0, lane};
-      run_gemv<H, 2, T_GU, false, false>(u1 - u0, c.act, task);
+      run_gemv<H, 2, T_GU, false, false, false>(u1 - u0, c.act, task);
     } else {
       int f0, f1;
       gu_range(c, FD, f0, f1);
       struct {
         const StepArgs* a; int f0, lane;
         __device__ __forceinline__ ActRange acts(int) const { return {nullptr, 0, a->n}; }
-        __device__ __forceinline__ void out(int t, int b, int, float v0, float v1) const {
-          if (lane == 0) a->sc.dact[b * FD + f0 + t] = silu(v0) * v1;
+        __device__ __forceinline__ void put(int t, int b, int, float v0, float v1) const {
+          a->sc.dact[b * FD + f0 + t] = silu(v0) * v1;
         }
       } task{&a, f0, lane};
-      run_gemv<H, 2, T_GU, false, false>(f1 - f0, c.act, task);
+      run_gemv<H, 2, T_GU, false, false, true>(f1 - f0, c.act, task);
     }
   }
 
@@ -969,7 +1199,7 @@ struct Model {
     const int tid = threadIdx.x, lane = tid & 31;
     const int n = c.n, nr = c.nr;
     if constexpr (MOE) {
-      const int cap = c.act_bytes / GE::ACT_BYTES;
+      const int cap = c.act_bytes / moe_entry_bytes(c);
 #pragma unroll 1
       for (int ua = 0; ua < F.n_ue;) {
         const int ub = moe_round_end(F, ua, cap);
@@ -978,7 +1208,7 @@ struct Model {
           const float* act = a.sc.act;
           const Fixed* Fp = &F;
           stage_block<WDT, FE, false>(
-              c.act, ecnt,
+              c.act, ecnt, false,
               [&](int r, int f4) -> float4 {
                 const int en = e0 + r;
                 const float* src = act + (Fp->ent_b[en] * TOPK + Fp->ent_j[en]) * FE;
@@ -994,22 +1224,22 @@ struct Model {
             const int ue = ua + t / nr;
             return {nullptr, F->ue_start[ue] - e0, F->ue_len[ue]};
           }
-          __device__ __forceinline__ void out(int t, int ai, int, float v0, float) const {
-            if (lane == 0) F->dots[e0 + ai][t % nr] = v0;
+          __device__ __forceinline__ void put(int t, int ai, int, float v0, float) const {
+            F->dots[e0 + ai][t % nr] = v0;
           }
         } task{&F, ua, nr, e0, lane};
-        run_gemv<FE, 1, T_DN, GE::ACT_REGS, true>((ub - ua) * nr, c.act, task);
+        run_gemv<FE, 1, T_DN, GE::ACT_REGS, true, false>((ub - ua) * nr, c.act, task);
         ua = ub;
       }
     } else {
-      const int cap = c.act_bytes / GD::ACT_BYTES;
+      const int cap = c.act_bytes / dense_entry_bytes(c);
 #pragma unroll 1
       for (int ba = 0; ba < n; ba += cap) {
         const int cnt = min(cap, n - ba);
         {
           const float* dact = a.sc.dact;
           stage_block<WDT, FD, false>(
-              c.act, cnt,
+              c.act, cnt, c.tc,
               [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(dact + (ba + r) * FD) + f4); },
               0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
         }
@@ -1018,11 +1248,11 @@ struct Model {
         struct {
           Fixed* F; int ba, cnt, lane;
           __device__ __forceinline__ ActRange acts(int) const { return {nullptr, 0, cnt}; }
-          __device__ __forceinline__ void out(int t, int ai, int, float v0, float) const {
-            if (lane == 0) F->dots[ba + ai][t] = v0;
+          __device__ __forceinline__ void put(int t, int ai, int, float v0, float) const {
+            F->dots[ba + ai][t] = v0;
           }
         } task{&F, ba, cnt, lane};
-        run_gemv<FD, 1, T_DD, false, false>(nr, c.act, task);
+        run_gemv<FD, 1, T_DD, false, false, true>(nr, c.act, task);
       }
     }
     for (int idx = tid; idx < n * nr; idx += kThreads) {
@@ -1052,39 +1282,29 @@ struct Model {
       const void* nw = a.final_norm;
       const float* x = a.sc.x + a.out_first * H;
       stage_block<WDT, H, true>(
-          c.act + a.out_first * GH::ACT_BYTES, n - a.out_first,
+          c.act + a.out_first * (c.tc ? plain_stride(H) : GH::ACT_BYTES), n - a.out_first, c.tc,
           [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4); },
           a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
     }
-    for (int i = tid; i < kWarps * kMaxBatch; i += kThreads) {
-      F.best_v[i / kMaxBatch][i % kMaxBatch] = -INFINITY;
-      F.best_i[i / kMaxBatch][i % kMaxBatch] = INT_MAX;
-    }
+    if (tid < kMaxBatch) F.best_key[tid] = 0ull;
     csync();
     int v0, v1;
     gu_range(c, a.vocab, v0, v1);
     struct {
       const StepArgs* a; Fixed* F; float* tr; int vr0, lane, wid;
       __device__ __forceinline__ ActRange acts(int) const { return {nullptr, a->out_first, a->n - a->out_first}; }
-      __device__ __forceinline__ void out(int t, int b, int, float v0, float) const {
-        if (lane != 0) return;
+      __device__ __forceinline__ void put(int t, int b, int, float v0, float) const {
         const int tok = vr0 + t;
-        // a warp visits its rows in increasing order: '>' keeps the lowest id
-        if (v0 > F->best_v[wid][b]) { F->best_v[wid][b] = v0; F->best_i[wid][b] = tok; }
+        // one 64-bit key per row: larger logit first, then the lower token id
+        atomicMax(&F->best_key[b], argmax_key(v0, tok));
         if (tr) tr[(size_t)b * a->vocab + tok] = v0;
       }
     } task{&a, &F, c.tr_fin, v0, lane, wid};
-    run_gemv<H, 1, T_LM, GH::ACT_REGS, false>(v1 - v0, c.act, task);
+    run_gemv<H, 1, T_LM, GH::ACT_REGS, false, true>(v1 - v0, c.act, task);
     if (tid < n) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
-      for (int w = 0; w < kWarps; ++w) {
-        const float v = F.best_v[w][tid];
-        const int i = F.best_i[w][tid];
-        if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
-      }
-      a.sc.amax_v[c.bid * kMaxBatch + tid] = bv;
-      a.sc.amax_i[c.bid * kMaxBatch + tid] = bi;
+      const unsigned long long key = F.best_key[tid];
+      a.sc.amax_v[c.bid * kMaxBatch + tid] = key ? key_value(key) : -INFINITY;
+      a.sc.amax_i[c.bid * kMaxBatch + tid] = key ? key_token(key) : INT_MAX;
     }
     csync();
     if (tid == 0) {
@@ -1268,7 +1488,7 @@ struct Model {
           }
           p.end();
         }
-        const int cap = c.act_bytes / GE::ACT_BYTES;
+        const int cap = c.act_bytes / moe_entry_bytes(c);
         const int nr = c.nr;
 #pragma unroll 1
         for (int ua = 0; ua < F.n_ue;) {
@@ -1303,7 +1523,7 @@ struct Model {
                   (const uint8_t*)Lg.s[UP] + (size_t)t0 * SBH, RBH, SBH);
           p.end();
         }
-        const int cap = c.act_bytes / GD::ACT_BYTES;
+        const int cap = c.act_bytes / dense_entry_bytes(c);
 #pragma unroll 1
         for (int ba = 0; ba < n; ba += cap) {
 #pragma unroll 1
@@ -1344,6 +1564,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     static_assert(sizeof(StepArgs) % 4 == 0, "word copy");
     for (int i = tid; i < (int)(sizeof(StepArgs) / 4); i += kBlockThreads) dst[i] = src[i];
   }
+  for (int i = tid; i < 2 * kMmaUnits * 128; i += kBlockThreads) F.mma_acc[i] = 0.f;
   const int n = a.n;
   if (tid == 0) {
     Ctx& c = F.ctx;
@@ -1357,8 +1578,9 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     c.nr = (r1 - r0) * M::A_H;
     // staging area, then the ring in what is left
     const int avail = kSmemBytes - kActOffset;
-    int act = M::act_base_bytes(n);
-    const int want = n * S::TOPK * M::GE::ACT_BYTES;
+    c.tc = M::TC && n >= 2;
+    int act = M::act_base_bytes(n, c.tc);
+    const int want = n * S::TOPK * M::moe_entry_bytes(c);
     if (want > act) act = max(act, min(want, avail - 3 * M::STAGE));
     act = (act + 127) / 128 * 128;
     c.act_bytes = act;
@@ -1379,6 +1601,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     F.unit_start[n] = acc;
     F.kc = 0;
     F.prod_k = 0;
+    F.mma_flip = 0;
     F.route_gen = 0;
     F.abort = 0;
     for (int s = 0; s < c.ns; ++s) {

@@ -4,7 +4,8 @@ top-6, vocabulary 151936), in the launch configuration the bench times
 
 Oracle parity runs on a short prompt so that the float64 oracle finishes in
 about a minute; long contexts are covered at this size by properties that
-hold at any length (a sequence gives the same result batched or alone), and
+hold at any length (a sequence gives the same result batched or alone, within
+the parity tolerance, since batched launches take the tensor-core GEMV), and
 against the oracle on the tiny model (test_gpu_parity.py)."""
 import numpy as np
 import pytest
@@ -60,6 +61,7 @@ def test_flint_int4_long_context_batched_equals_solo(gpu_lib):
         eng.prefill(s, p, out=toks[s:s + 1])
     got = [[int(toks[s].item())] for s in range(2)]
     eng.enable_trace(2)
+    worst = 0.0
     for i in range(steps):
         eng.decode_step([0, 1], toks, [lens[0] + i, lens[1] + i], toks)
         eng.sync()
@@ -67,10 +69,14 @@ def test_flint_int4_long_context_batched_equals_solo(gpu_lib):
         for s in range(2):
             got[s].append(int(toks[s].item()))
             e = PR.rel_l2(tr["x"][:, s].double().cpu().numpy(), solo[s][1][i]).max()
-            assert e < 2e-3, (s, i, e)
+            worst = max(worst, e)
+            assert e < PR.tol_for(m), (s, i, e)
+    print(f"batched vs solo: worst per-layer residual rel L2 {worst:.2e}")
     for s in range(2):
         for k, (a, b) in enumerate(zip(got[s], solo[s][0])):
-            # a different attention split changes rounding: tokens must agree
-            # wherever the top-2 logits are not within rounding of each other
-            assert a == b or solo[s][2][k] < 1e-3, (s, k, a, b)
+            # a batched launch takes the tensor-core GEMV for the dense
+            # projections and another attention split, a solo launch the dp4a
+            # GEMV: rounding differs (and drifts through bf16 K/V rounding
+            # flips), so tokens must agree where the top-2 margin is clear
+            assert a == b or solo[s][2][k] <= PR.TOKEN_MARGIN, (s, k, a, b)
     eng.close()
