@@ -140,13 +140,31 @@ typedef struct mk_info {
 
 /* Create a context on the current CUDA device.
  * d: model description (copied).  w: weight pointers in the logical layouts
- * above; every pointer must be 16-byte aligned.  The weights are BORROWED:
- * the library reads them in place and they must stay valid and unchanged
- * until mk_destroy.  The host array w->layers is copied and may be freed
- * after the call.  Allocates library-owned scratch and the RoPE table
- * (computed on the host in double precision).  *out receives the context.
+ * above; every pointer must be 16-byte aligned.  The linear layers (wq, wk,
+ * wv, wo, gate/up/down, the experts and lm_head) are COPIED during the call
+ * into a library-owned packed buffer (the layout of mk_pack_weights); the
+ * embedding, the norms and the routers are BORROWED: the library reads them
+ * in place and they must stay valid and unchanged until mk_destroy.  The host
+ * array w->layers is copied and may be freed after the call.  Allocates the
+ * packed weights, library-owned scratch and the RoPE table (computed on the
+ * host in double precision).  *out receives the context.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 MK_API int mk_create(const mk_model_desc* d, const mk_weights* w, mk_ctx** out);
+
+/* Bytes of the packed linear weights of a model (0 if d is invalid).  The
+ * packed layout is the library's own: one 16-byte aligned record per output
+ * row (codes, then the int4 group scales), the rows a decode task reads
+ * together adjacent (the two RoPE rows of a q/k/v pair, the gate and up rows
+ * of an FFN row).  The paper has no counterpart: it exists so that the
+ * allocation-free entry point can run on weights its caller packed. */
+MK_API size_t mk_packed_bytes(const mk_model_desc* d);
+
+/* Pack the linear weights of w (logical layouts above) into dst_dev, a
+ * caller-owned device buffer of at least mk_packed_bytes(d) bytes, 256-byte
+ * aligned.  Runs kernels on `stream` and returns without waiting; w must stay
+ * valid until they finish.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+MK_API int mk_pack_weights(const mk_model_desc* d, const mk_weights* w, void* dst_dev, size_t dst_bytes,
+                           void* stream);
 
 /* Allocate the KV cache: a pool of n_pages pages of page_tokens (128)
  * positions for every layer, bf16, laid out
@@ -236,7 +254,10 @@ MK_API int mk_destroy(mk_ctx* ctx);
  * until the process exits.  Positions must be below 8192 (the size of that
  * RoPE table); a model whose scratch does not fit in the array is rejected
  * with MK_ERR_UNSUPPORTED.
- * d, w: as for mk_create (weights borrowed for the duration of the call).
+ * d, w: as for mk_create (weights borrowed for the duration of the call;
+ *   the linear layers are read from packed_dev instead).
+ * packed_dev: the caller's packed linear weights (mk_pack_weights), 256-byte
+ *   aligned.
  * kv_dev: caller-owned KV pool of n_pages pages in the layout of mk_kv_alloc.
  * block_table_dev: caller-owned int32 [max_seqs][max_pages_per_seq]; entry
  *   [slot][p / 128] must hold the page of every cached position p < position;
@@ -254,8 +275,8 @@ MK_API int mk_destroy(mk_ctx* ctx);
  * clears the counters that must start at zero): calls that overlap on the
  * GPU, on any stream, race.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
-MK_API int mk_decode_step_static(const mk_model_desc* d, const mk_weights* w, void* kv_dev,
-                                 int32_t n_pages, int32_t* block_table_dev,
+MK_API int mk_decode_step_static(const mk_model_desc* d, const mk_weights* w, const void* packed_dev,
+                                 void* kv_dev, int32_t n_pages, int32_t* block_table_dev,
                                  int32_t max_pages_per_seq, const int32_t* slots_host,
                                  const int32_t* positions_host, const int32_t* pages_host,
                                  int32_t n, const int32_t* tokens_dev, int32_t* out_tokens_dev,

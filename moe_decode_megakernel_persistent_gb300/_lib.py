@@ -83,8 +83,11 @@ SIGNATURES = {
     "mk_get_info": (C.c_int, [C.c_void_p, C.POINTER(mk_info)]),
     "mk_destroy": (C.c_int, [C.c_void_p]),
     "mk_last_error": (C.c_char_p, []),
+    "mk_packed_bytes": (C.c_size_t, [C.POINTER(mk_model_desc)]),
+    "mk_pack_weights": (C.c_int, [C.POINTER(mk_model_desc), C.POINTER(mk_weights), C.c_void_p, C.c_size_t,
+                                  C.c_void_p]),
     "mk_decode_step_static": (C.c_int, [C.POINTER(mk_model_desc), C.POINTER(mk_weights), C.c_void_p,
-                                        C.c_int32, C.c_void_p, C.c_int32, C.POINTER(C.c_int32),
+                                        C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.POINTER(C.c_int32),
                                         C.POINTER(C.c_int32), C.POINTER(C.c_int32), C.c_int32,
                                         C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
 }
@@ -175,13 +178,23 @@ def mk_destroy(ctx: int):
     _check(load().mk_destroy(ctx))
 
 
-def mk_decode_step_static(desc: mk_model_desc, weights: mk_weights, kv_dev: int, n_pages: int,
+def mk_packed_bytes(desc: mk_model_desc) -> int:
+    return int(load().mk_packed_bytes(C.byref(desc)))
+
+
+def mk_pack_weights(desc: mk_model_desc, weights: mk_weights, dst_dev: int, dst_bytes: int, stream: int = 0):
+    """Pack the linear weights into a caller-owned device buffer (for the
+    allocation-free entry point)."""
+    _check(load().mk_pack_weights(C.byref(desc), C.byref(weights), dst_dev, dst_bytes, stream))
+
+
+def mk_decode_step_static(desc: mk_model_desc, weights: mk_weights, packed_dev: int, kv_dev: int, n_pages: int,
                           block_table_dev: int, max_pages_per_seq: int, slots, positions, pages,
                           tokens_dev: int, out_tokens_dev: int, status_dev: int = 0, stream: int = 0):
     """Decode step with no device allocation (scratch in the library's static
     device array); for callers that cannot call cudaMalloc."""
     n = len(slots)
-    _check(load().mk_decode_step_static(C.byref(desc), C.byref(weights), kv_dev, n_pages,
+    _check(load().mk_decode_step_static(C.byref(desc), C.byref(weights), packed_dev, kv_dev, n_pages,
                                         block_table_dev, max_pages_per_seq, _i32(slots),
                                         _i32(positions), _i32(pages), n, tokens_dev,
                                         out_tokens_dev, status_dev or None, stream))

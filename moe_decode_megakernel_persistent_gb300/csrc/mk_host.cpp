@@ -58,6 +58,9 @@ struct mk_ctx {
   const void* final_norm = nullptr;
   const void* lm_head = nullptr;
   const void* lm_head_s = nullptr;
+  uint8_t* packed_dev = nullptr;   // the library's packed copy of the linear weights
+  size_t packed_bytes = 0;
+  const uint8_t* lm_pk = nullptr;
   float2* rope_dev = nullptr;
   void* scratch_dev = nullptr;
   size_t scratch_bytes = 0;
@@ -81,8 +84,8 @@ namespace {
 
 int validate_desc(const mk_model_desc* d, int* shape) {
   if (!d) return fail(MK_ERR_INVALID_ARG, "model description is NULL");
-  if (d->n_layers < 1 || d->vocab < 1 || d->n_dense < 0 || d->n_dense > d->n_layers)
-    return fail(MK_ERR_INVALID_ARG, "n_layers / vocab / n_dense out of range");
+  if (d->n_layers < 1 || d->n_layers > kMaxLayers || d->vocab < 1 || d->n_dense < 0 || d->n_dense > d->n_layers)
+    return fail(MK_ERR_INVALID_ARG, "n_layers (1..128) / vocab / n_dense out of range");
   if (d->wdtype == MK_INT4_G64 && d->vocab % 8 != 0)
     return fail(MK_ERR_UNSUPPORTED, "int4 lm_head needs a vocabulary that is a multiple of 8 rows");
   if (d->page_tokens != kPageTokens) return fail(MK_ERR_UNSUPPORTED, "page_tokens must be 128");
@@ -218,6 +221,7 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
   a.final_norm = c->final_norm;
   a.lm_head = c->lm_head;
   a.lm_head_s = c->lm_head_s;
+  a.lm_pk = c->lm_pk;
   a.rope = c->rope_dev;
   a.kv = c->kv_dev;
   a.block_table = c->block_table_dev;
@@ -257,6 +261,7 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
 namespace mk {
 
 int host_fail(int code, const char* msg) { return fail(code, msg); }
+int host_validate_desc(const mk_model_desc* d, int* shape) { return validate_desc(d, shape); }
 void host_clear_error() { g_err.clear(); }
 
 size_t host_carve_scratch(const mk_model_desc& d, int grid, int max_units, char* base, Scratch* sc) {
@@ -414,11 +419,25 @@ MK_API int mk_create(const mk_model_desc* d, const mk_weights* w, mk_ctx** out) 
     return fail(MK_ERR_UNSUPPORTED, "one block per SM cannot be resident (occupancy check)");
   }
 
-  // weights (borrowed) and the per-layer pointer table
+  // weights: the linear layers are copied into the packed layout (mk_pack.cu);
+  // embedding, norms and router stay borrowed
   c->embed = w->embed;
   c->final_norm = w->final_norm;
   c->lm_head = w->lm_head.w;
   c->lm_head_s = int4 ? w->lm_head.scales : nullptr;
+  {
+    PackLayout pl;
+    c->packed_bytes = host_pack_layout(*d, &pl);
+    e = cudaMalloc(&c->packed_dev, c->packed_bytes);
+    if (e != cudaSuccess)
+      return bail(fail(MK_ERR_CUDA, std::string("cudaMalloc(packed weights): ") + cudaGetErrorString(e)));
+    if (int r = host_pack(*d, *w, c->packed_dev, 0)) return bail(r);
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return bail(fail(MK_ERR_CUDA, std::string("weight pack: ") + cudaGetErrorString(e)));
+    for (int l = 0; l < d->n_layers; ++l)
+      for (int k = 0; k < NPK; ++k) lw[l].pk[k] = c->packed_dev + pl.layer[l][k];
+    c->lm_pk = c->packed_dev + pl.lm;
+  }
   e = cudaMalloc(&c->layers_dev, sizeof(LayerW) * d->n_layers);
   if (e != cudaSuccess) return bail(fail(MK_ERR_CUDA, std::string("cudaMalloc(layers): ") + cudaGetErrorString(e)));
   e = cudaMemcpy(c->layers_dev, lw.data(), sizeof(LayerW) * d->n_layers, cudaMemcpyHostToDevice);
@@ -619,6 +638,7 @@ MK_API int mk_destroy(mk_ctx* c) {
   if (!c) return MK_OK;
   cudaError_t e = cudaDeviceSynchronize();
   cudaFree(c->layers_dev);
+  cudaFree(c->packed_dev);
   cudaFree(c->rope_dev);
   cudaFree(c->scratch_dev);
   cudaFree(c->kv_dev);

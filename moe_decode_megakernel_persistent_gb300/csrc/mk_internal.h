@@ -24,6 +24,10 @@ constexpr int kSmemBytes = 227 * 1024;  // dynamic shared memory per block (the 
 // Linear-weight slots of a layer.
 enum Lin { WQ = 0, WK, WV, WO, GATE, UP, DOWN, EGATE, EUP, EDOWN, NLIN };
 
+// Blocks of the packed linear weights of a layer (see mk_pack.cu).
+enum PackBlock { PK_QKV = 0, PK_O, PK_GU, PK_DN, NPK };
+constexpr int kMaxLayers = 128;
+
 // Device-side copy of one layer's weight pointers.
 struct LayerW {
   const void* attn_norm;
@@ -31,6 +35,13 @@ struct LayerW {
   const void* router;
   const void* w[NLIN];
   const void* s[NLIN];   // int4 scales (null otherwise)
+  const uint8_t* pk[NPK];  // packed records (QKV pairs, o_proj, gate/up pairs, down)
+};
+
+// Byte offsets of the packed blocks inside one packed buffer.
+struct PackLayout {
+  size_t layer[kMaxLayers][NPK];
+  size_t lm;
 };
 
 struct PageUpd {
@@ -63,6 +74,7 @@ struct StepArgs {
   const void* final_norm;
   const void* lm_head;
   const void* lm_head_s;
+  const uint8_t* lm_pk;      // packed lm_head records
   const float2* rope;        // [max_ctx][hd/2] (cos, sin)
   uint16_t* kv;              // bf16 pool
   int32_t* block_table;      // [max_seqs][max_pages_per_seq]
@@ -115,5 +127,14 @@ size_t host_carve_scratch(const mk_model_desc& d, int grid, int max_units, char*
 void host_attention_split(int n_kv_heads, int grid, const int32_t* pos, int n, int* chunk, int* units);
 int host_fail(int code, const char* msg);
 void host_clear_error();
+int host_validate_desc(const mk_model_desc* d, int* shape);
+
+// Packed weights (mk_pack.cu): record sizes, the layout (returns the total
+// bytes; pl may be null) and the pack itself (kernels on stream st).
+int pack_row_bytes(int wdtype, int K);
+int pack_scale_bytes(int wdtype, int K);
+int pack_rec_bytes(int wdtype, int K);
+size_t host_pack_layout(const mk_model_desc& d, PackLayout* pl);
+int host_pack(const mk_model_desc& d, const mk_weights& w, uint8_t* dst, cudaStream_t st);
 
 }  // namespace mk

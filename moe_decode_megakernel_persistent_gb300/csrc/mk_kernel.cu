@@ -211,32 +211,32 @@ struct Model {
   using GE = Gemv<WDT, FE>;
   using GD = Gemv<WDT, FD>;
 
-  // ring stage: data bytes (+ int4 scales, 1/16 of the codes)
-  static constexpr int STD = WDT == WBF16 ? 32768 : 16384;
-  static constexpr int AUXB = WDT == WINT4 ? STD / 16 : 0;
-  static constexpr int STAGE = STD + AUXB;
+  // ring stage: 17 KB for int4 (16 KB of codes + their scales), 32 KB for
+  // bf16 and 16 KB for fp32 weights
+  static constexpr int STAGE = WDT == WINT4 ? 17408 : (WDT == WBF16 ? 32768 : 16384);
   __host__ __device__ static constexpr int cmax(int a, int b) { return a > b ? a : b; }
-  // task ranges and tiles start at multiples of A rows (16-byte aligned scales)
-  static constexpr int A_Q = GH::A;
-  // hidden rows go to blocks in groups of at least 2, so a block's slice of
-  // a bf16 row (router, norm) starts and ends on a 4-byte boundary
-  static constexpr int A_H = cmax(2, cmax(GQ::A, cmax(GE::A, GD::A)));
-  __host__ __device__ static constexpr int tmax(int rp, int rb, int sb, int al) {
-    int t = STD / (rp * rb);
-    if (sb) t = t < AUXB / (rp * sb) ? t : AUXB / (rp * sb);
-    return t - t % al;
+  // a packed weight record: one row's codes, then its scales, 16-byte aligned
+  template <int K>
+  __host__ __device__ static constexpr int rec() {
+    return (Gemv<WDT, K>::ROW_BYTES + Gemv<WDT, K>::SCALE_BYTES + 15) / 16 * 16;
   }
-  static constexpr int T_QKV = tmax(2, GH::ROW_BYTES, GH::SCALE_BYTES, A_Q);
-  static constexpr int T_O = tmax(1, GQ::ROW_BYTES, GQ::SCALE_BYTES, A_H);
-  static constexpr int T_GU = tmax(2, GH::ROW_BYTES, GH::SCALE_BYTES, A_Q);
-  static constexpr int T_DN = tmax(1, GE::ROW_BYTES, GE::SCALE_BYTES, A_H);
-  static constexpr int T_DD = tmax(1, GD::ROW_BYTES, GD::SCALE_BYTES, A_H);
-  static constexpr int T_LM = tmax(1, GH::ROW_BYTES, GH::SCALE_BYTES, A_Q);
+  static constexpr int REC_H = rec<H>(), REC_Q = rec<QD>(), REC_E = rec<FE>(), REC_D = rec<FD>();
+  // hidden rows go to blocks in groups of 2, so a block's slice of a bf16 row
+  // (router, norm) starts and ends on a 4-byte boundary
+  static constexpr int A_Q = 1;
+  static constexpr int A_H = 2;
+  // tasks per tile (RP records each)
+  static constexpr int T_QKV = STAGE / (2 * REC_H);
+  static constexpr int T_O = STAGE / REC_Q;
+  static constexpr int T_GU = STAGE / (2 * REC_H);
+  static constexpr int T_DN = STAGE / REC_E;
+  static constexpr int T_DD = STAGE / REC_D;
+  static constexpr int T_LM = STAGE / REC_H;
   static_assert(T_QKV >= 1 && T_O >= 1 && T_GU >= 1 && T_DN >= 1 && T_DD >= 1 && T_LM >= 1, "tile sizes");
-  static constexpr int TU = STD / (4 * HD) / kWarps;  // positions per warp per stage
+  static constexpr int TU = STAGE / (4 * HD) / kWarps;  // positions per warp per stage
   static constexpr int TT = TU * kWarps;              // cached positions per stage (K and V rows, bf16)
   static_assert(TU >= 1, "a stage holds a position per warp");
-  static_assert(HALF % A_Q == 0 && FE % A_Q == 0 && FD % A_Q == 0 && H % A_H == 0, "aligned row groups");
+  static_assert(H % A_H == 0, "aligned row groups");
   static_assert(TOPK <= 8 && E <= 64, "router tables");
 
   static constexpr int NQP = NH * HALF, NKP = NKV * HALF, NP = NQP + 2 * NKP;
@@ -329,13 +329,14 @@ struct Model {
 #pragma unroll 1
       for (int j = j_first; j < j_end; j += CONTIG ? 1 : kWarps) {
         const int t = t0 + j;
+        constexpr int RC = rec<K>();
         const uint8_t* wr[2];
         const uint8_t* sr[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const int rr = r < RP ? r : 0;
-          wr[r] = st + (rr * T + j) * Gv::ROW_BYTES;
-          sr[r] = st + STD + (rr * T + j) * Gv::SCALE_BYTES;
+          wr[r] = st + (size_t)(j * RP + rr) * RC;
+          sr[r] = wr[r] + Gv::ROW_BYTES;
         }
         const ActRange ar = task.acts(t);
 #pragma unroll 1
@@ -430,7 +431,7 @@ struct Model {
     using Gv = Gemv<WDT, K>;
     constexpr int NGR = K / 64;
     constexpr int MT = RP == 2 ? 8 : 16;
-    constexpr int RB = Gv::ROW_BYTES, SB = Gv::SCALE_BYTES, AS = plain_stride(K);
+    constexpr int RB = Gv::ROW_BYTES, AS = plain_stride(K);
     static_assert(K % 64 == 0, "whole 64-value groups");
     Fixed& F = fixed();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, q = lane & 3;
@@ -465,10 +466,11 @@ struct Model {
               else { j0 = ta + g; j1 = ta + 8 + g; seg1 = 0; }
               j0 = j0 < tb ? j0 : ta;
               j1 = j1 < tb ? j1 : ta;
-              const uint8_t* w0 = st + (size_t)j0 * RB;
-              const uint8_t* w1 = st + (size_t)(seg1 * T + j1) * RB;
-              const uint8_t* s0p = st + STD + (size_t)j0 * SB;
-              const uint8_t* s1p = st + STD + (size_t)(seg1 * T + j1) * SB;
+              constexpr int RC = rec<K>();
+              const uint8_t* w0 = st + (size_t)(j0 * RP) * RC;
+              const uint8_t* w1 = st + (size_t)(j1 * RP + seg1) * RC;
+              const uint8_t* s0p = w0 + RB;
+              const uint8_t* s1p = w1 + RB;
               // this lane's activation column
               const int col = c0 + g;
               const bool cv = col < ar.count;
@@ -1334,12 +1336,9 @@ struct Model {
   }
 
   // ---------------------------------------------------------------- streaming warp
-  // One run of `cnt` consecutive rows (codes at w0, scales at s0) into
-  // segment `seg` of a tile of T tasks, starting at task j.
-  __device__ static __forceinline__ void put_run(Producer& p, int seg, int T, int j, int cnt, const void* w0,
-                                                 const void* s0, int rb, int sb) {
-    p.copy((uint32_t)((seg * T + j) * rb), w0, (uint32_t)(cnt * rb));
-    if (sb) p.copy((uint32_t)(STD + (seg * T + j) * sb), s0, (uint32_t)(cnt * sb));
+  // One run of `cnt` consecutive packed records into the stage at record j.
+  __device__ static __forceinline__ void put_recs(Producer& p, int j, int cnt, const uint8_t* src, int rc) {
+    p.copy((uint32_t)(j * rc), src, (uint32_t)(cnt * rc));
   }
 
   // Pool pages of this block's attention units (positions before new0 only,
@@ -1376,9 +1375,8 @@ struct Model {
   }
 
   // The block's schedule of ring items for the whole launch, in the order the
-  // compute warps consume them (lane 0 of the streaming warp).  Runs of rows
-  // contiguous in memory are known from the layouts: a QKV run ends at a head
-  // boundary, an expert run at an expert boundary.
+  // compute warps consume them (lane 0 of the streaming warp).  Every tile is
+  // one run of packed records, or one run per expert.
   __device__ static __noinline__ void produce() {
     Producer p;  // registers of the streaming lane; the item count goes to F.prod_k
     run_schedule(p);
@@ -1389,31 +1387,16 @@ struct Model {
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
     const int n = c.n;
-    constexpr int RBH = GH::ROW_BYTES, SBH = GH::SCALE_BYTES;
 #pragma unroll 1
     for (int l = 0; l < a.n_layers; ++l) {
       const LayerW Lg = a.layers[l];  // one batch of loads per layer
-      {  // P1: pair tasks [p0, p1); a run stays inside one head of one matrix
+      {  // P1: RoPE pair tasks [p0, p1): records 2p, 2p + 1
         int p0, p1;
         qkv_range(c, p0, p1);
 #pragma unroll 1
         for (int ta = p0; ta < p1; ta += T_QKV) {
           if (!p.template begin<STAGE>()) return;
-          const int tb = min(p1, ta + T_QKV);
-#pragma unroll 1
-          for (int q0 = ta; q0 < tb;) {
-            const int q1 = min(tb, (q0 / HALF + 1) * HALF);
-            int m, qq;
-            if (q0 < NQP) { m = WQ; qq = q0; }
-            else if (q0 < NQP + NKP) { m = WK; qq = q0 - NQP; }
-            else { m = WV; qq = q0 - NQP - NKP; }
-            const size_t row = (size_t)(qq / HALF) * HD + qq % HALF;
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-              put_run(p, r, T_QKV, q0 - ta, q1 - q0, (const uint8_t*)Lg.w[m] + (row + r * HALF) * RBH,
-                      (const uint8_t*)Lg.s[m] + (row + r * HALF) * SBH, RBH, SBH);
-            q0 = q1;
-          }
+          put_recs(p, 0, 2 * min(T_QKV, p1 - ta), Lg.pk[PK_QKV] + (size_t)2 * ta * REC_H, REC_H);
           p.end();
         }
       }
@@ -1445,13 +1428,11 @@ struct Model {
           }
         }
       }
-      // P3: o_proj rows [r0, r0 + nr), one run
+      // P3: o_proj rows [r0, r0 + nr)
 #pragma unroll 1
       for (int t0 = 0; t0 < c.nr; t0 += T_O) {
         if (!p.template begin<STAGE>()) return;
-        const size_t row = (size_t)(c.r0 + t0);
-        put_run(p, 0, T_O, 0, min(T_O, c.nr - t0), (const uint8_t*)Lg.w[WO] + row * GQ::ROW_BYTES,
-                (const uint8_t*)Lg.s[WO] + row * GQ::SCALE_BYTES, GQ::ROW_BYTES, GQ::SCALE_BYTES);
+        put_recs(p, 0, min(T_O, c.nr - t0), Lg.pk[PK_O] + (size_t)(c.r0 + t0) * REC_Q, REC_Q);
         p.end();
       }
       if (l >= a.n_dense) {
@@ -1477,13 +1458,10 @@ struct Model {
           if (!p.template begin<STAGE>()) return;
           const int tb = min(u1, ta + T_GU);
 #pragma unroll 1
-          for (int q0 = ta; q0 < tb;) {  // a run stays inside one expert
+          for (int q0 = ta; q0 < tb;) {  // a run stays inside one expert: records 2t, 2t + 1
             const int q1 = min(tb, (q0 / FE + 1) * FE);
-            const size_t row = (size_t)F.ue_expert[q0 / FE] * FE + q0 % FE;
-            put_run(p, 0, T_GU, q0 - ta, q1 - q0, (const uint8_t*)Lg.w[EGATE] + row * RBH,
-                    (const uint8_t*)Lg.s[EGATE] + row * SBH, RBH, SBH);
-            put_run(p, 1, T_GU, q0 - ta, q1 - q0, (const uint8_t*)Lg.w[EUP] + row * RBH,
-                    (const uint8_t*)Lg.s[EUP] + row * SBH, RBH, SBH);
+            const size_t t = (size_t)F.ue_expert[q0 / FE] * FE + q0 % FE;
+            put_recs(p, 2 * (q0 - ta), 2 * (q1 - q0), Lg.pk[PK_GU] + 2 * t * REC_H, REC_H);
             q0 = q1;
           }
           p.end();
@@ -1502,8 +1480,7 @@ struct Model {
             for (int q0 = ta; q0 < tb;) {  // a run stays inside one expert
               const int q1 = min(tb, (q0 / nr + 1) * nr);
               const size_t row = (size_t)F.ue_expert[ua + q0 / nr] * H + c.r0 + q0 % nr;
-              put_run(p, 0, T_DN, q0 - ta, q1 - q0, (const uint8_t*)Lg.w[EDOWN] + row * GE::ROW_BYTES,
-                      (const uint8_t*)Lg.s[EDOWN] + row * GE::SCALE_BYTES, GE::ROW_BYTES, GE::SCALE_BYTES);
+              put_recs(p, q0 - ta, q1 - q0, Lg.pk[PK_DN] + row * REC_E, REC_E);
               q0 = q1;
             }
             p.end();
@@ -1516,11 +1493,7 @@ struct Model {
 #pragma unroll 1
         for (int t0 = f0; t0 < f1; t0 += T_GU) {
           if (!p.template begin<STAGE>()) return;
-          const int cnt = min(T_GU, f1 - t0);
-          put_run(p, 0, T_GU, 0, cnt, (const uint8_t*)Lg.w[GATE] + (size_t)t0 * RBH,
-                  (const uint8_t*)Lg.s[GATE] + (size_t)t0 * SBH, RBH, SBH);
-          put_run(p, 1, T_GU, 0, cnt, (const uint8_t*)Lg.w[UP] + (size_t)t0 * RBH,
-                  (const uint8_t*)Lg.s[UP] + (size_t)t0 * SBH, RBH, SBH);
+          put_recs(p, 0, 2 * min(T_GU, f1 - t0), Lg.pk[PK_GU] + (size_t)2 * t0 * REC_H, REC_H);
           p.end();
         }
         const int cap = c.act_bytes / dense_entry_bytes(c);
@@ -1529,9 +1502,7 @@ struct Model {
 #pragma unroll 1
           for (int t0 = 0; t0 < c.nr; t0 += T_DD) {
             if (!p.template begin<STAGE>()) return;
-            const size_t row = (size_t)(c.r0 + t0);
-            put_run(p, 0, T_DD, 0, min(T_DD, c.nr - t0), (const uint8_t*)Lg.w[DOWN] + row * GD::ROW_BYTES,
-                    (const uint8_t*)Lg.s[DOWN] + row * GD::SCALE_BYTES, GD::ROW_BYTES, GD::SCALE_BYTES);
+            put_recs(p, 0, min(T_DD, c.nr - t0), Lg.pk[PK_DN] + (size_t)(c.r0 + t0) * REC_D, REC_D);
             p.end();
           }
         }
@@ -1543,8 +1514,7 @@ struct Model {
 #pragma unroll 1
       for (int t0 = v0; t0 < v1; t0 += T_LM) {
         if (!p.template begin<STAGE>()) return;
-        put_run(p, 0, T_LM, 0, min(T_LM, v1 - t0), (const uint8_t*)a.lm_head + (size_t)t0 * RBH,
-                (const uint8_t*)a.lm_head_s + (size_t)t0 * SBH, RBH, SBH);
+        put_recs(p, 0, min(T_LM, v1 - t0), a.lm_pk + (size_t)t0 * REC_H, REC_H);
         p.end();
       }
     }

@@ -5,8 +5,10 @@
 // partials, router partials, expert activations, argmax candidates, barrier
 // counters and the error word) lives in one file-scope device array of
 // kStaticBytes bytes.  Every GPU that loads the library holds that array
-// until the process exits.  Weights, the KV cache and its block table,
-// tokens and outputs are the caller's memory.
+// until the process exits.  Weights (the logical tensors for embedding, norms
+// and router, and the packed copy of the linear layers made by
+// mk_pack_weights), the KV cache and its block table, tokens and outputs are
+// the caller's memory.
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -81,7 +83,7 @@ int setup(int dev, const mk_model_desc& d, char** base) {
 using namespace mk;
 
 extern "C" MK_API int mk_decode_step_static(
-    const mk_model_desc* d, const mk_weights* w, void* kv_dev, int32_t n_pages,
+    const mk_model_desc* d, const mk_weights* w, const void* packed_dev, void* kv_dev, int32_t n_pages,
     int32_t* block_table_dev, int32_t max_pages_per_seq, const int32_t* slots_host,
     const int32_t* positions_host, const int32_t* pages_host, int32_t n,
     const int32_t* tokens_dev, int32_t* out_tokens_dev, int32_t* status_dev, void* stream) {
@@ -92,6 +94,13 @@ extern "C" MK_API int mk_decode_step_static(
     return host_fail(MK_ERR_INVALID_ARG, "more layers than the static layer table holds (128)");
   LayerW layers[kMaxStaticLayers];
   if (int r = host_check_model(d, w, &shape, layers)) return r;
+  if (!packed_dev || (reinterpret_cast<uintptr_t>(packed_dev) & 255u) != 0)
+    return host_fail(MK_ERR_INVALID_ARG, "packed weights (mk_pack_weights) missing or not 256-byte aligned");
+  PackLayout pl;
+  host_pack_layout(*d, &pl);
+  const uint8_t* pk = static_cast<const uint8_t*>(packed_dev);
+  for (int l = 0; l < d->n_layers; ++l)
+    for (int k = 0; k < NPK; ++k) layers[l].pk[k] = pk + pl.layer[l][k];
   if (!kv_dev || !block_table_dev || !slots_host || !positions_host || !pages_host || !tokens_dev ||
       !out_tokens_dev)
     return host_fail(MK_ERR_INVALID_ARG, "NULL argument");
@@ -156,6 +165,7 @@ extern "C" MK_API int mk_decode_step_static(
   a.final_norm = w->final_norm;
   a.lm_head = w->lm_head.w;
   a.lm_head_s = d->wdtype == MK_INT4_G64 ? w->lm_head.scales : nullptr;
+  a.lm_pk = pk + pl.lm;
   a.rope = reinterpret_cast<const float2*>(base);
   a.kv = static_cast<uint16_t*>(kv_dev);
   a.block_table = block_table_dev;

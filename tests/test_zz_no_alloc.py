@@ -66,9 +66,14 @@ def test_static_entry_matches_context_entry(gpu_lib, wdtype):
     eng.sync()
     eng.close()
 
-    # the allocation-free entry point on caller-owned KV pool and block table
+    # the allocation-free entry point on caller-owned packed weights, KV pool
+    # and block table
     desc = eng.desc
     ws, _keep = _weights_struct(m, w)
+    pbytes = L.mk_packed_bytes(desc)
+    assert pbytes > 0
+    packed = torch.empty(pbytes, dtype=torch.uint8, device="cuda")
+    L.mk_pack_weights(desc, ws, _ptr(packed), pbytes, torch.cuda.current_stream().cuda_stream)
     page_elems = m.n_layers * 2 * m.n_kv_heads * 128 * m.head_dim
     kv = torch.zeros(n_pages * page_elems, dtype=torch.int16, device="cuda")
     maxpp = (max_ctx + 127) // 128
@@ -78,7 +83,8 @@ def test_static_entry_matches_context_entry(gpu_lib, wdtype):
     got = []
     for p in range(PROMPT + DECODE):
         tin = prompt[p:p + 1] if p < PROMPT else out
-        L.mk_decode_step_static(desc, ws, _ptr(kv), n_pages, _ptr(table), maxpp, [0], [p], [p // 128],
+        L.mk_decode_step_static(desc, ws, _ptr(packed), _ptr(kv), n_pages, _ptr(table), maxpp, [0], [p],
+                                [p // 128],
                                 _ptr(tin), _ptr(out), _ptr(status), stream)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
@@ -93,14 +99,16 @@ def test_static_entry_rejects_out_of_range_input(gpu_lib):
     from moe_decode_megakernel_persistent_gb300.engine import make_desc
     d = make_desc(m, max_ctx=16384)
     ws, _keep = _weights_struct(m, w)
+    packed = torch.empty(L.mk_packed_bytes(d), dtype=torch.uint8, device="cuda")
+    L.mk_pack_weights(d, ws, _ptr(packed), packed.numel(), torch.cuda.current_stream().cuda_stream)
     kv = torch.zeros(1024, dtype=torch.int16, device="cuda")
     table = torch.zeros((64, 128), dtype=torch.int32, device="cuda")
     tok = torch.zeros(1, dtype=torch.int32, device="cuda")
     with pytest.raises(L.MKError) as e:      # beyond the static RoPE table
-        L.mk_decode_step_static(d, ws, _ptr(kv), 1, _ptr(table), 128, [0], [8192], [0],
+        L.mk_decode_step_static(d, ws, _ptr(packed), _ptr(kv), 1, _ptr(table), 128, [0], [8192], [0],
                                 _ptr(tok), _ptr(tok))
     assert e.value.code == L.MK_ERR_INVALID_ARG and "8192" in str(e.value)
     with pytest.raises(L.MKError) as e:      # page outside the caller's pool
-        L.mk_decode_step_static(d, ws, _ptr(kv), 1, _ptr(table), 128, [0], [0], [3],
+        L.mk_decode_step_static(d, ws, _ptr(packed), _ptr(kv), 1, _ptr(table), 128, [0], [0], [3],
                                 _ptr(tok), _ptr(tok))
     assert e.value.code == L.MK_ERR_INVALID_ARG
