@@ -135,7 +135,7 @@ size_t carve_scratch(const mk_model_desc& d, int grid, int max_units, char* base
   s.q = (float*)take(sizeof(float) * kMaxBatch * QD);
   s.attn = (float*)take(sizeof(float) * kMaxBatch * QD);
   s.part = (float*)take(sizeof(float) * (size_t)max_units * GQA * (d.head_dim + 4));
-  s.rlogit = (float*)take(sizeof(float) * kMaxBatch * d.n_experts);
+  s.rlogit = (float*)take(sizeof(float) * kRlogitGroups * kMaxBatch * d.n_experts);
   s.act = (float*)take(sizeof(float) * kMaxBatch * d.top_k * d.expert_ffn);
   s.dact = (float*)take(sizeof(float) * kMaxBatch * d.dense_ffn);
   s.amax_v = (float*)take(sizeof(float) * (size_t)grid * kMaxBatch);
@@ -147,21 +147,33 @@ size_t carve_scratch(const mk_model_desc& d, int grid, int max_units, char* base
   return off;
 }
 
-// Split of the attention work: chunk length (a multiple of 16 positions)
-// chosen so that all (row, kv-head, chunk) units roughly fill the grid once.
-void attention_split(const mk_ctx* c, const int32_t* pos, int n, int* chunk, int* units) {
+// Split of the attention work: (row, kv head, chunk) units that roughly fill
+// the grid once, with chunks a whole number of ring tiles (tile_tokens
+// cached positions each) and at most kMaxChunks chunks per row.
+void host_attention_split_impl(int n_kv_heads, int grid, int tile_tokens, const int32_t* pos, int n, int* chunk,
+                               int* units) {
   long long total = 0, longest = 0;
   for (int i = 0; i < n; ++i) {
     total += pos[i] + 1;
     longest = std::max<long long>(longest, pos[i] + 1);
   }
-  long long ch = (c->d.n_kv_heads * total + c->grid - 1) / c->grid;
+  const long long tt = std::max(1, tile_tokens);
+  long long ch = (n_kv_heads * total + grid - 1) / grid;
   ch = std::max(ch, (longest + kMaxChunks - 1) / kMaxChunks);  // at most kMaxChunks chunks per row
-  ch = std::max<long long>(16, (ch + 15) / 16 * 16);
+  ch = std::max<long long>(8, (ch + tt - 1) / tt * tt);
   long long u = 0;
-  for (int i = 0; i < n; ++i) u += c->d.n_kv_heads * ((pos[i] + 1 + ch - 1) / ch);
+  for (;;) {  // a block takes at most kMaxOwnUnits units
+    u = 0;
+    for (int i = 0; i < n; ++i) u += n_kv_heads * ((pos[i] + 1 + ch - 1) / ch);
+    if (u <= (long long)kMaxOwnUnits * grid || ch >= longest) break;
+    ch += tt;
+  }
   *chunk = (int)ch;
   *units = (int)u;
+}
+
+void attention_split(const mk_ctx* c, const int32_t* pos, int n, int* chunk, int* units) {
+  host_attention_split_impl(c->d.n_kv_heads, c->grid, c->kern.tile_tokens, pos, n, chunk, units);
 }
 
 // One launch over `n` rows.  Pages for positions that start a new page are
@@ -212,6 +224,7 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
       if (a.slot[j] == a.slot[i] && a.pos[j] < a.new0[i]) a.new0[i] = a.pos[j];
   }
   attention_split(c, positions, n, &a.chunk, &a.n_units);
+  if (a.n_units > kMaxOwnUnits * c->grid) return fail(MK_ERR_INVALID_ARG, "more attention units than the grid can merge");
   if (a.n_units > c->max_units) {
     rollback();
     return fail(MK_ERR_INVALID_ARG, "attention split exceeds the partials buffer");
@@ -268,19 +281,9 @@ size_t host_carve_scratch(const mk_model_desc& d, int grid, int max_units, char*
   return carve_scratch(d, grid, max_units, base, sc);
 }
 
-void host_attention_split(int n_kv_heads, int grid, const int32_t* pos, int n, int* chunk, int* units) {
-  long long total = 0, longest = 0;
-  for (int i = 0; i < n; ++i) {
-    total += pos[i] + 1;
-    longest = std::max<long long>(longest, pos[i] + 1);
-  }
-  long long ch = (n_kv_heads * total + grid - 1) / grid;
-  ch = std::max(ch, (longest + kMaxChunks - 1) / kMaxChunks);  // at most kMaxChunks chunks per row
-  ch = std::max<long long>(16, (ch + 15) / 16 * 16);
-  long long u = 0;
-  for (int i = 0; i < n; ++i) u += n_kv_heads * ((pos[i] + 1 + ch - 1) / ch);
-  *chunk = (int)ch;
-  *units = (int)u;
+void host_attention_split(int n_kv_heads, int grid, int tile_tokens, const int32_t* pos, int n, int* chunk,
+                          int* units) {
+  host_attention_split_impl(n_kv_heads, grid, tile_tokens, pos, n, chunk, units);
 }
 
 int host_check_model(const mk_model_desc* d, const mk_weights* w, int* shape, LayerW* lw) {

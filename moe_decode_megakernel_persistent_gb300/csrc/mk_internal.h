@@ -16,8 +16,10 @@ constexpr int kThreads = 480;        // compute threads per block (15 warps)
 constexpr int kWarps = kThreads / 32;
 constexpr int kBlockThreads = kThreads + 32;  // plus one weight-streaming warp
 constexpr int kMaxStages = 16;       // shared-memory ring stages
+constexpr int kRlogitGroups = 8;     // copies of the router-logit sums (less atomic contention)
 constexpr int kMaxUpd = 64;          // block-table updates carried by one launch
 constexpr int kMaxRowsPerBlock = 32; // hidden rows owned by one block (hidden / grid)
+constexpr int kMaxOwnUnits = 4;     // attention units one block may take in a launch
 constexpr int kMaxChunks = 64;       // attention chunks per (row, kv head): one per lane-pair of a warp
 constexpr int kSmemBytes = 227 * 1024;  // dynamic shared memory per block (the sm_100 family maximum)
 
@@ -57,7 +59,8 @@ struct Scratch {
   float* q;          // [kMaxBatch][n_heads*hd] roped queries
   float* attn;       // [kMaxBatch][n_heads*hd] merged attention output
   float* part;       // [max_units][gqa][hd + 2] attention partials (m, l, o[hd])
-  float* rlogit;     // [kMaxBatch][E] router logits before the RMS scale (block partials summed)
+  float* rlogit;     // [kRlogitGroups][kMaxBatch][E] router logits before the RMS scale: block
+                     // partials summed into one of kRlogitGroups copies (block id mod groups)
   float* act;        // [kMaxBatch][top_k][Fe] expert activations
   float* dact;       // [kMaxBatch][Fd] dense-MLP activations
   float* amax_v;     // [grid][kMaxBatch] per-block best logit
@@ -114,6 +117,7 @@ enum ShapeId { SHAPE_FLINT = 0, SHAPE_TINY = 1, NSHAPE };
 struct KernelInfo {
   const void* fn;
   int smem_bytes;
+  int tile_tokens;  // cached positions per ring stage (attention chunks are multiples)
 };
 
 // Returns the kernel for (shape, wdtype) or fn == nullptr if not compiled.
@@ -124,7 +128,8 @@ KernelInfo get_kernel(int shape, int wdtype);
 // the per-layer pointer table (status code; message via mk_last_error).
 int host_check_model(const mk_model_desc* d, const mk_weights* w, int* shape, LayerW* layers);
 size_t host_carve_scratch(const mk_model_desc& d, int grid, int max_units, char* base, Scratch* sc);
-void host_attention_split(int n_kv_heads, int grid, const int32_t* pos, int n, int* chunk, int* units);
+void host_attention_split(int n_kv_heads, int grid, int tile_tokens, const int32_t* pos, int n, int* chunk,
+                          int* units);
 int host_fail(int code, const char* msg);
 void host_clear_error();
 int host_validate_desc(const mk_model_desc* d, int* shape);

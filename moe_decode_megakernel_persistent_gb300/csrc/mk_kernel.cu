@@ -78,6 +78,7 @@ struct Fixed {
   uint8_t ent_of[kMaxBatch][8];
   uint8_t efirst[kMaxEnt];
   int n_ue, flag;
+  int n_merge, merge_job[kMaxOwnUnits][4];  // attention merges this block owes: (b, g, h0, h1)
 };
 constexpr int kActOffset = (sizeof(Fixed) + 127) / 128 * 128;
 
@@ -299,6 +300,10 @@ struct Model {
     rt1 = min(t1, max(t0, a.new0[b]));
   }
 
+  static __device__ __forceinline__ bool same_acts(const ActRange& x, const ActRange& y) {
+    return x.list == y.list && x.start == y.start && x.count == y.count;
+  }
+
   // ---- generic GEMV over ring tiles.  Tasks [0, ntask) of the phase, T per
   // ring item; task t runs on warp t % kWarps, or (CONTIG) each warp takes a
   // contiguous block of a tile's tasks (tasks sharing an activation stay on
@@ -327,18 +332,22 @@ struct Model {
       const int j_first = CONTIG ? wid * per : ((wid - t0) % kWarps + kWarps) % kWarps;
       const int j_end = CONTIG ? min(tn, j_first + per) : tn;
 #pragma unroll 1
-      for (int j = j_first; j < j_end; j += CONTIG ? 1 : kWarps) {
+      for (int j = j_first; j < j_end;) {
         const int t = t0 + j;
         constexpr int RC = rec<K>();
+        const ActRange ar = task.acts(t);
+        // one-row tasks of a contiguous block: two consecutive rows that share
+        // an activation list are dotted together (two independent chains)
+        bool pair = false;
+        if constexpr (RP == 1 && CONTIG) pair = j + 1 < j_end && same_acts(task.acts(t + 1), ar);
         const uint8_t* wr[2];
         const uint8_t* sr[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const int rr = r < RP ? r : 0;
-          wr[r] = st + (size_t)(j * RP + rr) * RC;
+          const int rowi = RP == 2 ? j * 2 + r : j + (pair ? r : 0);
+          wr[r] = st + (size_t)rowi * RC;
           sr[r] = wr[r] + Gv::ROW_BYTES;
         }
-        const ActRange ar = task.acts(t);
 #pragma unroll 1
         for (int i = 0; i < ar.count; ++i) {
           const int ai = ar.list ? ar.list[ar.start + i] : ar.start + i;
@@ -347,9 +356,18 @@ struct Model {
             if (ai != loaded) { Gv::load_act(a, ab, lane); loaded = ai; }
           }
           float v0, v1;
-          Gv::template dots<RP, REGS>(wr, sr, a, ab, lane, v0, v1);
-          if (lane == 0) task.put(t, ai, i, v0, v1);
+          if (RP == 2 || pair) {
+            Gv::template dots<2, REGS>(wr, sr, a, ab, lane, v0, v1);
+            if (lane == 0) {
+              if (RP == 2) task.put(t, ai, i, v0, v1);
+              else { task.put(t, ai, i, v0, 0.f); task.put(t + 1, ai, i, v1, 0.f); }
+            }
+          } else {
+            Gv::template dots<1, REGS>(wr, sr, a, ab, lane, v0, v1);
+            if (lane == 0) task.put(t, ai, i, v0, v1);
+          }
         }
+        j += CONTIG ? (pair ? 2 : 1) : kWarps;
       }
       ring_release(k);
     }
@@ -421,9 +439,6 @@ struct Model {
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  }
-  static __device__ __forceinline__ bool same_acts(const ActRange& x, const ActRange& y) {
-    return x.list == y.list && x.start == y.start && x.count == y.count;
   }
 
   template <int K, int RP, int T, class TK>
@@ -603,7 +618,7 @@ struct Model {
       for (int i = tid; i < a.n_upd; i += kThreads)
         a.block_table[a.upd[i].slot * a.max_pages_per_seq + a.upd[i].index] = a.upd[i].page;
     if (c.bid == 0 && l >= a.n_dense)  // router logits are accumulated in P3
-      for (int i = tid; i < n * E; i += kThreads) a.sc.rlogit[i] = 0.f;
+      for (int i = tid; i < kRlogitGroups * kMaxBatch * E; i += kThreads) a.sc.rlogit[i] = 0.f;
     if (l >= a.n_dense) fetch_router_slice(Lw);
     {
       const void* nw = Lw.attn_norm;
@@ -875,43 +890,85 @@ struct Model {
         pu[i * PR + 4 + d] = O;
       }
       csync();
+      // release this unit's partial; the last MG units of (b, g) to arrive
+      // (MG = min(GQA, nch)) each merge a share of the GQA heads once every
+      // unit of the layer has arrived (the counter grows by nch per layer
+      // and is cleared when the launch ends)
+      // (a merge waits for other blocks' units, so it runs only after this
+      // block has finished all of its own units: no two blocks wait on each
+      // other)
+      const int MG = min(GQA, nch);
       if (tid == 0) {
-        // release this unit's partial, acquire the others' if it is the last
         int old;
         asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
                      : "=r"(old) : "l"(a.sc.merge_cnt + b * NKV + g) : "memory");
-        F.flag = old == nch - 1;
+        const int arr = old - l * nch;
+        if (arr >= nch - MG) {
+          const int r = arr - (nch - MG);
+          if (F.n_merge >= kMaxOwnUnits) {  // the host bounds units per block
+            set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, u);
+            F.n_merge = kMaxOwnUnits - 1;
+          }
+          F.merge_job[F.n_merge][0] = b;
+          F.merge_job[F.n_merge][1] = g;
+          F.merge_job[F.n_merge][2] = r * GQA / MG;
+          F.merge_job[F.n_merge][3] = (r + 1) * GQA / MG;
+          ++F.n_merge;
+        }
       }
       csync();
-      if (F.flag) merge(l, b, g, nch);
+    }
+#pragma unroll 1
+    for (int jm = 0; jm < F.n_merge; ++jm) {
+      const int b = F.merge_job[jm][0], g = F.merge_job[jm][1];
+      const int nch = (a.pos[b] + 1 + a.chunk - 1) / a.chunk;
+      if (tid == 0) {
+        const int target = (l + 1) * nch;
+        const uint64_t ts = globaltimer();
+        F.flag = 1;
+        for (uint32_t i = 0;; ++i) {
+          int v;
+          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(a.sc.merge_cnt + b * NKV + g) : "memory");
+          if (v >= target) break;
+          if ((i & 31u) == 0 && (*(volatile int32_t*)a.sc.err != 0 || globaltimer() - ts > a.spin_limit_ns)) {
+            set_error(a.sc.err, MK_ERR_BARRIER_TIMEOUT, SITE_UNIT, b * NKV + g);
+            F.flag = 0;
+            break;
+          }
+        }
+      }
+      csync();
+      if (F.flag) merge(l, b, g, nch, F.merge_job[jm][2], F.merge_job[jm][3]);
       csync();
     }
-    if (tid == 0) F.kc = k;
+    if (tid == 0) {
+      F.kc = k;
+      F.n_merge = 0;
+    }
     csync();
   }
 
-  // Last unit of (b, g): log-sum-exp merge of its chunks into the attention
-  // output.
-  __device__ static __noinline__ void merge(int l, int b, int g, int nch) {
+  // Heads [h0, h1) of (b, g): log-sum-exp merge of the chunk partials into
+  // the attention output, in chunk order.
+  __device__ static __forceinline__ void merge(int l, int b, int g, int nch, int h0, int h1) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int n = c.n;
-    if (nch > kMaxChunks || nch * GQA > kThreads) {
+    if (nch > kMaxChunks) {
       if (tid == 0) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, nch);
       return;
     }
     const float* pb = a.sc.part + (size_t)(F.unit_start[b] + g * nch) * GQA * PR;
-    // float4 output o = (head, 4 dims) is summed by NG thread groups over
-    // chunks grp, grp + NG, ...; the first batch of chunk outputs is requested
-    // together with the (m, l) pairs, so the merge costs one L2 round trip
-    constexpr int NOUT4 = GQA * HD / 4;
-    constexpr int NG = kThreads / NOUT4;
-    constexpr int BATCH = 12;
-    static_assert(NG >= 1, "one float4 output per thread at least");
-    const bool sum_thread = tid < NG * NOUT4;
-    const int grp = tid / NOUT4, o4 = tid % NOUT4, hi = o4 / (HD / 4), d4 = o4 % (HD / 4);
+    // float4 output o = (head h0 + o / (HD/4), 4 dims) is summed by NG thread
+    // groups over chunks grp, grp + NG, ...; the first batch of chunk outputs
+    // is requested together with the (m, l) pairs: one L2 round trip
+    constexpr int BATCH = 5;
+    const int nout4 = (h1 - h0) * (HD / 4);
+    const int NG = kThreads / nout4;
+    const bool sum_thread = tid < NG * nout4;
+    const int grp = tid / nout4, o4 = tid % nout4, hi = h0 + o4 / (HD / 4), d4 = o4 % (HD / 4);
     float4 ov[BATCH];
     if (sum_thread) {
 #pragma unroll
@@ -924,8 +981,8 @@ struct Model {
     // one warp per head: M = max_c m_c, L = sum_c l_c exp(m_c - M), and the
     // chunk factors exp(m_c - M) / L into shared memory
     float* mfac = F.red;  // [nch][GQA]
-    if (wid < GQA) {
-      const int i = wid;
+    if (wid < h1 - h0) {
+      const int i = h0 + wid;
       float mv[2], lv[2];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
@@ -945,7 +1002,7 @@ struct Model {
       }
     }
     csync();
-    float4* gsum = reinterpret_cast<float4*>(c.act);  // [NG][NOUT4] (the combine area is free now)
+    float4* gsum = reinterpret_cast<float4*>(c.act);  // [NG][nout4] (the combine area is free now)
     if (sum_thread) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int c0 = grp;; c0 += NG * BATCH) {
@@ -966,21 +1023,20 @@ struct Model {
                             : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      gsum[grp * NOUT4 + o4] = acc;
+      gsum[grp * nout4 + o4] = acc;
     }
     csync();
-    if (tid < NOUT4) {
-      const int i = tid / (HD / 4), dd = tid % (HD / 4);
+    if (tid < nout4) {
+      const int i = h0 + tid / (HD / 4), dd = tid % (HD / 4);
       float4 o = gsum[tid];
       for (int gg = 1; gg < NG; ++gg) {
-        const float4 v = gsum[gg * NOUT4 + tid];
+        const float4 v = gsum[gg * nout4 + tid];
         o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w;
       }
       const size_t off = (size_t)(g * GQA + i) * HD + 4 * dd;
       *reinterpret_cast<float4*>(a.sc.attn + b * QD + off) = o;
       if (c.tr_attn) *reinterpret_cast<float4*>(c.tr_attn + ((size_t)l * n + b) * QD + off) = o;
     }
-    if (tid == 0) a.sc.merge_cnt[b * NKV + g] = 0;
   }
 
   // ---------------------------------------------------------------- P3
@@ -1023,9 +1079,11 @@ struct Model {
       float s = 0.f;
       for (int t = 0; t < c.nr; ++t)
         s = fmaf(F.hs[b][t] * slice_val(F.nslw, t), slice_val(rs + e * kMaxRowsPerBlock, t), s);
-      // every block adds its partial; after the grid barrier all blocks read
-      // the same totals (the order of the additions may differ run to run)
-      atomicAdd(a.sc.rlogit + b * E + e, s);
+      // every block adds its partial into one of kRlogitGroups copies (fewer
+      // atomics queue on one address); after the grid barrier every block
+      // sums the copies in a fixed order (the order of the additions within a
+      // copy may differ run to run)
+      atomicAdd(a.sc.rlogit + (c.bid % kRlogitGroups) * kMaxBatch * E + b * E + e, s);
     }
   }
 
@@ -1048,7 +1106,12 @@ struct Model {
     if (moe) {
       // partial logits into shared memory (F.dots is free between P3 and P5)
       float* lg = &F.dots[0][0];
-      for (int i = tid; i < n * E; i += kThreads) lg[i] = __ldcg(a.sc.rlogit + i);
+      for (int i = tid; i < n * E; i += kThreads) {
+        float v = 0.f;
+#pragma unroll
+        for (int gr = 0; gr < kRlogitGroups; ++gr) v += __ldcg(a.sc.rlogit + gr * kMaxBatch * E + i);
+        lg[i] = v;
+      }
       for (int i = tid; i < n * TOPK; i += kThreads) F.topk_id[i / TOPK][i % TOPK] = i % TOPK;  // valid ids
       if (tid == 0) F.n_ue = 0;
       csync();
@@ -1125,7 +1188,7 @@ struct Model {
       const float r = F.rnorm[b];
       if (c.tr_rl && c.bid == 0)
         for (int e = lane; e < E; e += 32)
-          c.tr_rl[((size_t)l * n + b) * E + e] = r * __ldcg(a.sc.rlogit + b * E + e);
+          c.tr_rl[((size_t)l * n + b) * E + e] = r * (&F.dots[0][0])[b * E + e];
       if (lane == 0) {
         // softmax over the selection = softmax over all experts renormalised
         const float top = r * F.topk_w[b][0];
@@ -1573,6 +1636,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     F.prod_k = 0;
     F.mma_flip = 0;
     F.route_gen = 0;
+    F.n_merge = 0;
     F.abort = 0;
     for (int s = 0; s < c.ns; ++s) {
       mbar_init(&F.full[s], 1);
@@ -1669,7 +1733,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
 
 template <class S, int WDT>
 static KernelInfo make() {
-  return {reinterpret_cast<const void*>(&step_kernel<S, WDT>), kSmemBytes};
+  return {reinterpret_cast<const void*>(&step_kernel<S, WDT>), kSmemBytes, Model<S, WDT>::TT};
 }
 
 KernelInfo get_kernel(int shape, int wdtype) {
@@ -1681,7 +1745,7 @@ KernelInfo get_kernel(int shape, int wdtype) {
     if (wdtype == MK_BF16) return make<ShapeTiny, WBF16>();
     if (wdtype == MK_F32) return make<ShapeTiny, WF32>();
   }
-  return {nullptr, 0};
+  return {nullptr, 0, 0};
 }
 
 }  // namespace mk

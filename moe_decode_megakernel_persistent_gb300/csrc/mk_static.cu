@@ -151,8 +151,9 @@ extern "C" MK_API int mk_decode_step_static(
   StepArgs a;
   std::memset(&a, 0, sizeof(a));
   host_carve_scratch(*d, grid, max_units, base + off_scratch, &a.sc);
-  host_attention_split(d->n_kv_heads, grid, positions_host, n, &a.chunk, &a.n_units);
+  host_attention_split(d->n_kv_heads, grid, kern.tile_tokens, positions_host, n, &a.chunk, &a.n_units);
   if (a.n_units > max_units) return host_fail(MK_ERR_INVALID_ARG, "attention split exceeds its buffer");
+  if (a.n_units > kMaxOwnUnits * grid) return host_fail(MK_ERR_INVALID_ARG, "more attention units than the grid can merge");
   for (int i = 0; i < n; ++i) {
     a.slot[i] = slots_host[i];
     a.pos[i] = positions_host[i];
