@@ -401,7 +401,7 @@ struct Gemv {
 __host__ __device__ constexpr int plain_stride(int K) { return K * 4 + 16; }
 
 template <int WDT, int K, bool NORM, int RG, bool PLAIN, class LD, class WT>
-__device__ __noinline__ void stage_rows(uint8_t* dst, int rows, LD ld, float eps, WT wt, float* red,
+__device__ __forceinline__ void stage_rows(uint8_t* dst, int rows, LD ld, float eps, WT wt, float* red,
                                            float* rscale) {
   using Gv = Gemv<WDT, K>;
   constexpr int NW = K / 8;                      // 8-value words per vector
@@ -540,18 +540,19 @@ __device__ __noinline__ void stage_rows(uint8_t* dst, int rows, LD ld, float eps
   }
 }
 
-// Staging entry: the plain fp32 rows of the tensor-core path (plain), or
-// the GEMV engine's staged form: one row per pass for a single row (fewest
-// registers); otherwise four rows per pass with a norm (one load round trip
-// and one norm reduction for four rows) and, without one, as many rows as fit
-// two words per thread.
-template <int WDT, int K, bool NORM, class LD, class WT>
-__device__ __forceinline__ void stage_block(uint8_t* dst, int rows, bool plain, LD ld, float eps, WT wt,
-                                            float* red, float* rscale) {
-  // without a norm, as many rows per pass as two words per thread cover
+// Staging entry.  MODE 2: the plain fp32 rows of the tensor-core path;
+// otherwise the GEMV engine's staged form, MODE 0 one row per pass (fewest
+// registers), MODE 1 several rows per pass: four with a norm (one load round
+// trip and one norm reduction for four rows), as many as two words per
+// thread cover without one.  The mode is a template argument so that a
+// staging function holds one variant and its registers are allocated for it
+// alone.
+template <int MODE, int WDT, int K, bool NORM, class LD, class WT>
+__device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, float eps, WT wt, float* red,
+                                            float* rscale) {
   constexpr int RGM = NORM ? 4 : ((2 * kThreads) / (K / 8) > 1 ? (2 * kThreads) / (K / 8) : 1);
-  if (plain) stage_rows<WDT, K, NORM, RGM, true>(dst, rows, ld, eps, wt, red, rscale);
-  else if (rows == 1) stage_rows<WDT, K, NORM, 1, false>(dst, rows, ld, eps, wt, red, rscale);
+  if constexpr (MODE == 2) stage_rows<WDT, K, NORM, RGM, true>(dst, rows, ld, eps, wt, red, rscale);
+  else if constexpr (MODE == 0) stage_rows<WDT, K, NORM, 1, false>(dst, rows, ld, eps, wt, red, rscale);
   else stage_rows<WDT, K, NORM, RGM, false>(dst, rows, ld, eps, wt, red, rscale);
 }
 

@@ -607,18 +607,24 @@ struct Model {
   // tasks.  A task is a RoPE pair of rows (i, i + HD/2) of one q, k or v head,
   // so the warp that forms a pair also rotates it and writes it: q to
   // scratch, k and v as bf16 into the page.
-  __device__ static __noinline__ void qkv(int l) {
+  // Staging runs in functions of its own, called from the layer loop where
+  // few values are live: a call from inside a phase would save and restore
+  // the phase's registers through local memory, which the small L1 left
+  // beside 227 KB of shared memory mostly misses.
+  template <int MODE>
+  __device__ static __noinline__ void qkv_stage(int l) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x;
     const LayerW& Lw = F.lw;
     const int n = c.n;
     if (l == 0 && c.bid == 0)
       for (int i = tid; i < a.n_upd; i += kThreads)
         a.block_table[a.upd[i].slot * a.max_pages_per_seq + a.upd[i].index] = a.upd[i].page;
     if (c.bid == 0 && l >= a.n_dense)  // router logits are accumulated in P3
-      for (int i = tid; i < kRlogitGroups * kMaxBatch * E; i += kThreads) a.sc.rlogit[i] = 0.f;
+      for (int i = tid; i < kRlogitGroups * n * E; i += kThreads)
+        a.sc.rlogit[(i / (n * E)) * kMaxBatch * E + i % (n * E)] = 0.f;
     if (l >= a.n_dense) fetch_router_slice(Lw);
     {
       const void* nw = Lw.attn_norm;
@@ -626,8 +632,8 @@ struct Model {
       const float* x = a.sc.x;
       const int* tok = F.tok;
       const bool first = l == 0;
-      stage_block<WDT, H, true>(
-          c.act, n, c.tc,
+      stage_block<MODE, WDT, H, true>(
+          c.act, n,
           [&](int r, int f4) -> float4 {
             return first ? ld_aux4<AUX>(embed, (size_t)tok[r] * (H / 4) + f4)
                          : __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4);
@@ -641,7 +647,12 @@ struct Model {
       }
     csync();
     MK_STAMP(c, l, 0, 0);
-
+  }
+  __device__ static __noinline__ void qkv(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int lane = threadIdx.x & 31;
     int p0, p1;
     qkv_range(c, p0, p1);
     struct {
@@ -691,6 +702,19 @@ struct Model {
     }
   }
 
+  // One K or V row slice of a ring stage (32-bit shared address).
+  __device__ static __forceinline__ void lds_kv(uint32_t addr, float (&f)[DPL]) {
+    if constexpr (DPL == 4) {
+      uint32_t x, y;
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(addr));
+      f[0] = bf16_to_f(x & 0xffff); f[1] = bf16_to_f(x >> 16);
+      f[2] = bf16_to_f(y & 0xffff); f[3] = bf16_to_f(y >> 16);
+    } else {
+      uint32_t x;
+      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(addr));
+      f[0] = bf16_to_f(x & 0xffff); f[1] = bf16_to_f(x >> 16);
+    }
+  }
   // K and V rows of TU positions into registers.
   template <bool GL>
   __device__ static __forceinline__ void ld_tokens(const uint16_t* const (&kp)[TU], const uint16_t* const (&vp)[TU],
@@ -823,21 +847,19 @@ struct Model {
       }
 #pragma unroll 1
       for (int tb = t0; tb < rt1; tb += TT, ++k) {
-        const uint8_t* st = ring_acquire<STAGE>(k);
+        // 32-bit shared addresses: K rows of the stage, then V rows
+        const uint32_t st = smem_u32(ring_acquire<STAGE>(k)) + lane * DPL * 2;
         const int nt = min(TT, rt1 - tb);
-        const uint16_t* kp[TU];
-        const uint16_t* vp[TU];
         bool ok[TU];
+        float kf[TU][DPL], vf[TU][DPL];
 #pragma unroll
         for (int i = 0; i < TU; ++i) {
           const int j = wid + kWarps * i;
           ok[i] = j < nt;
-          const int jj = ok[i] ? j : 0;
-          kp[i] = reinterpret_cast<const uint16_t*>(st + (size_t)jj * HD * 2) + lane * DPL;
-          vp[i] = reinterpret_cast<const uint16_t*>(st + (size_t)(TT + jj) * HD * 2) + lane * DPL;
+          const uint32_t ka = st + (uint32_t)(ok[i] ? j : 0) * HD * 2;
+          lds_kv(ka, kf[i]);
+          lds_kv(ka + TT * HD * 2, vf[i]);
         }
-        float kf[TU][DPL], vf[TU][DPL];
-        ld_tokens<false>(kp, vp, kf, vf);
         attend(kf, vf, ok, q, m, lsum, o, lane);
         ring_release(k);
       }
@@ -1044,21 +1066,26 @@ struct Model {
   // its partial router logits: the post-attention RMSNorm is one scalar per
   // row times w2, so logits = rsqrt(mean(h^2) + eps) * sum_blocks(partials);
   // the scalar is applied in P4.
+  template <int MODE>
+  __device__ static __noinline__ void oproj_stage(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    {
+      const float* at = a.sc.attn;
+      stage_block<MODE, WDT, QD, false>(
+          c.act, c.n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(at + r * QD) + f4); },
+          0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
+    }
+    csync();
+    MK_STAMP(c, l, 2, 0);
+  }
   __device__ static __noinline__ void oproj(int l) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31;
-    const LayerW& Lw = F.lw;
     const int n = c.n;
-    {
-      const float* at = a.sc.attn;
-      stage_block<WDT, QD, false>(
-          c.act, n, c.tc, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(at + r * QD) + f4); },
-          0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
-    }
-    csync();
-    MK_STAMP(c, l, 2, 0);
     struct {
       const StepArgs* a; Fixed* F; int r0, lane;
       __device__ __forceinline__ ActRange acts(int) const { return {nullptr, 0, a->n}; }
@@ -1099,8 +1126,7 @@ struct Model {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const LayerW& Lw = F.lw;
+    const int tid = threadIdx.x;
     const bool moe = l >= a.n_dense;
     const int n = c.n;
     if (moe) {
@@ -1174,16 +1200,28 @@ struct Model {
         F.route_gen = l + 1;
       }
     }
+  }
+  template <int MODE>
+  __device__ static __noinline__ void ffn_stage(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
     {
-      const void* nw = Lw.ffn_norm;
+      const void* nw = F.lw.ffn_norm;
       const float* hp = a.sc.h;
-      stage_block<WDT, H, true>(
-          c.act, n, c.tc && !moe, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(hp + r * H) + f4); },
+      stage_block<MODE, WDT, H, true>(
+          c.act, c.n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(hp + r * H) + f4); },
           a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, F.rnorm);
     }
     csync();
     MK_STAMP(c, l, 3, 0);
-    if (!moe) return;
+  }
+  // Softmax weights of the selection, once the norm factor is known.
+  __device__ static __forceinline__ void route_weights(int l) {
+    Fixed& F = fixed();
+    const Ctx& c = F.ctx;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int n = c.n;
     for (int b = wid; b < n; b += kWarps) {
       const float r = F.rnorm[b];
       if (c.tr_rl && c.bid == 0)
@@ -1219,6 +1257,7 @@ struct Model {
     const Ctx& c = F.ctx;
     const int lane = threadIdx.x & 31;
     if (l >= a.n_dense) {
+      route_weights(l);
       int u0, u1;
       gu_range(c, F.n_ue * FE, u0, u1);
       struct {
@@ -1256,70 +1295,83 @@ struct Model {
   // batch rows are staged in rounds, the full-width rows of the block are
   // streamed once per round.  Then the weighted sum over experts in slot
   // order and the residual.
+  // A round is the expert entries (MoE) or batch rows (dense) that fit the
+  // staging area; `u` is the round's first distinct expert / row.
   template <bool MOE>
-  __device__ static __noinline__ void down(int l) {
+  __device__ static __forceinline__ int down_next(int u) {
+    const Fixed& F = fixed();
+    if constexpr (MOE) return moe_round_end(F, u, F.ctx.act_bytes / moe_entry_bytes(F.ctx));
+    else return u + F.ctx.act_bytes / dense_entry_bytes(F.ctx);
+  }
+  template <bool MOE, int MODE>
+  __device__ static __noinline__ void down_stage(int l, int u) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int n = c.n, nr = c.nr;
+    const int ub = down_next<MOE>(u);
     if constexpr (MOE) {
-      const int cap = c.act_bytes / moe_entry_bytes(c);
-#pragma unroll 1
-      for (int ua = 0; ua < F.n_ue;) {
-        const int ub = moe_round_end(F, ua, cap);
-        const int e0 = F.ue_start[ua], ecnt = F.ue_start[ub - 1] + F.ue_len[ub - 1] - e0;
-        {
-          const float* act = a.sc.act;
-          const Fixed* Fp = &F;
-          stage_block<WDT, FE, false>(
-              c.act, ecnt, false,
-              [&](int r, int f4) -> float4 {
-                const int en = e0 + r;
-                const float* src = act + (Fp->ent_b[en] * TOPK + Fp->ent_j[en]) * FE;
-                return __ldcg(reinterpret_cast<const float4*>(src) + f4);
-              },
-              0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
-        }
-        csync();
-        MK_STAMP(c, l, 4, 0);
-        struct {
-          Fixed* F; int ua, nr, e0, lane;
-          __device__ __forceinline__ ActRange acts(int t) const {
-            const int ue = ua + t / nr;
-            return {nullptr, F->ue_start[ue] - e0, F->ue_len[ue]};
-          }
-          __device__ __forceinline__ void put(int t, int ai, int, float v0, float) const {
-            F->dots[e0 + ai][t % nr] = v0;
-          }
-        } task{&F, ua, nr, e0, lane};
-        run_gemv<FE, 1, T_DN, GE::ACT_REGS, true, false>((ub - ua) * nr, c.act, task);
-        ua = ub;
-      }
+      const int e0 = F.ue_start[u], ecnt = F.ue_start[ub - 1] + F.ue_len[ub - 1] - e0;
+      const float* act = a.sc.act;
+      const Fixed* Fp = &F;
+      stage_block<MODE, WDT, FE, false>(
+          c.act, ecnt,
+          [&](int r, int f4) -> float4 {
+            const int en = e0 + r;
+            const float* src = act + (Fp->ent_b[en] * TOPK + Fp->ent_j[en]) * FE;
+            return __ldcg(reinterpret_cast<const float4*>(src) + f4);
+          },
+          0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
     } else {
-      const int cap = c.act_bytes / dense_entry_bytes(c);
-#pragma unroll 1
-      for (int ba = 0; ba < n; ba += cap) {
-        const int cnt = min(cap, n - ba);
-        {
-          const float* dact = a.sc.dact;
-          stage_block<WDT, FD, false>(
-              c.act, cnt, c.tc,
-              [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(dact + (ba + r) * FD) + f4); },
-              0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
-        }
-        csync();
-        MK_STAMP(c, l, 4, 0);
-        struct {
-          Fixed* F; int ba, cnt, lane;
-          __device__ __forceinline__ ActRange acts(int) const { return {nullptr, 0, cnt}; }
-          __device__ __forceinline__ void put(int t, int ai, int, float v0, float) const {
-            F->dots[ba + ai][t] = v0;
-          }
-        } task{&F, ba, cnt, lane};
-        run_gemv<FD, 1, T_DD, false, false, true>(nr, c.act, task);
-      }
+      const int cnt = min(ub, c.n) - u;
+      const float* dact = a.sc.dact;
+      stage_block<MODE, WDT, FD, false>(
+          c.act, cnt,
+          [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(dact + (u + r) * FD) + f4); },
+          0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
     }
+    csync();
+    MK_STAMP(c, l, 4, 0);
+  }
+  template <bool MOE>
+  __device__ static __noinline__ void down_gemv(int l, int u) {
+    Fixed& F = fixed();
+    const Ctx& c = F.ctx;
+    const int lane = threadIdx.x & 31;
+    const int nr = c.nr;
+    const int ub = down_next<MOE>(u);
+    if constexpr (MOE) {
+      const int e0 = F.ue_start[u];
+      struct {
+        Fixed* F; int ua, nr, e0, lane;
+        __device__ __forceinline__ ActRange acts(int t) const {
+          const int ue = ua + t / nr;
+          return {nullptr, F->ue_start[ue] - e0, F->ue_len[ue]};
+        }
+        __device__ __forceinline__ void put(int t, int ai, int, float v0, float) const {
+          F->dots[e0 + ai][t % nr] = v0;
+        }
+      } task{&F, u, nr, e0, lane};
+      run_gemv<FE, 1, T_DN, GE::ACT_REGS, true, false>((ub - u) * nr, c.act, task);
+    } else {
+      const int cnt = min(ub, c.n) - u;
+      struct {
+        Fixed* F; int ba, cnt, lane;
+        __device__ __forceinline__ ActRange acts(int) const { return {nullptr, 0, cnt}; }
+        __device__ __forceinline__ void put(int t, int ai, int, float v0, float) const {
+          F->dots[ba + ai][t] = v0;
+        }
+      } task{&F, u, cnt, lane};
+      run_gemv<FD, 1, T_DD, false, false, true>(nr, c.act, task);
+    }
+  }
+  // The weighted sum over the experts in slot order, plus the residual.
+  template <bool MOE>
+  __device__ static __noinline__ void down_finish(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    const int tid = threadIdx.x;
+    const int n = c.n, nr = c.nr;
     for (int idx = tid; idx < n * nr; idx += kThreads) {
       const int b = idx / nr, rr = idx % nr;
       float s = 0.f;
@@ -1332,27 +1384,54 @@ struct Model {
       if (c.tr_x) c.tr_x[((size_t)l * n + b) * H + c.r0 + rr] = xv;
     }
   }
+  template <bool MOE>
+  __device__ static __forceinline__ void down(int l) {
+    const Fixed& F = fixed();
+    const int end = MOE ? F.n_ue : F.ctx.n;
+    // MoE rounds hold several entries (the experts of a row); dense rounds
+    // are batch rows
+    const int mode = MOE ? 1 : stage_mode(F.ctx, true);
+#pragma unroll 1
+    for (int u = 0; u < end; u = down_next<MOE>(u)) {
+      if (mode == 0) down_stage<MOE, 0>(l, u);
+      else if (mode == 1) down_stage<MOE, 1>(l, u);
+      else down_stage<MOE, 2>(l, u);
+      down_gemv<MOE>(l, u);
+    }
+    down_finish<MOE>(l);
+  }
+  // staging variant of a launch: plain rows for the tensor-core path, one
+  // row, or several
+  __device__ static __forceinline__ int stage_mode(const Ctx& c, bool tc_ok) {
+    return (c.tc && tc_ok) ? 2 : (c.n == 1 ? 0 : 1);
+  }
 
   // ---------------------------------------------------------------- lm_head
   // Final RMSNorm, this block's vocabulary rows, argmax per row of the batch
   // (ties -> lowest token id); the last block to finish reduces the blocks'
   // candidates in block order and writes the tokens.
+  template <int MODE>
+  __device__ static __noinline__ void lm_stage() {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const Ctx& c = F.ctx;
+    {
+      const void* nw = a.final_norm;
+      const float* x = a.sc.x + a.out_first * H;
+      stage_block<MODE, WDT, H, true>(
+          c.act + a.out_first * (MODE == 2 ? plain_stride(H) : GH::ACT_BYTES), c.n - a.out_first,
+          [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4); },
+          a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
+    }
+    if (threadIdx.x < kMaxBatch) F.best_key[threadIdx.x] = 0ull;
+    csync();
+  }
   __device__ static __noinline__ void lm_head() {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int n = c.n;
-    {
-      const void* nw = a.final_norm;
-      const float* x = a.sc.x + a.out_first * H;
-      stage_block<WDT, H, true>(
-          c.act + a.out_first * (c.tc ? plain_stride(H) : GH::ACT_BYTES), n - a.out_first, c.tc,
-          [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4); },
-          a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
-    }
-    if (tid < kMaxBatch) F.best_key[tid] = 0ull;
-    csync();
     int v0, v1;
     gu_range(c, a.vocab, v0, v1);
     struct {
@@ -1678,6 +1757,10 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     load_lw(0);
     csync();
     for (int l = 0; ok && l < a.n_layers; ++l) {
+      const int sm = M::stage_mode(c, true);
+      if (sm == 0) M::template qkv_stage<0>(l);
+      else if (sm == 1) M::template qkv_stage<1>(l);
+      else M::template qkv_stage<2>(l);
       M::qkv(l);
       MK_STAMP(c, l, 0, 1);
       if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
@@ -1686,12 +1769,20 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
       MK_STAMP(c, l, 1, 1);
       if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
       MK_STAMP(c, l, 1, 2);
+      if (sm == 0) M::template oproj_stage<0>(l);
+      else if (sm == 1) M::template oproj_stage<1>(l);
+      else M::template oproj_stage<2>(l);
       M::oproj(l);
       MK_STAMP(c, l, 2, 1);
       if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
       MK_STAMP(c, l, 2, 2);
       M::route(l);
-      csync();
+      {
+        const int fm = M::stage_mode(c, l < a.n_dense);
+        if (fm == 0) M::template ffn_stage<0>(l);
+        else if (fm == 1) M::template ffn_stage<1>(l);
+        else M::template ffn_stage<2>(l);
+      }
       if (l + 1 < a.n_layers) load_lw(l + 1);
       M::gateup(l);
       MK_STAMP(c, l, 3, 1);
@@ -1703,7 +1794,14 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
       if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
       MK_STAMP(c, l, 4, 2);
     }
-    if (ok && a.out_first < n) M::lm_head();
+    if (ok && a.out_first < n) {
+      // rows from out_first on: one row alone takes the one-row variant
+      const int lm = c.tc ? 2 : (n - a.out_first == 1 ? 0 : 1);
+      if (lm == 0) M::template lm_stage<0>();
+      else if (lm == 1) M::template lm_stage<1>();
+      else M::template lm_stage<2>();
+      M::lm_head();
+    }
     if (c.tm && tid == 0) c.tm[1 + 16 * a.n_layers] = globaltimer();
     csync();
     if (tid == 0 && !ok) F.abort = 1;
