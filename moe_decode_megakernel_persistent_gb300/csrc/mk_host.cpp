@@ -259,7 +259,7 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
   c->dbg_flags &= ~MK_DBG_SKIP_ARRIVAL;
   void* args[] = {&a};
   cudaError_t e = cudaLaunchCooperativeKernel(c->kern.fn, dim3(c->grid), dim3(kBlockThreads), args,
-                                              (size_t)c->kern.smem_bytes, st);
+                                              (size_t)launch_smem_bytes(c->kern, n), st);
   if (e != cudaSuccess) {
     rollback();
     return fail(MK_ERR_CUDA, std::string("cudaLaunchCooperativeKernel: ") + cudaGetErrorString(e));
@@ -411,6 +411,10 @@ MK_API int mk_create(const mk_model_desc* d, const mk_weights* w, mk_ctx** out) 
     return fail(MK_ERR_UNSUPPORTED, "too few SMs for the compiled per-block row budget");
   }
   e = cudaFuncSetAttribute(c->kern.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, c->kern.smem_bytes);
+  // prefer L1: each launch then gets the smallest shared-memory carve-out its
+  // dynamic size needs
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(c->kern.fn, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxL1);
   if (e != cudaSuccess) {
     delete c;
     return fail(MK_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));

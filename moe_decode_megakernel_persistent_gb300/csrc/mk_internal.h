@@ -22,6 +22,11 @@ constexpr int kMaxRowsPerBlock = 32; // hidden rows owned by one block (hidden /
 constexpr int kMaxOwnUnits = 4;     // attention units one block may take in a launch
 constexpr int kMaxChunks = 64;       // attention chunks per (row, kv head): one per lane-pair of a warp
 constexpr int kSmemBytes = 227 * 1024;  // dynamic shared memory per block (the sm_100 family maximum)
+// A launch of one row asks for less (its staging area and a ring of a few
+// stages), so that more of the SM's 256 KB of L1/shared storage stays L1 for
+// local memory and cached loads (the full size leaves 28 KB); 128 KB is the
+// most that the 132 KB carve-out holds.
+constexpr int kSmemSingleRow = 128 * 1024;
 
 // Linear-weight slots of a layer.
 enum Lin { WQ = 0, WK, WV, WO, GATE, UP, DOWN, EGATE, EUP, EDOWN, NLIN };
@@ -118,7 +123,9 @@ struct KernelInfo {
   const void* fn;
   int smem_bytes;
   int tile_tokens;  // cached positions per ring stage (attention chunks are multiples)
+  int smem_single;  // dynamic shared memory of a one-row launch
 };
+inline int launch_smem_bytes(const KernelInfo& k, int rows) { return rows == 1 ? k.smem_single : k.smem_bytes; }
 
 // Returns the kernel for (shape, wdtype) or fn == nullptr if not compiled.
 KernelInfo get_kernel(int shape, int wdtype);

@@ -256,6 +256,12 @@ struct Model {
   }
   static_assert(kActOffset + act_base_bytes(kMaxBatch, TC) + 2 * STAGE <= kSmemBytes,
                 "a full batch leaves at least two ring stages");
+  // dynamic shared memory of a one-row launch: the staging area and four
+  // ring stages, at least kSmemSingleRow (what one L1/shared carve-out step
+  // holds), at most the full size
+  static constexpr int SMEM1 =
+      cmax(kSmemSingleRow, (kActOffset + act_base_bytes(1, false) + TOPK * GE::ACT_BYTES + 4 * STAGE + 1023) / 1024 * 1024);
+  static constexpr int SMEM_SINGLE = SMEM1 < kSmemBytes ? SMEM1 : kSmemBytes;
 
   __device__ static __forceinline__ void unit_of(const StepArgs& a, const int* unit_start, int u, int n,
                                                  int& b, int& g, int& ci, int& nch) {
@@ -1689,7 +1695,10 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     c.r0 = r0 * M::A_H;
     c.nr = (r1 - r0) * M::A_H;
     // staging area, then the ring in what is left
-    const int avail = kSmemBytes - kActOffset;
+    // the launch's dynamic shared memory (less for one row: more L1)
+    uint32_t dsz;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dsz));
+    const int avail = (int)dsz - kActOffset;
     c.tc = M::TC && n >= 2;
     int act = M::act_base_bytes(n, c.tc);
     const int want = n * S::TOPK * M::moe_entry_bytes(c);
@@ -1831,7 +1840,8 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
 
 template <class S, int WDT>
 static KernelInfo make() {
-  return {reinterpret_cast<const void*>(&step_kernel<S, WDT>), kSmemBytes, Model<S, WDT>::TT};
+  return {reinterpret_cast<const void*>(&step_kernel<S, WDT>), kSmemBytes, Model<S, WDT>::TT,
+          Model<S, WDT>::SMEM_SINGLE};
 }
 
 KernelInfo get_kernel(int shape, int wdtype) {

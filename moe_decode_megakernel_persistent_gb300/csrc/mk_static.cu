@@ -146,6 +146,8 @@ extern "C" MK_API int mk_decode_step_static(
   char* base = nullptr;
   if (int r = setup(dev, *d, &base)) return r;
   e = cudaFuncSetAttribute(kern.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kern.smem_bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern.fn, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxL1);
   if (e != cudaSuccess) return host_fail(MK_ERR_CUDA, cudaGetErrorString(e));
 
   StepArgs a;
@@ -193,7 +195,8 @@ extern "C" MK_API int mk_decode_step_static(
     e = cudaMemcpyAsync(base + off_layers, layers, sizeof(LayerW) * d->n_layers, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return host_fail(MK_ERR_CUDA, cudaGetErrorString(e));
   void* args[] = {&a};
-  e = cudaLaunchCooperativeKernel(kern.fn, dim3(grid), dim3(kBlockThreads), args, (size_t)kern.smem_bytes, st);
+  e = cudaLaunchCooperativeKernel(kern.fn, dim3(grid), dim3(kBlockThreads), args,
+                                  (size_t)launch_smem_bytes(kern, n), st);
   if (e != cudaSuccess)
     return host_fail(MK_ERR_CUDA, (std::string("cudaLaunchCooperativeKernel: ") + cudaGetErrorString(e)).c_str());
   if (status_dev) {
