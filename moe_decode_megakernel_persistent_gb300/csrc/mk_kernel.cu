@@ -237,12 +237,31 @@ struct Model {
   static constexpr int TU = STAGE / (4 * HD) / kWarps;  // positions per warp per stage
   static constexpr int TT = TU * kWarps;              // cached positions per stage (K and V rows, bf16)
   static_assert(TU >= 1, "a stage holds a position per warp");
+  // attention: tiles of TT positions, MTS m-tiles of 16
+  static constexpr int MTS = (TT + 15) / 16;  // position m-tiles of a tile (score warps) = PV k-steps
+  static constexpr int TTP = MTS * 16;        // padded positions of a tile
+  static constexpr int NDT = HD / 16;         // dim m-tiles (value warps)
+  static constexpr int KST = HD / 16;         // score k-steps
+  static constexpr int W_SC = NDT;            // first score warp
+  static constexpr int W_SM = kWarps - GQA;   // first softmax warp
+  static_assert(GQA <= 8 && HD % 16 == 0, "one n-tile of heads, whole k-steps");
+  static_assert(NDT + MTS <= kWarps && GQA <= kWarps, "warp roles");
+  // attention scratch in the staging area (byte offsets)
+  static constexpr int AO_QS = 0;                                 // float [GQA][HD] scaled queries
+  static constexpr int AO_QF = AO_QS + GQA * HD * 4;              // uint4 [KST][32] q fragments (hi b0 b1, lo b0 b1)
+  static constexpr int AO_SC = AO_QF + KST * 32 * 16;             // float [TTP][8] scores
+  static constexpr int AO_PB = AO_SC + TTP * 8 * 4;               // bf16 [2][8][TTP] P hi, lo
+  static constexpr int AO_ML = AO_PB + 2 * 8 * TTP * 2;           // float [3][8] m, l, corr
+  static constexpr int AO_NT = (AO_ML + 3 * 8 * 4 + 127) / 128 * 128;  // bf16 [2][TT][HD] new-position tile
+  // (the value warps read V rows up to TTP - 1: the padding rows stay inside)
+  static constexpr int ATT_SMEM = AO_NT + (TT + TTP) * HD * 2;
+  static constexpr int SPL = (TTP + 31) / 32;  // positions per softmax lane
+  static_assert(STAGE >= (TT + TTP) * HD * 2, "padding rows of a ring tile stay inside the stage");
   static_assert(H % A_H == 0, "aligned row groups");
   static_assert(TOPK <= 8 && E <= 64, "router tables");
 
   static constexpr int NQP = NH * HALF, NKP = NKV * HALF, NP = NQP + 2 * NKP;
   static constexpr int PR = HD + 4;  // partial row: m, l, pad, pad, o[HD] (16-byte rows)
-  static constexpr int ATT_BYTES = (kWarps * GQA * (HD + 2) + GQA * HD) * 4;
 
   // Staging area for n rows: every phase's activations fit; the MoE down
   // entries take what is left above 3 ring stages (rounds if they do not fit).
@@ -252,7 +271,7 @@ struct Model {
   __host__ __device__ static constexpr int act_base_bytes(int n, bool tc) {
     return cmax(tc ? cmax(cmax(n * plain_stride(H), n * plain_stride(QD)), plain_stride(FD)) : 0,
                 cmax(cmax(n * GH::ACT_BYTES, n * GQ::ACT_BYTES),
-                     cmax(cmax(ATT_BYTES, GD::ACT_BYTES), n * GE::ACT_BYTES)));
+                     cmax(cmax(ATT_SMEM, GD::ACT_BYTES), n * GE::ACT_BYTES)));
   }
   static_assert(kActOffset + act_base_bytes(kMaxBatch, TC) + 2 * STAGE <= kSmemBytes,
                 "a full batch leaves at least two ring stages");
@@ -693,109 +712,147 @@ struct Model {
     run_gemv<H, 2, T_QKV, false, false, true>(p1 - p0, c.act, task);
   }
 
-  // K/V rows of TU positions into registers (bf16 -> float), from shared
-  // memory (ring) or, for positions this launch wrote, from global memory at
-  // L2 (written by other blocks before the grid barrier).
-  template <bool GL>
-  __device__ static __forceinline__ void ld_kv(const uint16_t* p, float (&f)[DPL]) {
-    if constexpr (DPL == 4) {
-      const uint2 r = GL ? __ldcg(reinterpret_cast<const uint2*>(p)) : lds64(p);
-      f[0] = bf16_to_f(r.x & 0xffff); f[1] = bf16_to_f(r.x >> 16);
-      f[2] = bf16_to_f(r.y & 0xffff); f[3] = bf16_to_f(r.y >> 16);
-    } else {
-      const uint32_t r = GL ? __ldcg(reinterpret_cast<const unsigned int*>(p)) : lds32(p);
-      f[0] = bf16_to_f(r & 0xffff); f[1] = bf16_to_f(r >> 16);
-    }
-  }
-
-  // One K or V row slice of a ring stage (32-bit shared address).
-  __device__ static __forceinline__ void lds_kv(uint32_t addr, float (&f)[DPL]) {
-    if constexpr (DPL == 4) {
-      uint32_t x, y;
-      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(addr));
-      f[0] = bf16_to_f(x & 0xffff); f[1] = bf16_to_f(x >> 16);
-      f[2] = bf16_to_f(y & 0xffff); f[3] = bf16_to_f(y >> 16);
-    } else {
-      uint32_t x;
-      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(addr));
-      f[0] = bf16_to_f(x & 0xffff); f[1] = bf16_to_f(x >> 16);
-    }
-  }
-  // K and V rows of TU positions into registers.
-  template <bool GL>
-  __device__ static __forceinline__ void ld_tokens(const uint16_t* const (&kp)[TU], const uint16_t* const (&vp)[TU],
-                                                   float (&kf)[TU][DPL], float (&vf)[TU][DPL]) {
-#pragma unroll
-    for (int k = 0; k < TU; ++k) {
-      ld_kv<GL>(kp[k], kf[k]);
-      ld_kv<GL>(vp[k], vf[k]);
-    }
-  }
-  // One online-softmax update of a warp's GQA heads with TU positions
-  // (`ok` false for padding positions).
-  __device__ static __forceinline__ void attend(const float (&kf)[TU][DPL], const float (&vf)[TU][DPL],
-                                                const bool (&ok)[TU], const float (&q)[GQA][DPL], float (&m)[GQA],
-                                                float (&lsum)[GQA], float (&o)[GQA][DPL], int lane) {
-    // scores of the TU positions for the GQA heads: lane partials, one
-    // transposing reduction for all of them, then broadcast back
-    constexpr int NV = TU * GQA;
-    constexpr int NB = NV == 32 ? 5 : NV == 16 ? 4 : NV == 8 ? 3 : NV == 4 ? 2 : NV == 2 ? 1 : 0;
-    static_assert((1 << NB) == NV, "TU * GQA is a power of two <= 32");
-    float sv[NV];
-#pragma unroll
-    for (int k = 0; k < TU; ++k)
-#pragma unroll
-      for (int i = 0; i < GQA; ++i) {
-        float acc = 0.f;
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) acc = fmaf(q[i][d], kf[k][d], acc);
-        sv[k * GQA + i] = acc;
-      }
-    const float mine = warp_reduce_scatter<NV>(sv, lane);
-    float sc[TU][GQA];
-#pragma unroll
-    for (int idx = 0; idx < NV; ++idx) sc[idx / GQA][idx % GQA] = __shfl_sync(0xffffffffu, mine, bitrev<NB>(idx));
-#pragma unroll
-    for (int i = 0; i < GQA; ++i) {
-      float mn = m[i];
-#pragma unroll
-      for (int k = 0; k < TU; ++k) mn = ok[k] ? fmaxf(mn, sc[k][i]) : mn;
-      const float corr = mn == -INFINITY ? 1.f : __expf(m[i] - mn);
-      float psum = 0.f, p[TU];
-#pragma unroll
-      for (int k = 0; k < TU; ++k) {
-        p[k] = ok[k] ? __expf(sc[k][i] - mn) : 0.f;
-        psum += p[k];
-      }
-      lsum[i] = fmaf(lsum[i], corr, psum);
-#pragma unroll
-      for (int d = 0; d < DPL; ++d) {
-        float acc = o[i][d] * corr;
-#pragma unroll
-        for (int k = 0; k < TU; ++k) acc = fmaf(p[k], vf[k][d], acc);
-        o[i][d] = acc;
-      }
-      m[i] = mn;
-    }
-  }
-
   // ---------------------------------------------------------------- P2
   // Split attention over the paged cache.  Unit = (row, kv head, chunk of
   // positions).  Cached positions arrive through the ring, TT per stage (K
-  // rows, then V rows); warp w takes positions w, w + 15, ... of a stage and
-  // keeps a running max, sum and weighted value (online softmax) for the GQA
-  // heads of the kv head.  Positions this launch wrote are read from global
-  // memory.  The warps are combined and the unit's partial (m, l, o) written;
-  // the last unit of a (row, kv head) to finish merges all its chunks in
-  // chunk order (log-sum-exp).
+  // rows, then V rows, bf16); positions this launch wrote are copied from
+  // global memory into a tile of the same layout.  The whole block works on
+  // one tile at a time with mma.sync m16n8k16 (bf16 in, fp32 accumulate):
+  //   scores  S^T = K q^T     (m = 16 positions, n = the GQA heads, k = 16
+  //           dims), by the score warps, one m-tile each; q is split into
+  //           bf16 hi + lo (16 significant bits; K is bf16 exactly);
+  //   softmax one warp per head: running max m, sum l, correction factor
+  //           exp(m_old - m_new) and P = exp(S - m_new), split hi + lo;
+  //   values  O^T = O^T corr + V^T P^T (m = 16 dims, n = heads, k = 16
+  //           positions), by the value warps, one m-tile of dims each, the
+  //           accumulators kept in registers across the unit's tiles.
+  // Padding positions of a tile get P = 0 and their V operand is zeroed.
+  // The unit's partial (m, l, o) is written straight from those registers;
+  // the last units of a (row, kv head) merge all its chunks in chunk order
+  // (log-sum-exp).
+
+  __device__ static __forceinline__ void split2(float x0, float x1, uint32_t& h, uint32_t& l) {
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(x1), "f"(x0));
+    const float r0 = x0 - __uint_as_float(h << 16), r1 = x1 - __uint_as_float(h & 0xFFFF0000u);
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(l) : "f"(r1), "f"(r0));
+  }
+  __device__ static __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                 uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+  }
+  __device__ static __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                   uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+  }
+
+  // One tile of nt positions (K rows at kv, V rows at kv + TT * HD * 2,
+  // 32-bit shared addresses): scores, softmax, values.  `o` is the value
+  // warps' accumulator (rows g, g + 8 = dims, columns 2q, 2q + 1 = heads).
+  __device__ static __forceinline__ void att_tile(uint32_t kv, int nt, uint8_t* att, float (&o)[4]) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, q = lane & 3;
+    float* sc = reinterpret_cast<float*>(att + AO_SC);
+    uint16_t* pb = reinterpret_cast<uint16_t*>(att + AO_PB);
+    float* ml = reinterpret_cast<float*>(att + AO_ML);
+    if (wid >= W_SC && wid < W_SC + MTS) {
+      // S^T rows 16 mt .. 16 mt + 15 (positions), all heads
+      const int mt = wid - W_SC;
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint4* qf = reinterpret_cast<const uint4*>(att + AO_QF);
+      // ldmatrix rows: lanes 0-7 / 8-15 positions 0-7 / 8-15 at dims +0,
+      // lanes 16-31 the same positions at dims +8
+      const uint32_t ra = kv + (uint32_t)(16 * mt + (lane & 15)) * HD * 2 + (uint32_t)(lane >> 4) * 16;
+#pragma unroll
+      for (int ks = 0; ks < KST; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(ra + ks * 32, a0, a1, a2, a3);
+        const uint4 b = qf[ks * 32 + lane];
+        mma16816(s, a0, a1, a2, a3, b.x, b.y);
+        mma16816(s, a0, a1, a2, a3, b.z, b.w);
+      }
+      const int p0 = 16 * mt + g;
+      sc[p0 * 8 + 2 * q] = s[0];
+      sc[p0 * 8 + 2 * q + 1] = s[1];
+      sc[(p0 + 8) * 8 + 2 * q] = s[2];
+      sc[(p0 + 8) * 8 + 2 * q + 1] = s[3];
+    }
+    csync();
+    if (wid >= W_SM) {
+      // head i: positions lane + 32 j
+      const int i = wid - W_SM;
+      float v[SPL];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < SPL; ++j) {
+        const int p = lane + 32 * j;
+        v[j] = p < nt ? sc[p * 8 + i] : -INFINITY;
+        mx = fmaxf(mx, v[j]);
+      }
+      const float mold = ml[i];
+      const float mn = fmaxf(mold, warp_max(mx));
+      const float corr = mold == -INFINITY ? 0.f : __expf(mold - mn);
+      float ps = 0.f;
+#pragma unroll
+      for (int j = 0; j < SPL; ++j) {
+        const int p = lane + 32 * j;
+        const float e = p < nt ? __expf(v[j] - mn) : 0.f;
+        ps += e;
+        // P = hi + lo, two bf16
+        const __nv_bfloat16 h = __float2bfloat16_rn(e);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(e - __bfloat162float(h));
+        if (p < TTP) {
+          pb[i * TTP + p] = __bfloat16_as_ushort(h);
+          pb[8 * TTP + i * TTP + p] = __bfloat16_as_ushort(lo);
+        }
+      }
+      ps = warp_sum(ps);
+      if (lane == 0) {
+        ml[i] = mn;
+        ml[8 + i] = ml[8 + i] * corr + ps;
+        ml[16 + i] = corr;
+      }
+    }
+    csync();
+    if (wid < NDT) {
+      const float c0 = ml[16 + 2 * q], c1 = ml[16 + 2 * q + 1];  // heads >= GQA: 0 (never used)
+      o[0] *= c0; o[1] *= c1; o[2] *= c0; o[3] *= c1;
+      // V^T via transposed ldmatrix: matrices (dims +0, positions +0),
+      // (dims +8, +0), (dims +0, +8), (dims +8, +8)
+      const int mi = lane >> 3;
+      const uint32_t ra = kv + (uint32_t)TT * HD * 2 +
+                          (uint32_t)((mi >> 1) * 8 + (lane & 7)) * HD * 2 + (uint32_t)(16 * wid + (mi & 1) * 8) * 2;
+      const uint32_t* pw = reinterpret_cast<const uint32_t*>(pb);
+#pragma unroll
+      for (int kt = 0; kt < MTS; ++kt) {
+        uint32_t a0, a1, a2, a3;
+        // rows past the tile's TT positions are never read: clamp the
+        // address (their P is 0 and the operand is zeroed below)
+        ldsm_x4_t(ra + (uint32_t)kt * 16 * HD * 2, a0, a1, a2, a3);
+        const int pa = 16 * kt + 2 * q, pbp = pa + 8;
+        if (pa >= nt) { a0 = 0u; a1 = 0u; } else if (pa + 1 >= nt) { a0 &= 0xFFFFu; a1 &= 0xFFFFu; }
+        if (pbp >= nt) { a2 = 0u; a3 = 0u; } else if (pbp + 1 >= nt) { a2 &= 0xFFFFu; a3 &= 0xFFFFu; }
+        const uint32_t bh0 = pw[(g * TTP + pa) >> 1], bh1 = pw[(g * TTP + pbp) >> 1];
+        const uint32_t bl0 = pw[(8 * TTP + g * TTP + pa) >> 1], bl1 = pw[(8 * TTP + g * TTP + pbp) >> 1];
+        mma16816(o, a0, a1, a2, a3, bh0, bh1);
+        mma16816(o, a0, a1, a2, a3, bl0, bl1);
+      }
+    }
+  }
+
   __device__ static __noinline__ void attention(int l) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int n = c.n;
-    float* comb = reinterpret_cast<float*>(c.act);  // [warp][GQA][HD + 2]
-    float* qs = comb + kWarps * GQA * (HD + 2);     // [GQA][HD] this unit's queries
+    uint8_t* att = c.act;
+    float* qs = reinterpret_cast<float*>(att + AO_QS);
+    float* ml = reinterpret_cast<float*>(att + AO_ML);
+    uint16_t* pb = reinterpret_cast<uint16_t*>(att + AO_PB);
+    const uint32_t nt_base = smem_u32(att + AO_NT);
     const float qscale = rsqrtf((float)HD);
     uint32_t k = F.kc;
 #pragma unroll 1
@@ -804,33 +861,52 @@ struct Model {
       unit_of(a, F.unit_start, u, n, b, g, ci, nch);
       int t0, rt1, t1;
       unit_span(a, b, ci, t0, rt1, t1);
-      // this unit's queries into shared memory once (coalesced), not per warp
-      for (int v = tid; v < GQA * HD / 4; v += kThreads)
-        reinterpret_cast<float4*>(qs)[v] =
-            __ldcg(reinterpret_cast<const float4*>(a.sc.q + b * QD + g * GQA * HD) + v);
-      csync();
-      float q[GQA][DPL];
-#pragma unroll
-      for (int i = 0; i < GQA; ++i)
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) q[i][d] = qs[i * HD + lane * DPL + d] * qscale;
-      float m[GQA], lsum[GQA], o[GQA][DPL];
-#pragma unroll
-      for (int i = 0; i < GQA; ++i) {
-        m[i] = -INFINITY;
-        lsum[i] = 0.f;
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) o[i][d] = 0.f;
+      // this unit's queries (scaled), the softmax state, P of the padding
+      // heads (never written by the softmax warps) zero
+      for (int v = tid; v < GQA * HD / 4; v += kThreads) {
+        float4 x = __ldcg(reinterpret_cast<const float4*>(a.sc.q + b * QD + g * GQA * HD) + v);
+        x.x *= qscale; x.y *= qscale; x.z *= qscale; x.w *= qscale;
+        reinterpret_cast<float4*>(qs)[v] = x;
       }
-      // positions this launch wrote (global memory): the first batch is
-      // requested now, so its latency overlaps the ring tiles
-      auto new_tokens = [&](int tb, const uint16_t* (&kp)[TU], const uint16_t* (&vp)[TU], bool (&ok)[TU]) {
-#pragma unroll
-        for (int i = 0; i < TU; ++i) {
-          const int t = tb + wid + kWarps * i;
-          ok[i] = t < t1;
-          const int tt = ok[i] ? t : rt1;
-          const int pi = tt / kPageTokens;
+      if (tid < 8) {
+        ml[tid] = -INFINITY;
+        ml[8 + tid] = 0.f;
+        ml[16 + tid] = 0.f;
+      }
+      for (int v = tid; v < 2 * (8 - GQA) * TTP; v += kThreads) {
+        const int hl = v / ((8 - GQA) * TTP), r = v % ((8 - GQA) * TTP);
+        pb[hl * 8 * TTP + GQA * TTP + r] = 0;
+      }
+      csync();
+      // B fragments of q^T for the score warps: thread (g, q) of k-step ks
+      // holds head g, dims 16 ks + 2q, +1 (b0) and + 8 (b1), hi then lo
+      for (int v = tid; v < KST * 32; v += kThreads) {
+        const int ks = v >> 5, ln = v & 31, hg = ln >> 2, qq = ln & 3;
+        uint4 f = make_uint4(0u, 0u, 0u, 0u);
+        if (hg < GQA) {
+          const float* qr = qs + hg * HD + 16 * ks + 2 * qq;
+          split2(qr[0], qr[1], f.x, f.z);
+          split2(qr[8], qr[9], f.y, f.w);
+        }
+        reinterpret_cast<uint4*>(att + AO_QF)[v] = f;
+      }
+      csync();
+      float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int tb = t0; tb < rt1; tb += TT, ++k) {
+        const uint32_t st = smem_u32(ring_acquire<STAGE>(k));
+        att_tile(st, min(TT, rt1 - tb), att, o);
+        ring_release(k);
+      }
+      // positions this launch wrote (at L2, written before the grid barrier)
+#pragma unroll 1
+      for (int tb = rt1; tb < t1; tb += TT) {
+        const int nt = min(TT, t1 - tb);
+        csync();  // the previous tile's readers are done with the new-position tile
+        constexpr int RW = HD * 2 / 16;  // 16-byte words per row
+        for (int v = tid; v < 2 * nt * RW; v += kThreads) {
+          const int kvh = v / (nt * RW), r = (v / RW) % nt, w = v % RW;
+          const int t = tb + r, pi = t / kPageTokens;
           int page = pi == a.pos[b] / kPageTokens
                          ? a.cur_page[b]
                          : (pi < a.max_pages_per_seq ? __ldcg(a.block_table + a.slot[b] * a.max_pages_per_seq + pi)
@@ -839,83 +915,30 @@ struct Model {
             set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_PAGE, pi);
             page = 0;
           }
-          kp[i] = a.kv + Kv<S>::offset(l, a.n_pages, page, 0, g, tt % kPageTokens) + lane * DPL;
-          vp[i] = a.kv + Kv<S>::offset(l, a.n_pages, page, 1, g, tt % kPageTokens) + lane * DPL;
+          const uint4 x =
+              __ldcg(reinterpret_cast<const uint4*>(a.kv + Kv<S>::offset(l, a.n_pages, page, kvh, g, t % kPageTokens)) + w);
+          reinterpret_cast<uint4*>(att + AO_NT)[(kvh * TT + r) * RW + w] = x;
         }
-      };
-      float nkf[TU][DPL], nvf[TU][DPL];
-      bool nok[TU];
-      if (rt1 < t1) {
-        const uint16_t* kp[TU];
-        const uint16_t* vp[TU];
-        new_tokens(rt1, kp, vp, nok);
-        ld_tokens<true>(kp, vp, nkf, nvf);
-      }
-#pragma unroll 1
-      for (int tb = t0; tb < rt1; tb += TT, ++k) {
-        // 32-bit shared addresses: K rows of the stage, then V rows
-        const uint32_t st = smem_u32(ring_acquire<STAGE>(k)) + lane * DPL * 2;
-        const int nt = min(TT, rt1 - tb);
-        bool ok[TU];
-        float kf[TU][DPL], vf[TU][DPL];
-#pragma unroll
-        for (int i = 0; i < TU; ++i) {
-          const int j = wid + kWarps * i;
-          ok[i] = j < nt;
-          const uint32_t ka = st + (uint32_t)(ok[i] ? j : 0) * HD * 2;
-          lds_kv(ka, kf[i]);
-          lds_kv(ka + TT * HD * 2, vf[i]);
-        }
-        attend(kf, vf, ok, q, m, lsum, o, lane);
-        ring_release(k);
-      }
-      if (rt1 < t1) attend(nkf, nvf, nok, q, m, lsum, o, lane);
-#pragma unroll 1
-      for (int tb = rt1 + kWarps * TU; tb < t1; tb += kWarps * TU) {
-        const uint16_t* kp[TU];
-        const uint16_t* vp[TU];
-        bool ok[TU];
-        new_tokens(tb, kp, vp, ok);
-        float kf[TU][DPL], vf[TU][DPL];
-        ld_tokens<true>(kp, vp, kf, vf);
-        attend(kf, vf, ok, q, m, lsum, o, lane);
-      }
-#pragma unroll
-      for (int i = 0; i < GQA; ++i) {
-        float* cw = comb + (wid * GQA + i) * (HD + 2);
-        if (lane == 0) { cw[0] = m[i]; cw[1] = lsum[i]; }
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) cw[2 + lane * DPL + d] = o[i][d];
+        csync();
+        att_tile(nt_base, nt, att, o);
       }
       csync();
       if (u >= a.max_units) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, u);
       float* pu = a.sc.part + (size_t)min(u, a.max_units - 1) * GQA * PR;
-      // factors exp(m_w - M) once per (warp, head), then a weighted sum per dim
-      float* fac = F.red;                 // [kWarps][GQA], then M[GQA]
-      float* Ms = F.red + kWarps * GQA;
-      if (tid < GQA) {
-        float M = -INFINITY;
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, comb[(w * GQA + tid) * (HD + 2)]);
-        Ms[tid] = M;
-      }
-      csync();
-      if (tid < kWarps * GQA) {
-        const int w = tid / GQA, i = tid % GQA;
-        const float mw = comb[(w * GQA + i) * (HD + 2)];
-        fac[tid] = mw == -INFINITY ? 0.f : __expf(mw - Ms[i]);
-      }
-      csync();
-      for (int idx = tid; idx < GQA * HD; idx += kThreads) {
-        const int i = idx / HD, d = idx % HD;
-        float L = 0.f, O = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float* cw = comb + (w * GQA + i) * (HD + 2);
-          L = fmaf(cw[1], fac[w * GQA + i], L);
-          O = fmaf(cw[2 + d], fac[w * GQA + i], O);
+      if (wid < NDT) {
+        const int gg = lane >> 2, qq = lane & 3, d0 = 16 * wid + gg;
+        if (2 * qq < GQA) {
+          pu[(2 * qq) * PR + 4 + d0] = o[0];
+          pu[(2 * qq) * PR + 4 + d0 + 8] = o[2];
         }
-        if (d == 0) { pu[i * PR] = Ms[i]; pu[i * PR + 1] = L; }
-        pu[i * PR + 4 + d] = O;
+        if (2 * qq + 1 < GQA) {
+          pu[(2 * qq + 1) * PR + 4 + d0] = o[1];
+          pu[(2 * qq + 1) * PR + 4 + d0 + 8] = o[3];
+        }
+      }
+      if (tid < GQA) {
+        pu[tid * PR] = ml[tid];
+        pu[tid * PR + 1] = ml[8 + tid];
       }
       csync();
       // release this unit's partial; the last MG units of (b, g) to arrive
