@@ -891,18 +891,10 @@ struct Model {
         reinterpret_cast<uint4*>(att + AO_QF)[v] = f;
       }
       csync();
-      float o[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int tb = t0; tb < rt1; tb += TT, ++k) {
-        const uint32_t st = smem_u32(ring_acquire<STAGE>(k));
-        att_tile(st, min(TT, rt1 - tb), att, o);
-        ring_release(k);
-      }
       // positions this launch wrote (at L2, written before the grid barrier)
-#pragma unroll 1
-      for (int tb = rt1; tb < t1; tb += TT) {
-        const int nt = min(TT, t1 - tb);
-        csync();  // the previous tile's readers are done with the new-position tile
+      // are copied into the new-position tile with cp.async; the first such
+      // tile is requested now and lands while the ring tiles are processed
+      auto stage_new = [&](int tb, int nt) {
         constexpr int RW = HD * 2 / 16;  // 16-byte words per row
         for (int v = tid; v < 2 * nt * RW; v += kThreads) {
           const int kvh = v / (nt * RW), r = (v / RW) % nt, w = v % RW;
@@ -915,10 +907,30 @@ struct Model {
             set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_PAGE, pi);
             page = 0;
           }
-          const uint4 x =
-              __ldcg(reinterpret_cast<const uint4*>(a.kv + Kv<S>::offset(l, a.n_pages, page, kvh, g, t % kPageTokens)) + w);
-          reinterpret_cast<uint4*>(att + AO_NT)[(kvh * TT + r) * RW + w] = x;
+          const uint4* src =
+              reinterpret_cast<const uint4*>(a.kv + Kv<S>::offset(l, a.n_pages, page, kvh, g, t % kPageTokens)) + w;
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(nt_base + (uint32_t)((kvh * TT + r) * RW + w) * 16),
+                       "l"(src)
+                       : "memory");
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      };
+      if (rt1 < t1) stage_new(rt1, min(TT, t1 - rt1));
+      float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int tb = t0; tb < rt1; tb += TT, ++k) {
+        const uint32_t st = smem_u32(ring_acquire<STAGE>(k));
+        att_tile(st, min(TT, rt1 - tb), att, o);
+        ring_release(k);
+      }
+#pragma unroll 1
+      for (int tb = rt1; tb < t1; tb += TT) {
+        const int nt = min(TT, t1 - tb);
+        if (tb != rt1) {
+          csync();  // the previous tile's readers are done with the new-position tile
+          stage_new(tb, nt);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
         csync();
         att_tile(nt_base, nt, att, o);
       }
