@@ -275,11 +275,13 @@ struct Model {
   }
   static_assert(kActOffset + act_base_bytes(kMaxBatch, TC) + 2 * STAGE <= kSmemBytes,
                 "a full batch leaves at least two ring stages");
-  // dynamic shared memory of a one-row launch: the staging area and four
-  // ring stages, at least kSmemSingleRow (what one L1/shared carve-out step
-  // holds), at most the full size
+  // dynamic shared memory of a one-row launch: the staging area and three
+  // ring stages, at least kSmemSingleRow (the most that the 132 KB
+  // L1/shared carve-out holds), at most the full size
   static constexpr int SMEM1 =
-      cmax(kSmemSingleRow, (kActOffset + act_base_bytes(1, false) + TOPK * GE::ACT_BYTES + 4 * STAGE + 1023) / 1024 * 1024);
+      cmax(kSmemSingleRow,
+           (kActOffset + (cmax(act_base_bytes(1, false), TOPK * GE::ACT_BYTES) + 127) / 128 * 128 + 3 * STAGE + 1023) /
+               1024 * 1024);
   static constexpr int SMEM_SINGLE = SMEM1 < kSmemBytes ? SMEM1 : kSmemBytes;
 
   __device__ static __forceinline__ void unit_of(const StepArgs& a, const int* unit_start, int u, int n,
@@ -1406,12 +1408,15 @@ struct Model {
     }
   }
   // The weighted sum over the experts in slot order, plus the residual.
+  // (The next layer's pointers, requested during gate/up, land here: the
+  // grid barrier that follows publishes them to the whole block.)
   template <bool MOE>
   __device__ static __noinline__ void down_finish(int l) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
     const int tid = threadIdx.x;
+    asm volatile("cp.async.wait_all;" ::: "memory");
     const int n = c.n, nr = c.nr;
     for (int idx = tid; idx < n * nr; idx += kThreads) {
       const int b = idx / nr, rr = idx % nr;
@@ -1792,13 +1797,18 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     uint32_t nbar = 0;
     if (c.tm && tid == 0) c.tm[0] = globaltimer();
     // the layer's norm / router pointers in shared memory; layer l + 1's are
-    // fetched once layer l's routing has used them, during gate/up
+    // requested (cp.async, nothing waits on them) once layer l's staging has
+    // used them, and have landed by the end of the layer (down_finish waits)
     auto load_lw = [&](int l) {
       const uint32_t* src = reinterpret_cast<const uint32_t*>(a.layers + l);
-      uint32_t* dst = reinterpret_cast<uint32_t*>(&F.lw);
-      for (int i = tid; i < (int)(sizeof(LayerW) / 4); i += kThreads) dst[i] = __ldg(src + i);
+      for (int i = tid; i < (int)(sizeof(LayerW) / 4); i += kThreads)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(reinterpret_cast<uint32_t*>(&F.lw) + i)),
+                     "l"(src + i)
+                     : "memory");
+      asm volatile("cp.async.commit_group;" ::: "memory");
     };
     load_lw(0);
+    asm volatile("cp.async.wait_all;" ::: "memory");
     csync();
     for (int l = 0; ok && l < a.n_layers; ++l) {
       const int sm = M::stage_mode(c, true);
