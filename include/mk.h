@@ -129,7 +129,8 @@ typedef struct mk_info {
   int32_t num_sms;
   int32_t grid;              /* blocks per launch (one per SM) */
   int32_t block_threads;
-  int32_t smem_bytes;        /* dynamic shared memory per block */
+  int32_t smem_bytes;        /* dynamic shared memory per block of a launch of 2+ rows (one-row
+                                launches ask for less, leaving more of the SM's storage as L1) */
   int32_t n_pages;           /* KV pages in the pool (0 before mk_kv_alloc) */
   int32_t free_pages;
   int64_t scratch_bytes;     /* library-owned device scratch */
