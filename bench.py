@@ -344,6 +344,22 @@ def run_ours(args, rank, world):
                             "bytes_per_step": int(bytes16)},
                "clocks": clk16}
 
+    # per-phase timeline of one more decode launch (MK_DBG_TIMING), outside
+    # the timed region: medians over the MoE layers
+    timeline = None
+    if not args.no_timeline:
+        eng.enable_timing()
+        pos_t = prompt_len + K
+        for _ in range(2):          # the second launch is the one kept
+            eng.decode_step([0], tok, [pos_t], tok)
+            pos_t += 1
+        eng.sync()
+        timeline = eng.phase_times_us()
+        if args.timeline_out:
+            np.savez(args.timeline_out, stamps=eng.timing_stamps(), ring=eng.ring_log(),
+                     n_layers=m.n_layers, n_dense=m.n_dense)
+        eng.disable_trace()
+
     ctxs = [prompt_len + i + 1 for i in range(K)]
     bytes_avg = sum(step_bytes(m, [c], m.top_k) for c in ctxs) / K
     peaks, peak_kind = load_peaks()
@@ -379,6 +395,8 @@ def run_ours(args, rank, world):
         "clocks": clk,
         "setup_s": {"weights": round(gen_s, 1), "prefill": round(prefill_s, 3)},
     }
+    if timeline is not None:
+        out["timeline_us"] = timeline
     if b16 is not None:
         out["batch16"] = b16
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -533,6 +551,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch16-steps", type=int, default=32,
                     help="timed decode steps of the 16-sequence batch (0 = skip)")
+    ap.add_argument("--no-timeline", action="store_true", help="skip the per-phase timeline launch")
+    ap.add_argument("--timeline-out", default="", help="save the timeline launch's raw stamps (.npz)")
     ap.add_argument("--profile-case", action="store_true",
                     help="prefill + --steps decode launches only (for an ncu capture)")
     args = ap.parse_args()

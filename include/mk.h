@@ -200,10 +200,47 @@ MK_API int mk_decode_step(mk_ctx* ctx, const int32_t* seq_ids_host, const int32_
                           const int32_t* positions_host, int32_t n, int32_t* out_tokens_dev,
                           void* stream);
 
-/* Close a sequence and return its pages to the pool.  Pages become reusable
- * by launches enqueued after this call on the context's stream.
+/* Close a sequence and return its pages to the pool (a page shared with a
+ * forked sequence stays held until its last holder is released).  Pages
+ * become reusable by launches enqueued after this call on the context's
+ * stream.
  * Errors: INVALID_ARG (bad id), STATE (sequence not open). */
 MK_API int mk_seq_release(mk_ctx* ctx, int32_t seq_id);
+
+/* Copy K/V between a sequence's pages and a caller buffer.  Buffer layout:
+ * device bf16 [n_layers][n][2 (K, V)][n_kv_heads][head_dim], 16-byte
+ * aligned, owned by the caller.  Both calls run a kernel on `stream` and
+ * return without waiting; the buffer must stay valid until it finishes.
+ *
+ * mk_kv_write stores positions start_pos .. start_pos+n-1 of seq_id.
+ * start_pos must lie in [0, length]: positions below the length are
+ * overwritten, positions at or past it extend the sequence (pages are taken
+ * from the pool, the length becomes start_pos + n, a closed sequence is
+ * opened).  The KV written this way is what later launches attend to, as if
+ * the model had computed it: a prefix restored from elsewhere, or (in tests)
+ * a reference computation's cache.  "rec Megakernel and Tempo9 Compared",
+ * §1 (Prefix cache), measures the value of not recomputing a known prefix.
+ * Errors: INVALID_ARG, STATE (start_pos past the length, or a position in a
+ * page shared with another sequence), NO_PAGES (nothing written), CUDA.
+ *
+ * mk_kv_read copies positions start_pos .. start_pos+n-1 (all below the
+ * length) into dst_dev.  Errors: INVALID_ARG, STATE, CUDA. */
+MK_API int mk_kv_write(mk_ctx* ctx, int32_t seq_id, int32_t start_pos, int32_t n, const void* src_dev,
+                       void* stream);
+MK_API int mk_kv_read(mk_ctx* ctx, int32_t seq_id, int32_t start_pos, int32_t n, void* dst_dev,
+                      void* stream);
+
+/* Open sequence dst_seq as a copy of the first n_tokens positions of src_seq
+ * by SHARING their pages (no K/V is copied): n_tokens must be a positive
+ * multiple of 128 (whole pages, so neither sequence ever writes a shared
+ * page again) and at most src_seq's length; dst_seq must be closed.  Pages
+ * are reference-counted: mk_seq_release of either sequence keeps the pages
+ * the other still holds.  This is the page-pool form of the prefix reuse that
+ * "rec Megakernel and Tempo9 Compared", §1 (Prefix cache) measures (a turn
+ * reusing 7,936 of 8,022 prompt tokens in 128-token spans).  Sets dst_seq's
+ * block-table entries with a kernel on `stream`.
+ * Errors: INVALID_ARG, STATE, CUDA. */
+MK_API int mk_seq_fork(mk_ctx* ctx, int32_t src_seq, int32_t dst_seq, int32_t n_tokens, void* stream);
 
 /* Current length (positions written) of a sequence; -1 if it is not open. */
 MK_API int32_t mk_seq_length(mk_ctx* ctx, int32_t seq_id);
@@ -222,12 +259,18 @@ MK_API int mk_sync(mk_ctx* ctx, void* stream);
 #define MK_DBG_TRACE 1u
 #define MK_DBG_SKIP_ARRIVAL 2u
 #define MK_DBG_TIMING 4u   /* trace_dev receives uint64 %globaltimer stamps (ns) of
-                              block 0 instead of the trace: [0] kernel start; for layer l
-                              and phase p (0 qkv, 1 attention, 2 o_proj, 3 routing and
-                              gate/up, 4 down) [1 + 16*l + 3*p + k] with k = 0 staging
-                              done, 1 phase work done, 2 grid barrier released; then
-                              [1 + 16*n_layers] lm_head done.  Size: 8 * (16 * n_layers
-                              + 2) bytes.  Not combinable with MK_DBG_TRACE. */
+                              every block: block b's record of R = 16 * n_layers + 2
+                              stamps starts at [b * R]; in it [0] block start; for
+                              layer l and phase p (0 qkv, 1 attention, 2 o_proj,
+                              3 routing and gate/up, 4 down) [1 + 16*l + 3*p + k]
+                              with k = 0 staging done, 1 phase work done, 2 grid
+                              barrier released; then [1 + 16*n_layers] lm_head done.
+                              After the grid's records, each block's ring log of
+                              2048 stamps at [grid * R + b * 2048]: [2k] the time
+                              the block's k-th weight / KV tile was issued, [2k + 1]
+                              the time the compute warps found it landed (k < 1024).
+                              Size: 8 * grid * (R + 2048) bytes (grid: mk_get_info).
+                              Not combinable with MK_DBG_TRACE. */
 MK_API int mk_set_debug(mk_ctx* ctx, uint32_t flags, uint32_t arg, void* trace_dev,
                         size_t trace_bytes, uint32_t spin_limit_us);
 
@@ -244,11 +287,11 @@ MK_API int mk_get_info(mk_ctx* ctx, mk_info* info);
 /* Release every resource of the context (waits for its device work). */
 MK_API int mk_destroy(mk_ctx* ctx);
 
-/* Decode step that allocates no device memory.  The paper has no counterpart:
- * this entry point exists for callers that cannot call cudaMalloc — code
- * running while a stream is being captured, hosts that hand the library a
- * fixed memory budget carved by their own allocator, or real-time loops
- * that must not take the implicit device synchronisation of an allocation.
+/* Decode step that allocates no device memory.  The paper has no
+ * counterpart.  It is for callers that cannot call cudaMalloc: a host that
+ * gives the library a fixed memory budget carved by its own allocator (and
+ * so must not see allocations it did not plan), or a loop that must not take
+ * the device-wide synchronisation that cudaMalloc / cudaFree can bring.
  * It launches the same kernel as mk_decode_step without a context: the
  * per-layer pointer table, the RoPE table and the kernel's scratch live in a
  * file-scope device array of 8 MiB that every GPU loading the library holds
@@ -269,12 +312,19 @@ MK_API int mk_destroy(mk_ctx* ctx);
  * tokens_dev / out_tokens_dev: device int32[n] inputs / greedy next tokens.
  * status_dev: optional device int32[1] that receives the kernel's error word
  *   (0, MK_ERR_BARRIER_TIMEOUT or MK_ERR_DEVICE_INDEX) after the launch.
- * The first call on a device resolves the array's address and uploads the
- * RoPE table with a synchronous copy (again when rope_theta or head_dim
- * changes); make that first call before any stream capture.  Every call
- * shares the one array and it keeps the last call's contents (the call
- * clears the counters that must start at zero): calls that overlap on the
- * GPU, on any stream, race.
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address and uploads the RoPE and layer tables with
+ * synchronous copies; make that first call before any stream capture.  A
+ * later call whose model differs (weights, n_layers, rope_theta, head_dim)
+ * first waits for the whole device to go idle (cudaDeviceSynchronize: an
+ * earlier call on any stream may still read the tables), then rewrites the
+ * tables the same way.  A call with the same model as the previous one only
+ * enqueues on `stream`: three memsets that clear the counters and the error
+ * word (the array keeps the last call's contents), the launch and the
+ * optional status copy.
+ * Every call shares the one array: calls that overlap on the GPU, on any
+ * stream, race, and so does a call that changes the model while another
+ * thread's call is being enqueued.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 MK_API int mk_decode_step_static(const mk_model_desc* d, const mk_weights* w, const void* packed_dev,
                                  void* kv_dev, int32_t n_pages, int32_t* block_table_dev,

@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
               "-I" + CSRC]
-SOURCES = ["mk_kernel.cu", "mk_host.cpp", "mk_static.cu", "mk_pack.cu"]
+SOURCES = ["mk_kernel.cu", "mk_host.cpp", "mk_static.cu", "mk_pack.cu", "mk_kv.cu"]
 
 
 def _nvcc() -> str:

@@ -75,6 +75,9 @@ SIGNATURES = {
     "mk_decode_step": (C.c_int, [C.c_void_p, C.POINTER(C.c_int32), C.c_void_p,
                                  C.POINTER(C.c_int32), C.c_int32, C.c_void_p, C.c_void_p]),
     "mk_seq_release": (C.c_int, [C.c_void_p, C.c_int32]),
+    "mk_kv_write": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
+    "mk_kv_read": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]),
+    "mk_seq_fork": (C.c_int, [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p]),
     "mk_seq_length": (C.c_int32, [C.c_void_p, C.c_int32]),
     "mk_sync": (C.c_int, [C.c_void_p, C.c_void_p]),
     "mk_set_debug": (C.c_int, [C.c_void_p, C.c_uint32, C.c_uint32, C.c_void_p, C.c_size_t,
@@ -149,6 +152,18 @@ def mk_decode_step(ctx: int, seq_ids, tokens_dev: int, positions, out_tokens_dev
 
 def mk_seq_release(ctx: int, seq_id: int):
     _check(load().mk_seq_release(ctx, seq_id))
+
+
+def mk_kv_write(ctx: int, seq_id: int, start_pos: int, n: int, src_dev: int, stream: int = 0):
+    _check(load().mk_kv_write(ctx, seq_id, start_pos, n, src_dev, stream))
+
+
+def mk_kv_read(ctx: int, seq_id: int, start_pos: int, n: int, dst_dev: int, stream: int = 0):
+    _check(load().mk_kv_read(ctx, seq_id, start_pos, n, dst_dev, stream))
+
+
+def mk_seq_fork(ctx: int, src_seq: int, dst_seq: int, n_tokens: int, stream: int = 0):
+    _check(load().mk_seq_fork(ctx, src_seq, dst_seq, n_tokens, stream))
 
 
 def mk_seq_length(ctx: int, seq_id: int) -> int:

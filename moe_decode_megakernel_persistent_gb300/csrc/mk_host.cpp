@@ -70,6 +70,7 @@ struct mk_ctx {
   int32_t n_pages = 0;
   size_t kv_bytes = 0;
   std::vector<int32_t> free_pages;  // stack; back() is handed out next
+  std::vector<int32_t> page_ref;    // sequences holding each page (forked sequences share pages)
   int32_t* block_table_dev = nullptr;
   int32_t max_pages_per_seq = 0;
   std::vector<Seq> seqs;
@@ -135,7 +136,7 @@ size_t carve_scratch(const mk_model_desc& d, int grid, int max_units, char* base
   s.q = (float*)take(sizeof(float) * kMaxBatch * QD);
   s.attn = (float*)take(sizeof(float) * kMaxBatch * QD);
   s.part = (float*)take(sizeof(float) * (size_t)max_units * GQA * (d.head_dim + 4));
-  s.rlogit = (float*)take(sizeof(float) * kRlogitGroups * kMaxBatch * d.n_experts);
+  s.rlogit = (long long*)take(sizeof(long long) * kRlogitGroups * kMaxBatch * d.n_experts);
   s.act = (float*)take(sizeof(float) * kMaxBatch * d.top_k * d.expert_ffn);
   s.dact = (float*)take(sizeof(float) * kMaxBatch * d.dense_ffn);
   s.amax_v = (float*)take(sizeof(float) * (size_t)grid * kMaxBatch);
@@ -183,14 +184,16 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
   if (!c->kv_dev) return fail(MK_ERR_STATE, "mk_kv_alloc has not been called");
   if ((c->dbg_flags & MK_DBG_TRACE) && c->trace_bytes < mk_trace_bytes(&c->d, n))
     return fail(MK_ERR_INVALID_ARG, "trace buffer is smaller than mk_trace_bytes(rows)");
-  if ((c->dbg_flags & MK_DBG_TIMING) && c->trace_bytes < sizeof(uint64_t) * (16 * (size_t)c->d.n_layers + 2))
-    return fail(MK_ERR_INVALID_ARG, "timing buffer is smaller than 8 * (16 * n_layers + 2) bytes");
+  if ((c->dbg_flags & MK_DBG_TIMING) &&
+      c->trace_bytes < sizeof(uint64_t) * (size_t)c->grid * (16 * (size_t)c->d.n_layers + 2 + 2 * kRingLog))
+    return fail(MK_ERR_INVALID_ARG, "timing buffer is smaller than 8 * grid * (16 * n_layers + 2 + 2048) bytes");
   StepArgs a;
   std::memset(&a, 0, sizeof(a));
   std::vector<std::pair<int, int32_t>> taken;  // (slot, page) handed out by this call
   auto rollback = [&]() {
     for (auto it = taken.rbegin(); it != taken.rend(); ++it) {
       c->seqs[it->first].pages.pop_back();
+      c->page_ref[it->second] = 0;
       c->free_pages.push_back(it->second);
     }
   };
@@ -205,6 +208,7 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
       }
       const int32_t pg = c->free_pages.back();
       c->free_pages.pop_back();
+      c->page_ref[pg] = 1;
       q.pages.push_back(pg);
       taken.emplace_back(s, pg);
       a.upd[a.n_upd++] = PageUpd{s, pi, pg};
@@ -498,6 +502,7 @@ MK_API int mk_kv_alloc(mk_ctx* c, int32_t n_pages) {
     return fail(MK_ERR_CUDA, std::string("block table: ") + cudaGetErrorString(e));
   }
   c->n_pages = n_pages;
+  c->page_ref.assign(n_pages, 0);
   c->free_pages.clear();
   for (int32_t p = n_pages - 1; p >= 0; --p) c->free_pages.push_back(p);
   return MK_OK;
@@ -577,8 +582,125 @@ MK_API int mk_seq_release(mk_ctx* c, int32_t seq_id) {
   if (seq_id < 0 || seq_id >= c->d.max_seqs) return fail(MK_ERR_INVALID_ARG, "seq_id out of range");
   Seq& q = c->seqs[seq_id];
   if (!q.open) return fail(MK_ERR_STATE, "sequence is not open");
-  for (auto it = q.pages.rbegin(); it != q.pages.rend(); ++it) c->free_pages.push_back(*it);
+  for (auto it = q.pages.rbegin(); it != q.pages.rend(); ++it)
+    if (--c->page_ref[*it] == 0) c->free_pages.push_back(*it);
   q = Seq{};
+  return MK_OK;
+}
+
+// Common part of the KV transfers: a KvXfer with the context's pool.
+static KvXfer xfer_base(const mk_ctx* c, int32_t seq_id) {
+  KvXfer x;
+  std::memset(&x, 0, sizeof(x));
+  x.kv = c->kv_dev;
+  x.block_table = c->block_table_dev;
+  x.n_pages = c->n_pages;
+  x.max_pages_per_seq = c->max_pages_per_seq;
+  x.n_layers = c->d.n_layers;
+  x.n_kv_heads = c->d.n_kv_heads;
+  x.head_dim = c->d.head_dim;
+  x.slot = seq_id;
+  return x;
+}
+
+MK_API int mk_kv_write(mk_ctx* c, int32_t seq_id, int32_t start_pos, int32_t n, const void* src_dev,
+                       void* stream) {
+  g_err.clear();
+  if (!c) return fail(MK_ERR_INVALID_ARG, "ctx is NULL");
+  if (!src_dev || !aligned16(src_dev)) return fail(MK_ERR_INVALID_ARG, "src_dev is NULL or not 16-byte aligned");
+  if (n < 1) return fail(MK_ERR_INVALID_ARG, "n must be >= 1");
+  if (seq_id < 0 || seq_id >= c->d.max_seqs) return fail(MK_ERR_INVALID_ARG, "seq_id out of range");
+  if (!c->kv_dev) return fail(MK_ERR_STATE, "mk_kv_alloc has not been called");
+  Seq& q = c->seqs[seq_id];
+  const int len = q.open ? q.len : 0;
+  if (start_pos < 0 || start_pos > len) return fail(MK_ERR_STATE, "start_pos must be in [0, sequence length]");
+  if ((long long)start_pos + n > c->d.max_ctx) return fail(MK_ERR_INVALID_ARG, "positions exceed max_ctx");
+  // positions already held may be overwritten only in pages of this sequence alone
+  for (int pi = start_pos / kPageTokens; pi < (int)q.pages.size() && pi * kPageTokens < start_pos + n; ++pi)
+    if (c->page_ref[q.pages[pi]] > 1) return fail(MK_ERR_STATE, "position lies in a page shared with another sequence");
+  const int have = (int)q.pages.size();
+  const int need = (start_pos + n + kPageTokens - 1) / kPageTokens - have;
+  if (need > (int)c->free_pages.size()) return fail(MK_ERR_NO_PAGES, "KV page pool exhausted");
+  // segments of at most kMaxUpd - 1 pages, so one launch carries every new page it touches
+  const int seg = (kMaxUpd - 1) * kPageTokens;
+  const uint16_t* src = static_cast<const uint16_t*>(src_dev);
+  const size_t per_pos = (size_t)2 * c->d.n_kv_heads * c->d.head_dim;  // bf16 values of one position, one layer
+  for (int off = 0; off < n; off += seg) {
+    const int m = std::min(seg, n - off);
+    KvXfer x = xfer_base(c, seq_id);
+    x.start = start_pos + off;
+    x.n = m;
+    x.upd_index0 = (int)q.pages.size();
+    const int end_page = (x.start + m + kPageTokens - 1) / kPageTokens;
+    while ((int)q.pages.size() < end_page) {
+      const int32_t pg = c->free_pages.back();
+      c->free_pages.pop_back();
+      c->page_ref[pg] = 1;
+      x.upd[x.n_upd++] = PageUpd{seq_id, (int32_t)q.pages.size(), pg};
+      q.pages.push_back(pg);
+    }
+    // the caller buffer holds all n positions per layer: copy layer by layer
+    // when the call is split, else in one launch
+    if (m == n) {
+      x.src = src;
+      if (int r = launch_kv_xfer(x, (cudaStream_t)stream)) return r;
+    } else {
+      for (int l = 0; l < c->d.n_layers; ++l) {
+        KvXfer y = x;
+        y.n_layers = 1;
+        y.src = src + ((size_t)l * n + off) * per_pos;
+        y.kv = c->kv_dev + (size_t)l * c->n_pages * 2 * c->d.n_kv_heads * kPageTokens * c->d.head_dim;
+        if (l > 0) y.n_upd = 0;  // the entries are set by the first launch; reads use the list
+        if (int r = launch_kv_xfer(y, (cudaStream_t)stream)) return r;
+      }
+    }
+    q.open = true;
+    q.len = std::max(q.len, x.start + m);
+  }
+  return MK_OK;
+}
+
+MK_API int mk_kv_read(mk_ctx* c, int32_t seq_id, int32_t start_pos, int32_t n, void* dst_dev, void* stream) {
+  g_err.clear();
+  if (!c) return fail(MK_ERR_INVALID_ARG, "ctx is NULL");
+  if (!dst_dev || !aligned16(dst_dev)) return fail(MK_ERR_INVALID_ARG, "dst_dev is NULL or not 16-byte aligned");
+  if (n < 1) return fail(MK_ERR_INVALID_ARG, "n must be >= 1");
+  if (seq_id < 0 || seq_id >= c->d.max_seqs) return fail(MK_ERR_INVALID_ARG, "seq_id out of range");
+  if (!c->kv_dev) return fail(MK_ERR_STATE, "mk_kv_alloc has not been called");
+  const Seq& q = c->seqs[seq_id];
+  if (!q.open || start_pos < 0 || (long long)start_pos + n > q.len)
+    return fail(MK_ERR_STATE, "positions must lie within the open sequence");
+  KvXfer x = xfer_base(c, seq_id);
+  x.start = start_pos;
+  x.n = n;
+  x.dst = static_cast<uint16_t*>(dst_dev);
+  x.upd_index0 = INT32_MAX;
+  return launch_kv_xfer(x, (cudaStream_t)stream);
+}
+
+MK_API int mk_seq_fork(mk_ctx* c, int32_t src_seq, int32_t dst_seq, int32_t n_tokens, void* stream) {
+  g_err.clear();
+  if (!c) return fail(MK_ERR_INVALID_ARG, "ctx is NULL");
+  if (src_seq < 0 || src_seq >= c->d.max_seqs || dst_seq < 0 || dst_seq >= c->d.max_seqs || src_seq == dst_seq)
+    return fail(MK_ERR_INVALID_ARG, "sequence ids out of range or equal");
+  if (!c->kv_dev) return fail(MK_ERR_STATE, "mk_kv_alloc has not been called");
+  const Seq& a = c->seqs[src_seq];
+  Seq& b = c->seqs[dst_seq];
+  if (!a.open) return fail(MK_ERR_STATE, "source sequence is not open");
+  if (b.open) return fail(MK_ERR_STATE, "destination sequence is already open");
+  if (n_tokens < kPageTokens || n_tokens % kPageTokens != 0 || n_tokens > a.len)
+    return fail(MK_ERR_INVALID_ARG, "n_tokens must be a positive multiple of 128 within the source's length");
+  const int np = n_tokens / kPageTokens;
+  for (int i0 = 0; i0 < np; i0 += kMaxUpd) {
+    KvXfer x = xfer_base(c, dst_seq);
+    x.upd_index0 = i0;
+    for (int i = i0; i < std::min(np, i0 + kMaxUpd); ++i) x.upd[x.n_upd++] = PageUpd{dst_seq, i, a.pages[i]};
+    if (int r = launch_kv_xfer(x, (cudaStream_t)stream)) return r;
+  }
+  b.pages.assign(a.pages.begin(), a.pages.begin() + np);
+  for (int32_t pg : b.pages) ++c->page_ref[pg];
+  b.open = true;
+  b.len = n_tokens;
   return MK_OK;
 }
 

@@ -17,6 +17,12 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBlockThreads = kThreads + 32;  // plus one weight-streaming warp
 constexpr int kMaxStages = 16;       // shared-memory ring stages
 constexpr int kRlogitGroups = 8;     // copies of the router-logit sums (less atomic contention)
+// Router-logit partials are summed as 64-bit fixed-point integers (units of
+// 2^-32): integer addition is associative, so the sum, and with it the expert
+// selection, is the same bits whatever order the blocks' atomics land in.
+// Range: |sum| < 2^31.
+constexpr double kRlogitScale = 4294967296.0;
+constexpr int kRingLog = 1024;      // ring items per block whose issue / arrival times MK_DBG_TIMING logs
 constexpr int kMaxUpd = 64;          // block-table updates carried by one launch
 constexpr int kMaxRowsPerBlock = 32; // hidden rows owned by one block (hidden / grid)
 constexpr int kMaxOwnUnits = 4;     // attention units one block may take in a launch
@@ -64,8 +70,9 @@ struct Scratch {
   float* q;          // [kMaxBatch][n_heads*hd] roped queries
   float* attn;       // [kMaxBatch][n_heads*hd] merged attention output
   float* part;       // [max_units][gqa][hd + 2] attention partials (m, l, o[hd])
-  float* rlogit;     // [kRlogitGroups][kMaxBatch][E] router logits before the RMS scale: block
-                     // partials summed into one of kRlogitGroups copies (block id mod groups)
+  long long* rlogit; // [kRlogitGroups][kMaxBatch][E] router logits before the RMS scale, fixed
+                     // point (kRlogitScale): block partials summed into one of kRlogitGroups
+                     // copies (block id mod groups)
   float* act;        // [kMaxBatch][top_k][Fe] expert activations
   float* dact;       // [kMaxBatch][Fd] dense-MLP activations
   float* amax_v;     // [grid][kMaxBatch] per-block best logit
@@ -112,6 +119,24 @@ struct StepArgs {
   int32_t cur_page[kMaxBatch];
   PageUpd upd[kMaxUpd];
 };
+
+// One KV transfer (mk_kv.cu): block-table entries to set, then the K/V of
+// positions [start, start + n) of sequence `slot` copied from src into the
+// pool (src != null) or from the pool into dst.  Caller buffer layout: bf16
+// [n_layers][n][K|V][n_kv_heads][head_dim].  upd[i] sets page index
+// upd_index0 + i of sequence `slot` (fork calls may set other sequences'
+// entries with n == 0).
+struct KvXfer {
+  uint16_t* kv;
+  int32_t* block_table;
+  const uint16_t* src;
+  uint16_t* dst;
+  int32_t n_pages, max_pages_per_seq, n_layers, n_kv_heads, head_dim;
+  int32_t slot, start, n;
+  int32_t n_upd, upd_index0;
+  PageUpd upd[kMaxUpd];
+};
+int launch_kv_xfer(const KvXfer& a, cudaStream_t st);
 
 // Error sites recorded in err[1].
 enum ErrSite { SITE_BARRIER = 1, SITE_PAGE = 2, SITE_UNIT = 3, SITE_TOKEN = 4, SITE_RING = 5, SITE_SMEM = 6 };

@@ -34,7 +34,7 @@
 namespace mk {
 
 constexpr int kMaxEnt = kMaxBatch * 8;  // (row, expert slot) entries
-constexpr int kMmaUnits = 8;            // tensor-core units per pass (shared accumulators)
+constexpr int kMmaUnits = 2;            // tensor-core units per pass (a dense tile has at most 2)
 
 // Per-launch, per-block context shared by the phases (in shared memory).
 struct Ctx {
@@ -46,7 +46,8 @@ struct Ctx {
   int r0, nr;      // hidden rows owned by this block
   bool tc;         // tensor-core GEMV (plain fp32 staging) for this launch
   float *tr_x, *tr_attn, *tr_rl, *tr_tk, *tr_fin;
-  uint64_t* tm;    // timing stamps (block 0, thread 0 only) or null
+  uint64_t* tm;    // this block's timing stamps (thread 0 writes them) or null
+  uint64_t* ring_log;  // this block's ring log: [2k] item k issued, [2k + 1] item k landed (or null)
 };
 
 struct Fixed {
@@ -68,8 +69,7 @@ struct Fixed {
   uint32_t nslw[kMaxRowsPerBlock];  // raw slice of the post-attention norm weights
   float red[kThreads];
   unsigned long long best_key[kMaxBatch];  // lm_head argmax per row (argmax_key)
-  float mma_acc[2 * kMmaUnits * 128];      // tensor-core path: per-unit partial sums (two sets)
-  uint32_t mma_flip;                       // which set the next pass uses
+  float mma_part[kWarps * 128];            // tensor-core path: each warp's partial of its unit
   int unit_start[kMaxBatch + 1];
   int upages[2][64];      // pool pages of this block's attention units (streaming warp)
   float rnorm[kMaxBatch];
@@ -126,6 +126,7 @@ __device__ __forceinline__ const uint8_t* ring_acquire(uint32_t k) {
   const int s = (int)(k % (uint32_t)F.ctx.ns);
   const uint32_t par = (k / (uint32_t)F.ctx.ns) & 1u;
   mbar_wait(&F.full[s], par, &F.abort, F.args.sc.err, F.args.spin_limit_ns, (int)k);
+  if (F.ctx.ring_log && threadIdx.x == 0 && k < (uint32_t)kRingLog) F.ctx.ring_log[2 * k + 1] = globaltimer();
   return F.ctx.ring + (size_t)s * STAGE;
 }
 __device__ __forceinline__ void ring_release(uint32_t k) {
@@ -164,6 +165,7 @@ struct Producer {
     }
     stage = F.ctx.ring + (size_t)s * STAGE;
     bar = &F.full[s];
+    if (F.ctx.ring_log && k < (uint32_t)kRingLog) F.ctx.ring_log[2 * k] = globaltimer();
     return true;
   }
   __device__ __forceinline__ void copy(uint32_t off, const void* src, uint32_t bytes) {
@@ -468,164 +470,161 @@ struct Model {
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   }
 
+  // Walk the units of one ring tile in order: (m-tile, run of tasks sharing
+  // one activation list, n-tile of 8 activations); f(u, ta, tb, sa, sb, ar, c0).
+  template <int RP, class TK, class F_>
+  __device__ static __forceinline__ int for_units(int t0, int tn, const TK& task, F_ f) {
+    constexpr int MT = RP == 2 ? 8 : 16;
+    int u = 0;
+#pragma unroll 1
+    for (int ta = 0; ta < tn; ta += MT) {
+      const int tb = min(tn, ta + MT);
+#pragma unroll 1
+      for (int sa = ta; sa < tb;) {
+        const ActRange ar = task.acts(t0 + sa);
+        int sb = sa + 1;
+        while (sb < tb && same_acts(task.acts(t0 + sb), ar)) ++sb;
+#pragma unroll 1
+        for (int c0 = 0; c0 < ar.count; c0 += 8, ++u) f(u, ta, tb, sa, sb, ar, c0);
+        sa = sb;
+      }
+    }
+    return u;
+  }
+
   template <int K, int RP, int T, class TK>
   __device__ static __forceinline__ void run_mma(int ntask, const uint8_t* act_base, const TK& task) {
     using Gv = Gemv<WDT, K>;
     constexpr int NGR = K / 64;
-    constexpr int MT = RP == 2 ? 8 : 16;
     constexpr int RB = Gv::ROW_BYTES, AS = plain_stride(K);
     static_assert(K % 64 == 0, "whole 64-value groups");
     Fixed& F = fixed();
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, q = lane & 3;
     uint32_t k = F.kc;
-    uint32_t flip = F.mma_flip;  // every thread advances its own copy identically
 #pragma unroll 1
     for (int t0 = 0; t0 < ntask; t0 += T, ++k) {
       const uint8_t* st = ring_acquire<STAGE>(k);
       const int tn = min(T, ntask - t0);
+      const int n_units = for_units<RP>(t0, tn, task, [](int, int, int, int, int, const ActRange&, int) {});
 #pragma unroll 1
-      for (int base = 0;; base += kMmaUnits) {
-        // accumulators of this pass (two sets used alternately; the output
-        // step zeroes what it reads, so no separate clearing pass)
-        float* accs = F.mma_acc + (flip & 1) * (kMmaUnits * 128);
-        // walk the tile's units (m-tile, run of tasks, n-tile); units
-        // [base, base + kMmaUnits) are computed in this pass
-        int u = 0;
+      for (int base = 0; base < n_units; base += kMmaUnits) {
+        // units [base, base + U) are computed in this pass: warp w works on
+        // unit base + w % U, over the 64-value groups w / U, w / U + nw, ...
+        // (nw = warps on that unit), and writes its partial to its own slot;
+        // the slots of a unit are then summed in warp order, so the result
+        // does not depend on timing
+        const int U = min(kMmaUnits, n_units - base);
+        const int my_u = base + wid % U, kw = wid / U, nw = (kWarps - wid % U + U - 1) / U;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for_units<RP>(t0, tn, task, [&](int u, int ta, int tb, int, int, const ActRange& ar, int c0) {
+          if (u != my_u) return;
+          // rows of this lane: task rows rho0 = g, rho1 = g + 8 of the m-tile
+          int j0, j1, seg1;
+          if (RP == 2) { j0 = ta + g; j1 = j0; seg1 = 1; }
+          else { j0 = ta + g; j1 = ta + 8 + g; seg1 = 0; }
+          j0 = j0 < tb ? j0 : ta;
+          j1 = j1 < tb ? j1 : ta;
+          constexpr int RC = rec<K>();
+          const uint8_t* w0 = st + (size_t)(j0 * RP) * RC;
+          const uint8_t* w1 = st + (size_t)(j1 * RP + seg1) * RC;
+          const uint8_t* s0p = w0 + RB;
+          const uint8_t* s1p = w1 + RB;
+          // this lane's activation column
+          const int col = c0 + g;
+          const bool cv = col < ar.count;
+          const int ai = cv ? (ar.list ? ar.list[ar.start + col] : ar.start + col) : 0;
+          const uint8_t* xa = act_base + (size_t)ai * AS;
 #pragma unroll 1
-        for (int ta = 0; ta < tn; ta += MT) {
-          const int tb = min(tn, ta + MT);
-#pragma unroll 1
-          for (int sa = ta; sa < tb;) {
-            const ActRange ar = task.acts(t0 + sa);
-            int sb = sa + 1;
-            while (sb < tb && same_acts(task.acts(t0 + sb), ar)) ++sb;
-#pragma unroll 1
-            for (int c0 = 0; c0 < ar.count; c0 += 8, ++u) {
-              if (u < base || u >= base + kMmaUnits) continue;
-              // rows of this lane: task rows rho0 = g, rho1 = g + 8 of the m-tile
-              int j0, j1, seg1;
-              if (RP == 2) { j0 = ta + g; j1 = j0; seg1 = 1; }
-              else { j0 = ta + g; j1 = ta + 8 + g; seg1 = 0; }
-              j0 = j0 < tb ? j0 : ta;
-              j1 = j1 < tb ? j1 : ta;
-              constexpr int RC = rec<K>();
-              const uint8_t* w0 = st + (size_t)(j0 * RP) * RC;
-              const uint8_t* w1 = st + (size_t)(j1 * RP + seg1) * RC;
-              const uint8_t* s0p = w0 + RB;
-              const uint8_t* s1p = w1 + RB;
-              // this lane's activation column
-              const int col = c0 + g;
-              const bool cv = col < ar.count;
-              const int ai = cv ? (ar.list ? ar.list[ar.start + col] : ar.start + col) : 0;
-              const uint8_t* xa = act_base + (size_t)ai * AS;
-              float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-              for (int G = wid; G < NGR; G += kWarps) {
-                float xv[16];
+          for (int G = kw; G < NGR; G += nw) {
+            float xv[16];
 #pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4) {
-                  const uint4 r = cv ? lds128(xa + (64 * G + 16 * q + 4 * v4) * 4) : make_uint4(0u, 0u, 0u, 0u);
-                  xv[4 * v4] = __uint_as_float(r.x); xv[4 * v4 + 1] = __uint_as_float(r.y);
-                  xv[4 * v4 + 2] = __uint_as_float(r.z); xv[4 * v4 + 3] = __uint_as_float(r.w);
-                }
-                uint32_t aw[2][8];  // per row: bf16x2 words for steps 0..3 (2 per step)
-                if constexpr (WDT == WINT4) {
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const uint4 r = cv ? lds128(xa + (64 * G + 16 * q + 4 * v4) * 4) : make_uint4(0u, 0u, 0u, 0u);
+              xv[4 * v4] = __uint_as_float(r.x); xv[4 * v4 + 1] = __uint_as_float(r.y);
+              xv[4 * v4 + 2] = __uint_as_float(r.z); xv[4 * v4 + 3] = __uint_as_float(r.w);
+            }
+            uint32_t aw[2][8];  // per row: bf16x2 words for steps 0..3 (2 per step)
+            if constexpr (WDT == WINT4) {
 #pragma unroll
-                  for (int r = 0; r < 2; ++r) {
-                    const uint2 wv = lds64((r ? w1 : w0) + 32 * G + 8 * q);
-                    const uint32_t x2[2] = {wv.x, wv.y};
+              for (int r = 0; r < 2; ++r) {
+                const uint2 wv = lds64((r ? w1 : w0) + 32 * G + 8 * q);
+                const uint32_t x2[2] = {wv.x, wv.y};
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                      const uint32_t y = x2[h] ^ 0x88888888u;
-                      const uint32_t E = y & 0x0F0F0F0Fu, O = (y >> 4) & 0x0F0F0F0Fu;
+                for (int h = 0; h < 2; ++h) {
+                  const uint32_t y = x2[h] ^ 0x88888888u;
+                  const uint32_t E = y & 0x0F0F0F0Fu, O = (y >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
-                      for (int bi = 0; bi < 4; ++bi) aw[r][4 * h + bi] = nib_pair_bf16(E, O, bi);
-                    }
-                  }
-                } else {
-#pragma unroll
-                  for (int r = 0; r < 2; ++r) {
-                    const uint4 lo = lds128((r ? w1 : w0) + 128 * G + 32 * q);
-                    const uint4 hi = lds128((r ? w1 : w0) + 128 * G + 32 * q + 16);
-                    aw[r][0] = lo.x; aw[r][1] = lo.y; aw[r][2] = lo.z; aw[r][3] = lo.w;
-                    aw[r][4] = hi.x; aw[r][5] = hi.y; aw[r][6] = hi.z; aw[r][7] = hi.w;
-                  }
-                }
-                float cg[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int sstep = 0; sstep < 4; ++sstep) {
-                  uint32_t bh0, bm0, bl0, bh1, bm1, bl1;
-                  split3(xv[4 * sstep], xv[4 * sstep + 1], bh0, bm0, bl0);
-                  split3(xv[4 * sstep + 2], xv[4 * sstep + 3], bh1, bm1, bl1);
-                  const uint32_t a0 = aw[0][2 * sstep], a2 = aw[0][2 * sstep + 1];
-                  const uint32_t a1 = aw[1][2 * sstep], a3 = aw[1][2 * sstep + 1];
-                  mma16816(cg, a0, a1, a2, a3, bh0, bh1);
-                  mma16816(cg, a0, a1, a2, a3, bm0, bm1);
-                  mma16816(cg, a0, a1, a2, a3, bl0, bl1);
-                }
-                if constexpr (WDT == WINT4) {
-                  const float sc0 = bf16_to_f(lds16(s0p + 2 * G)), sc1 = bf16_to_f(lds16(s1p + 2 * G));
-                  acc[0] = fmaf(cg[0], sc0, acc[0]);
-                  acc[1] = fmaf(cg[1], sc0, acc[1]);
-                  acc[2] = fmaf(cg[2], sc1, acc[2]);
-                  acc[3] = fmaf(cg[3], sc1, acc[3]);
-                } else {
-#pragma unroll
-                  for (int r = 0; r < 4; ++r) acc[r] += cg[r];
+                  for (int bi = 0; bi < 4; ++bi) aw[r][4 * h + bi] = nib_pair_bf16(E, O, bi);
                 }
               }
+            } else {
 #pragma unroll
-              for (int r = 0; r < 4; ++r) atomicAdd(&accs[((u - base) * 32 + lane) * 4 + r], acc[r]);
-            }
-            sa = sb;
-          }
-        }
-        const int n_units = u;
-        csync();
-        // results: warp w writes unit base + w (lane: rows g / g + 8, columns 2q, 2q + 1)
-        u = 0;
-#pragma unroll 1
-        for (int ta = 0; ta < tn; ta += MT) {
-          const int tb = min(tn, ta + MT);
-#pragma unroll 1
-          for (int sa = ta; sa < tb;) {
-            const ActRange ar = task.acts(t0 + sa);
-            int sb = sa + 1;
-            while (sb < tb && same_acts(task.acts(t0 + sb), ar)) ++sb;
-#pragma unroll 1
-            for (int c0 = 0; c0 < ar.count; c0 += 8, ++u) {
-              if (u - base != wid) continue;
-              float* r4 = &accs[((u - base) * 32 + lane) * 4];
-#pragma unroll
-              for (int cc = 0; cc < 2; ++cc) {
-                const int col = c0 + 2 * q + cc;
-                if (col >= ar.count) continue;
-                const int ai = ar.list ? ar.list[ar.start + col] : ar.start + col;
-                if (RP == 2) {
-                  const int j = ta + g;
-                  if (j >= sa && j < sb) task.put(t0 + j, ai, col, r4[cc], r4[2 + cc]);
-                } else {
-                  const int ja = ta + g, jb = ta + 8 + g;
-                  if (ja >= sa && ja < sb) task.put(t0 + ja, ai, col, r4[cc], 0.f);
-                  if (jb >= sa && jb < sb) task.put(t0 + jb, ai, col, r4[2 + cc], 0.f);
-                }
+              for (int r = 0; r < 2; ++r) {
+                const uint4 lo = lds128((r ? w1 : w0) + 128 * G + 32 * q);
+                const uint4 hi = lds128((r ? w1 : w0) + 128 * G + 32 * q + 16);
+                aw[r][0] = lo.x; aw[r][1] = lo.y; aw[r][2] = lo.z; aw[r][3] = lo.w;
+                aw[r][4] = hi.x; aw[r][5] = hi.y; aw[r][6] = hi.z; aw[r][7] = hi.w;
               }
-              r4[0] = 0.f; r4[1] = 0.f; r4[2] = 0.f; r4[3] = 0.f;
             }
-            sa = sb;
+            float cg[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int sstep = 0; sstep < 4; ++sstep) {
+              uint32_t bh0, bm0, bl0, bh1, bm1, bl1;
+              split3(xv[4 * sstep], xv[4 * sstep + 1], bh0, bm0, bl0);
+              split3(xv[4 * sstep + 2], xv[4 * sstep + 3], bh1, bm1, bl1);
+              const uint32_t a0 = aw[0][2 * sstep], a2 = aw[0][2 * sstep + 1];
+              const uint32_t a1 = aw[1][2 * sstep], a3 = aw[1][2 * sstep + 1];
+              mma16816(cg, a0, a1, a2, a3, bh0, bh1);
+              mma16816(cg, a0, a1, a2, a3, bm0, bm1);
+              mma16816(cg, a0, a1, a2, a3, bl0, bl1);
+            }
+            if constexpr (WDT == WINT4) {
+              const float sc0 = bf16_to_f(lds16(s0p + 2 * G)), sc1 = bf16_to_f(lds16(s1p + 2 * G));
+              acc[0] = fmaf(cg[0], sc0, acc[0]);
+              acc[1] = fmaf(cg[1], sc0, acc[1]);
+              acc[2] = fmaf(cg[2], sc1, acc[2]);
+              acc[3] = fmaf(cg[3], sc1, acc[3]);
+            } else {
+#pragma unroll
+              for (int r = 0; r < 4; ++r) acc[r] += cg[r];
+            }
           }
-        }
-        ++flip;
-        if (base + kMmaUnits >= n_units) break;
+        });
+        *reinterpret_cast<float4*>(&F.mma_part[(wid * 32 + lane) * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         csync();
+        // results: warp j < U writes unit base + j (lane: rows g / g + 8,
+        // columns 2q, 2q + 1), summing the slots of warps j, j + U, ... in order
+        if (wid < U) {
+          const int my_out = base + wid;
+          for_units<RP>(t0, tn, task, [&](int u, int ta, int tb, int sa, int sb, const ActRange& ar, int c0) {
+            if (u != my_out) return;
+            float r4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int w = wid; w < kWarps; w += U) {
+              const float4 v = *reinterpret_cast<const float4*>(&F.mma_part[(w * 32 + lane) * 4]);
+              r4[0] += v.x; r4[1] += v.y; r4[2] += v.z; r4[3] += v.w;
+            }
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int col = c0 + 2 * q + cc;
+              if (col >= ar.count) continue;
+              const int ai = ar.list ? ar.list[ar.start + col] : ar.start + col;
+              if (RP == 2) {
+                const int j = ta + g;
+                if (j >= sa && j < sb) task.put(t0 + j, ai, col, r4[cc], r4[2 + cc]);
+              } else {
+                const int ja = ta + g, jb = ta + 8 + g;
+                if (ja >= sa && ja < sb) task.put(t0 + ja, ai, col, r4[cc], 0.f);
+                if (jb >= sa && jb < sb) task.put(t0 + jb, ai, col, r4[2 + cc], 0.f);
+              }
+            }
+          });
+        }
+        csync();  // the slots are free for the next pass
       }
       ring_release(k);
     }
     csync();
-    if (threadIdx.x == 0) {
-      F.kc = k;
-      F.mma_flip = flip;
-    }
+    if (threadIdx.x == 0) F.kc = k;
     csync();
   }
 
@@ -651,7 +650,7 @@ struct Model {
         a.block_table[a.upd[i].slot * a.max_pages_per_seq + a.upd[i].index] = a.upd[i].page;
     if (c.bid == 0 && l >= a.n_dense)  // router logits are accumulated in P3
       for (int i = tid; i < kRlogitGroups * n * E; i += kThreads)
-        a.sc.rlogit[(i / (n * E)) * kMaxBatch * E + i % (n * E)] = 0.f;
+        a.sc.rlogit[(i / (n * E)) * kMaxBatch * E + i % (n * E)] = 0ll;
     if (l >= a.n_dense) fetch_router_slice(Lw);
     {
       const void* nw = Lw.attn_norm;
@@ -1149,11 +1148,14 @@ struct Model {
       float s = 0.f;
       for (int t = 0; t < c.nr; ++t)
         s = fmaf(F.hs[b][t] * slice_val(F.nslw, t), slice_val(rs + e * kMaxRowsPerBlock, t), s);
-      // every block adds its partial into one of kRlogitGroups copies (fewer
-      // atomics queue on one address); after the grid barrier every block
-      // sums the copies in a fixed order (the order of the additions within a
-      // copy may differ run to run)
-      atomicAdd(a.sc.rlogit + (c.bid % kRlogitGroups) * kMaxBatch * E + b * E + e, s);
+      // every block adds its partial, as a 64-bit fixed-point integer, into
+      // one of kRlogitGroups copies (fewer atomics queue on one address);
+      // after the grid barrier every block sums the copies.  Integer sums do
+      // not depend on the order of the additions, so every run and every
+      // block get the same logits bit for bit.
+      const long long q = __double2ll_rn((double)s * kRlogitScale);
+      atomicAdd(reinterpret_cast<unsigned long long*>(a.sc.rlogit + (c.bid % kRlogitGroups) * kMaxBatch * E + b * E + e),
+                (unsigned long long)q);
     }
   }
 
@@ -1176,10 +1178,11 @@ struct Model {
       // partial logits into shared memory (F.dots is free between P3 and P5)
       float* lg = &F.dots[0][0];
       for (int i = tid; i < n * E; i += kThreads) {
-        float v = 0.f;
+        unsigned long long v = 0ull;  // wrapping two's-complement sum
 #pragma unroll
-        for (int gr = 0; gr < kRlogitGroups; ++gr) v += __ldcg(a.sc.rlogit + gr * kMaxBatch * E + i);
-        lg[i] = v;
+        for (int gr = 0; gr < kRlogitGroups; ++gr)
+          v += (unsigned long long)__ldcg(a.sc.rlogit + gr * kMaxBatch * E + i);
+        lg[i] = (float)((double)(long long)v * (1.0 / kRlogitScale));
       }
       for (int i = tid; i < n * TOPK; i += kThreads) F.topk_id[i / TOPK][i % TOPK] = i % TOPK;  // valid ids
       if (tid == 0) F.n_ue = 0;
@@ -1722,7 +1725,6 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     static_assert(sizeof(StepArgs) % 4 == 0, "word copy");
     for (int i = tid; i < (int)(sizeof(StepArgs) / 4); i += kBlockThreads) dst[i] = src[i];
   }
-  for (int i = tid; i < 2 * kMmaUnits * 128; i += kBlockThreads) F.mma_acc[i] = 0.f;
   const int n = a.n;
   if (tid == 0) {
     Ctx& c = F.ctx;
@@ -1752,7 +1754,9 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     c.tr_rl = a.trace ? c.tr_attn + (size_t)a.n_layers * n * M::QD : nullptr;
     c.tr_tk = a.trace ? c.tr_rl + (size_t)a.n_layers * n * S::E : nullptr;
     c.tr_fin = a.trace ? c.tr_tk + (size_t)a.n_layers * n * 2 * S::TOPK : nullptr;
-    c.tm = (a.timing && blockIdx.x == 0) ? a.timing : nullptr;
+    c.tm = a.timing ? a.timing + (size_t)blockIdx.x * (16 * a.n_layers + 2) : nullptr;
+    c.ring_log = a.timing ? a.timing + (size_t)c.G * (16 * a.n_layers + 2) + (size_t)blockIdx.x * 2 * kRingLog
+                          : nullptr;
     // attention work units: (row, kv head, chunk), row-major
     int acc = 0;
     for (int b = 0; b < n; ++b) {
@@ -1762,7 +1766,6 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     F.unit_start[n] = acc;
     F.kc = 0;
     F.prod_k = 0;
-    F.mma_flip = 0;
     F.route_gen = 0;
     F.n_merge = 0;
     F.abort = 0;

@@ -1,19 +1,20 @@
 // mk_decode_step_static: the decode step for callers that cannot allocate
-// device memory.  It launches the same decode kernel as mk_decode_step, but
-// everything the library would otherwise cudaMalloc (the per-layer pointer
-// table, the RoPE table and the kernel's scratch: residual stream, attention
-// partials, router partials, expert activations, argmax candidates, barrier
-// counters and the error word) lives in one file-scope device array of
-// kStaticBytes bytes.  Every GPU that loads the library holds that array
-// until the process exits.  Weights (the logical tensors for embedding, norms
-// and router, and the packed copy of the linear layers made by
-// mk_pack_weights), the KV cache and its block table, tokens and outputs are
-// the caller's memory.
+// device memory -- a host that hands the library a fixed memory budget from
+// its own allocator, or a loop that must not take the device-wide
+// synchronisation a cudaMalloc / cudaFree can bring.  It launches the same
+// decode kernel as mk_decode_step, but everything the library would
+// otherwise cudaMalloc (the per-layer pointer table, the RoPE table and the
+// kernel's scratch: residual stream, attention partials, router partials,
+// expert activations, argmax candidates, barrier counters and the error
+// word) lives in one file-scope device array of kStaticBytes bytes.  Every
+// GPU that loads the library holds that array until the process exits.
+// Weights (the logical tensors for embedding, norms and router, and the
+// packed copy of the linear layers made by mk_pack_weights), the KV cache
+// and its block table, tokens and outputs are the caller's memory.
 #include <cmath>
 #include <cstring>
 #include <mutex>
 #include <string>
-#include <vector>
 
 #include "mk_internal.h"
 
@@ -24,19 +25,25 @@ constexpr size_t kStaticBytes = size_t(8) << 20;  // 8 MiB per device
 constexpr int kStaticRopePositions = 8192;         // positions the RoPE table covers
 constexpr int kMaxDevices = 64;
 constexpr int kMaxStaticLayers = 128;
+constexpr int kMaxStaticHalf = 64;                 // head_dim / 2 of the compiled shapes
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 
-// Set-up state per device: the array's device address and which RoPE table
-// (theta, head_dim) it currently holds.
+// Set-up state per device: the array's device address and the RoPE table
+// (theta, head_dim) and layer table it currently holds.  Host copies live in
+// static storage, so a call allocates no memory on the host either.
 struct DeviceState {
   bool ready = false;
   char* base = nullptr;
   float rope_theta = 0.f;
   int head_dim = 0;
+  int n_layers = 0;
+  size_t off_layers = 0;
+  LayerW table[kMaxStaticLayers];
 };
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+float2 g_rope_host[(size_t)kStaticRopePositions * kMaxStaticHalf];  // guarded by g_mu
 
 size_t rope_bytes(int head_dim) {
   return sizeof(float2) * (size_t)kStaticRopePositions * (head_dim / 2);
@@ -44,11 +51,12 @@ size_t rope_bytes(int head_dim) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Once per device (with that device current): resolve the array's device
-// address; (re)build the RoPE table when theta or head_dim changes.  The
-// table upload is a synchronous copy, so the first call on a device, or the
-// first after a theta / head_dim change, must not run under stream capture.
-int setup(int dev, const mk_model_desc& d, char** base) {
+// With device `dev` current: the first call resolves the array's device
+// address.  When the RoPE parameters or the layer table differ from what the
+// array holds, the device is first drained (an earlier call, on any stream,
+// may still be reading them) and the tables are rewritten with synchronous
+// copies.  Calls with the same model reach neither step.
+int setup(int dev, const mk_model_desc& d, const LayerW* layers, size_t off_layers, char** base) {
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& s = g_dev[dev];
   if (!s.ready) {
@@ -59,19 +67,36 @@ int setup(int dev, const mk_model_desc& d, char** base) {
     s.base = static_cast<char*>(ptr);
     s.ready = true;
   }
-  if (s.rope_theta != d.rope_theta || s.head_dim != d.head_dim) {
-    const int half = d.head_dim / 2;
-    std::vector<float2> rope((size_t)kStaticRopePositions * half);
-    for (int p = 0; p < kStaticRopePositions; ++p)
-      for (int i = 0; i < half; ++i) {
-        const double ang = (double)p * std::pow((double)d.rope_theta, -2.0 * i / d.head_dim);
-        rope[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
-      }
-    cudaError_t e = cudaMemcpy(s.base, rope.data(), rope_bytes(d.head_dim), cudaMemcpyHostToDevice);
+  const bool rope_changed = s.rope_theta != d.rope_theta || s.head_dim != d.head_dim;
+  const bool table_changed = rope_changed || s.n_layers != d.n_layers || s.off_layers != off_layers ||
+                             std::memcmp(s.table, layers, sizeof(LayerW) * d.n_layers) != 0;
+  if (table_changed) {
+    cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess)
-      return host_fail(MK_ERR_CUDA, (std::string("RoPE table upload: ") + cudaGetErrorString(e)).c_str());
-    s.rope_theta = d.rope_theta;
-    s.head_dim = d.head_dim;
+      return host_fail(MK_ERR_CUDA, (std::string("waiting for earlier calls: ") + cudaGetErrorString(e)).c_str());
+    if (rope_changed) {
+      const int half = d.head_dim / 2;
+      for (int p = 0; p < kStaticRopePositions; ++p)
+        for (int i = 0; i < half; ++i) {
+          const double ang = (double)p * std::pow((double)d.rope_theta, -2.0 * i / d.head_dim);
+          g_rope_host[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        }
+      e = cudaMemcpy(s.base, g_rope_host, rope_bytes(d.head_dim), cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) {
+        s.rope_theta = 0.f;  // unknown contents: rebuilt by the next call
+        return host_fail(MK_ERR_CUDA, (std::string("RoPE table upload: ") + cudaGetErrorString(e)).c_str());
+      }
+      s.rope_theta = d.rope_theta;
+      s.head_dim = d.head_dim;
+    }
+    std::memcpy(s.table, layers, sizeof(LayerW) * d.n_layers);
+    e = cudaMemcpy(s.base + off_layers, s.table, sizeof(LayerW) * d.n_layers, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+      s.n_layers = 0;
+      return host_fail(MK_ERR_CUDA, (std::string("layer table upload: ") + cudaGetErrorString(e)).c_str());
+    }
+    s.n_layers = d.n_layers;
+    s.off_layers = off_layers;
   }
   *base = s.base;
   return MK_OK;
@@ -143,8 +168,9 @@ extern "C" MK_API int mk_decode_step_static(
                      ("model needs " + std::to_string(need) + " bytes of static scratch; the array holds " +
                       std::to_string(kStaticBytes)).c_str());
 
+  if (d->head_dim / 2 > kMaxStaticHalf) return host_fail(MK_ERR_UNSUPPORTED, "head_dim above 128");
   char* base = nullptr;
-  if (int r = setup(dev, *d, &base)) return r;
+  if (int r = setup(dev, *d, layers, off_layers, &base)) return r;
   e = cudaFuncSetAttribute(kern.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kern.smem_bytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kern.fn, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxL1);
@@ -191,8 +217,6 @@ extern "C" MK_API int mk_decode_step_static(
   e = cudaMemsetAsync(a.sc.merge_cnt, 0, sizeof(int32_t) * kMaxBatch * d->n_kv_heads, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(a.sc.sync, 0, sizeof(uint32_t) * 128, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(a.sc.err, 0, sizeof(int32_t) * 4, st);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(base + off_layers, layers, sizeof(LayerW) * d->n_layers, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return host_fail(MK_ERR_CUDA, cudaGetErrorString(e));
   void* args[] = {&a};
   e = cudaLaunchCooperativeKernel(kern.fn, dim3(grid), dim3(kBlockThreads), args,

@@ -22,6 +22,7 @@ import torch
 from . import _lib as L
 
 MAX_PREFILL = 4096
+RING_LOG = 1024      # ring items per block the timing record logs
 
 
 def _ptr(t) -> int:
@@ -105,6 +106,24 @@ class Engine:
     def release(self, seq_id: int):
         L.mk_seq_release(self.ctx, seq_id)
 
+    # ---- KV transfers and page sharing
+    def kv_write(self, seq_id: int, start_pos: int, kv: torch.Tensor):
+        """Store K/V for positions start_pos .. start_pos+n-1: kv is a CUDA
+        bfloat16 tensor [n_layers, n, 2, n_kv_heads, head_dim]."""
+        assert kv.dtype == torch.bfloat16 and kv.is_cuda and kv.is_contiguous()
+        L.mk_kv_write(self.ctx, seq_id, start_pos, kv.shape[1], _ptr(kv), self.stream)
+
+    def kv_read(self, seq_id: int, start_pos: int, n: int) -> torch.Tensor:
+        s = self.shape
+        out = torch.empty((s.n_layers, n, 2, s.n_kv_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+        L.mk_kv_read(self.ctx, seq_id, start_pos, n, _ptr(out), self.stream)
+        return out
+
+    def fork(self, src_seq: int, dst_seq: int, n_tokens: int):
+        """Open dst_seq sharing the pages of src_seq's first n_tokens
+        positions (a multiple of 128)."""
+        L.mk_seq_fork(self.ctx, src_seq, dst_seq, n_tokens, self.stream)
+
     def seq_length(self, seq_id: int) -> int:
         return L.mk_seq_length(self.ctx, seq_id)
 
@@ -121,31 +140,61 @@ class Engine:
         L.mk_set_debug(self.ctx, L.MK_DBG_TRACE, 0, _ptr(self.trace), nbytes, 0)
 
     def enable_timing(self):
-        """Per-phase %globaltimer stamps of block 0 for each following launch."""
-        n = 16 * self.shape.n_layers + 2
-        self.timing = torch.zeros(n, dtype=torch.int64, device="cuda")
-        L.mk_set_debug(self.ctx, L.MK_DBG_TIMING, 0, _ptr(self.timing), 8 * n, 0)
+        """Per-phase %globaltimer stamps of every block for each following launch."""
+        grid = self.info()["grid"]
+        R = 16 * self.shape.n_layers + 2
+        self.timing = torch.zeros(grid * (R + 2 * RING_LOG), dtype=torch.int64, device="cuda")
+        L.mk_set_debug(self.ctx, L.MK_DBG_TIMING, 0, _ptr(self.timing), 8 * self.timing.numel(), 0)
 
-    def phase_times_us(self) -> dict:
-        """Durations (us) of the last timed launch, summed over layers: per
-        phase the activation staging, the rest of the block's own work, and the
-        wait at the following grid barrier."""
-        t = self.timing.cpu().numpy().astype("float64")
+    PHASES = ("qkv", "attention", "oproj", "route+gateup", "down")
+
+    def timing_stamps(self):
+        """The last timed launch's stamps as float64 ns [blocks, 16 * n_layers + 2]."""
+        R = 16 * self.shape.n_layers + 2
+        grid = self.timing.numel() // (R + 2 * RING_LOG)
+        return self.timing[:grid * R].view(grid, R).cpu().numpy().astype("float64")
+
+    def ring_log(self):
+        """The last timed launch's ring log as float64 ns [blocks, items, 2]
+        (issued, landed; 0 where no item)."""
+        R = 16 * self.shape.n_layers + 2
+        grid = self.timing.numel() // (R + 2 * RING_LOG)
+        return self.timing[grid * R:].view(grid, RING_LOG, 2).cpu().numpy().astype("float64")
+
+    def phase_times_us(self, layers=None) -> dict:
+        """Per-phase times (us) of the last timed launch, medians over
+        `layers` (default: the MoE layers).  For each phase, from the
+        release of the previous grid barrier:
+          stage      block 0's activation staging;
+          work_med   the median block's time until it arrived at the barrier;
+          work_max   the last block's (the critical path);
+          barrier    from the last arrival to the first release;
+          span       from one release to the next.
+        Also lm_head (from the last release) and the launch total."""
+        import numpy as np
+        t = self.timing_stamps()
         Ln = self.shape.n_layers
-        names = ["qkv", "attention", "oproj", "route+gateup", "down"]
-        out = {k: {"stage": 0.0, "work": 0.0, "barrier": 0.0} for k in names}
-        prev = t[0]
+        if layers is None:
+            layers = range(self.shape.n_dense, Ln) if self.shape.n_dense < Ln else range(Ln)
+        per = {k: {"stage": [], "work_med": [], "work_max": [], "barrier": [], "span": []} for k in self.PHASES}
+        prev = t[:, 0]
         for l in range(Ln):
-            for p, k in enumerate(names):
-                st, end, rel = t[1 + 16 * l + 3 * p: 4 + 16 * l + 3 * p]
-                if st == 0:
-                    st = prev
-                out[k]["stage"] += (st - prev) / 1e3
-                out[k]["work"] += (end - st) / 1e3
-                out[k]["barrier"] += (rel - end) / 1e3
+            for p, k in enumerate(self.PHASES):
+                base = 1 + 16 * l + 3 * p
+                st, done, rel = t[:, base], t[:, base + 1], t[:, base + 2]
+                st = np.where(st == 0, prev, st)
+                if l in layers:
+                    start = prev.max()
+                    per[k]["stage"].append((st[0] - prev[0]) / 1e3)
+                    per[k]["work_med"].append(float(np.median(done - prev)) / 1e3)
+                    per[k]["work_max"].append((done.max() - start) / 1e3)
+                    per[k]["barrier"].append((rel.min() - done.max()) / 1e3)
+                    per[k]["span"].append((rel.max() - start) / 1e3)
                 prev = rel
-        out["lm_head"] = (t[1 + 16 * Ln] - prev) / 1e3
-        out["total"] = (t[1 + 16 * Ln] - t[0]) / 1e3
+        out = {k: {m: round(float(np.median(v)), 3) for m, v in d.items()} for k, d in per.items()}
+        out["lm_head"] = round(float((t[:, 1 + 16 * Ln].max() - prev.max()) / 1e3), 3)
+        out["total"] = round(float((t[:, 1 + 16 * Ln].max() - t[:, 0].min()) / 1e3), 3)
+        out["layer_median"] = round(sum(out[k]["span"] for k in self.PHASES), 3)
         return out
 
     def disable_trace(self):
@@ -179,6 +228,57 @@ class Engine:
             self.close()
         except Exception:
             pass
+
+
+class PrefixCache:
+    """Prefix reuse on the page pool: finished sequences stay in the cache
+    with their pages; a new prompt that starts with a cached sequence's
+    tokens opens its sequence by sharing the longest common prefix in whole
+    128-token pages (mk_seq_fork: no K/V is recomputed or copied) and
+    prefills only the rest.  Entries are evicted least recently used first
+    when the cache holds `capacity` sequences.  The cache owns the sequence
+    ids it keeps; callers must not reuse an id the cache holds.
+
+    The workload is the one "rec Megakernel and Tempo9 Compared", §1 (Prefix
+    cache) measures: a second turn over the same 8,022-token prompt reuses
+    7,936 tokens (62 pages), and returning to a prompt after another one
+    reuses it again when its entry is still held."""
+
+    def __init__(self, engine: Engine, capacity: int = 4):
+        self.e = engine
+        self.capacity = capacity
+        self.entries: list = []      # [(seq_id, tokens as a host list)], most recent last
+
+    def _match(self, toks: list) -> tuple:
+        best, best_n = None, 0
+        for sid, et in self.entries:
+            n = 0
+            lim = min(len(et), len(toks) - 1)   # keep >= 1 token to prefill (it yields the next token)
+            while n < lim and et[n] == toks[n]:
+                n += 1
+            n = n // 128 * 128
+            if n > best_n:
+                best, best_n = sid, n
+        return best, best_n
+
+    def prefill(self, seq_id: int, tokens: torch.Tensor, out: Optional[torch.Tensor] = None):
+        """Open seq_id for `tokens` (int32 CUDA); returns (next-token device
+        tensor, reused token count)."""
+        toks = tokens.cpu().tolist()
+        src, n = self._match(toks)
+        if src is not None:
+            self.e.fork(src, seq_id, n)
+            self.entries = [x for x in self.entries if x[0] != src] + [x for x in self.entries if x[0] == src]
+        out = self.e.prefill(seq_id, tokens[n:], start_pos=n, out=out)
+        return out, n
+
+    def keep(self, seq_id: int, tokens: list):
+        """Retain a finished sequence (its positions hold `tokens`) as an
+        entry; evicts the least recently used entry beyond capacity."""
+        self.entries.append((seq_id, list(tokens)))
+        while len(self.entries) > self.capacity:
+            sid, _ = self.entries.pop(0)
+            self.e.release(sid)
 
 
 @dataclasses.dataclass

@@ -100,7 +100,7 @@ def test_batch_of_16_matches_the_oracle_per_sequence(gpu_lib, tiny_int4):
         _, tro = orc.decode(kvs[s], nxt[s], lens[s])
         PR.compare_trace(rep, m, tr, tro, slice(s, s + 1), slice(0, 1), PR.tol_for(m), f"seq {s}", seq=s)
         PR.check_token(rep, int(toks[s].item()), int(tro["next_token"][-1]), float(tro["top2_margin"][-1]),
-                       f"seq {s}", seq=s, n_layers=m.n_layers)
+                       f"seq {s}", seq=s)
     assert not rep.failures, rep
     eng.close()
 
@@ -196,4 +196,121 @@ def test_grid_barrier_timeout_is_reported_and_the_context_recovers(gpu_lib, tiny
     eng.sync()
     ref, _ = _solo(m, w, p, 0)
     assert int(tok.item()) == ref[0]
+    eng.close()
+
+
+def test_kv_write_read_roundtrip_and_errors(gpu_lib, tiny_int4):
+    m, w = tiny_int4
+    eng = Engine(m, w, n_pages=4, max_ctx=1024, max_seqs=3)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    kv = (torch.randn((m.n_layers, 300, 2, m.n_kv_heads, m.head_dim), generator=g, device="cuda")
+          .to(torch.bfloat16))
+    eng.kv_write(0, 0, kv)                           # opens the sequence, takes 3 pages
+    assert eng.seq_length(0) == 300 and eng.info()["free_pages"] == 1
+    assert torch.equal(eng.kv_read(0, 0, 300).view(torch.int16), kv.view(torch.int16))
+    part = kv[:, 10:20].flip(0).contiguous()         # overwrite positions 10..19
+    eng.kv_write(0, 10, part)
+    got = eng.kv_read(0, 0, 300)
+    assert torch.equal(got[:, 10:20].view(torch.int16), part.view(torch.int16))
+    assert torch.equal(got[:, :10].view(torch.int16), kv[:, :10].view(torch.int16))
+    assert torch.equal(got[:, 20:].view(torch.int16), kv[:, 20:].view(torch.int16))
+    with pytest.raises(L.MKError) as e:              # a gap after the length
+        eng.kv_write(0, 301, kv[:, :1].contiguous())
+    assert e.value.code == L.MK_ERR_STATE
+    with pytest.raises(L.MKError) as e:              # needs 2 more pages, 1 left: nothing written
+        eng.kv_write(1, 0, kv[:, :200].contiguous())
+    assert e.value.code == L.MK_ERR_NO_PAGES and eng.seq_length(1) == -1
+    with pytest.raises(L.MKError) as e:
+        eng.kv_read(0, 290, 20)                      # past the length
+    assert e.value.code == L.MK_ERR_STATE
+    eng.close()
+
+
+def test_fork_shares_pages_and_gives_the_same_tokens(gpu_lib, tiny_int4):
+    m, w = tiny_int4
+    eng = Engine(m, w, n_pages=8, max_ctx=1024, max_seqs=3)
+    a = _prompt(m, 300, 0)
+    ta = eng.prefill(0, a).clone()
+    eng.sync()
+    free0 = eng.info()["free_pages"]                 # 8 - 3
+    eng.fork(0, 1, 256)                              # shares 2 pages, takes none
+    assert eng.info()["free_pages"] == free0 and eng.seq_length(1) == 256
+    tb = eng.prefill(1, a[256:], start_pos=256)      # the same positions, same launch grouping
+    eng.sync()
+    assert int(tb.item()) == int(ta.item())
+    assert torch.equal(eng.kv_read(1, 0, 300).view(torch.int16), eng.kv_read(0, 0, 300).view(torch.int16))
+    with pytest.raises(L.MKError) as e:              # position 5 is in a shared page
+        eng.kv_write(0, 5, torch.zeros((m.n_layers, 1, 2, m.n_kv_heads, m.head_dim),
+                                       dtype=torch.bfloat16, device="cuda"))
+    assert e.value.code == L.MK_ERR_STATE
+    with pytest.raises(L.MKError) as e:              # not whole pages
+        eng.fork(0, 2, 200)
+    assert e.value.code == L.MK_ERR_INVALID_ARG
+    eng.release(0)                                   # the shared pages stay with sequence 1
+    assert eng.info()["free_pages"] == 8 - 3
+    tok = tb.clone()
+    eng.decode_step([1], tok, [300], tok)
+    eng.sync()
+    eng.release(1)
+    assert eng.info()["free_pages"] == 8
+    eng.close()
+
+
+def test_prefix_cache_a_a_b_a(gpu_lib, tiny_int4):
+    """The prefix-cache sequence of turns A, A, B, A: the second and the last
+    turn over prompt A reuse its whole pages (512 of 600 tokens) and give the
+    tokens a cold prefill gives."""
+    from moe_decode_megakernel_persistent_gb300.engine import PrefixCache
+    m, w = tiny_int4
+    eng = Engine(m, w, n_pages=32, max_ctx=1024, max_seqs=8)
+    A, B = _prompt(m, 600, 0), _prompt(m, 600, 1)
+    cold = {}
+    for name, p in (("A", A), ("B", B)):
+        t = eng.prefill(7, p)
+        cold[name] = int(t.item())
+        eng.release(7)
+    pc = PrefixCache(eng, capacity=2)
+    reused = []
+    for sid, (name, p) in enumerate((("A", A), ("A", A), ("B", B), ("A", A))):
+        out, n = pc.prefill(sid, p)
+        eng.sync()
+        reused.append(n)
+        assert int(out.item()) == cold[name], (sid, name)
+        pc.keep(sid, p.cpu().tolist())
+    assert reused == [0, 512, 0, 512]
+    eng.close()
+
+
+def test_timing_stamps_cover_every_phase_of_every_block(gpu_lib, tiny_int4):
+    """MK_DBG_TIMING: every block stamps its start, each layer's phases (work
+    done, barrier released; staging done where the phase stages) and the
+    end, in increasing order; a barrier is released only after every block
+    arrived."""
+    m, w = tiny_int4
+    eng = Engine(m, w, n_pages=8, max_ctx=256, max_seqs=2)
+    tok = eng.prefill(0, _prompt(m, 40, 0))
+    eng.enable_timing()
+    eng.decode_step([0], tok, [40], tok)
+    eng.sync()
+    t = eng.timing_stamps()
+    grid = eng.info()["grid"]
+    assert t.shape[0] == grid
+    for b in range(grid):
+        seq = [t[b, 0]]
+        for l in range(m.n_layers):
+            for p in range(5):
+                base = 1 + 16 * l + 3 * p
+                if p != 1:                                # attention stages nothing
+                    seq.append(t[b, base])
+                seq += [t[b, base + 1], t[b, base + 2]]
+        seq.append(t[b, 1 + 16 * m.n_layers])
+        seq = np.asarray(seq)
+        assert (seq > 0).all(), b
+        assert (np.diff(seq) >= 0).all(), b
+    for l in range(m.n_layers):
+        for p in range(5):
+            base = 1 + 16 * l + 3 * p
+            assert t[:, base + 2].min() >= t[:, base + 1].max()
+    pt = eng.phase_times_us()
+    assert pt["total"] > 0 and all(pt[k]["span"] >= 0 for k in Engine.PHASES)
     eng.close()
