@@ -27,6 +27,7 @@
 // the layer's routing.  The compute warps wait on a stage's "full" mbarrier,
 // form their dot products from shared memory and release the stage.
 #include <cfloat>
+#include <cstddef>
 #include <climits>
 #include <type_traits>
 #include "mk_device.cuh"
@@ -69,7 +70,9 @@ struct Fixed {
   uint32_t nslw[kMaxRowsPerBlock];  // raw slice of the post-attention norm weights
   float red[kThreads];
   unsigned long long best_key[kMaxBatch];  // lm_head argmax per row (argmax_key)
-  float mma_part[kWarps * 128];            // tensor-core path: each warp's partial of its unit
+  // tensor-core path: each warp's partial of its unit, read and written as
+  // float4 (16-byte aligned whatever precedes it)
+  alignas(16) float mma_part[kWarps * 128];
   int unit_start[kMaxBatch + 1];
   int upages[2][64];      // pool pages of this block's attention units (streaming warp)
   float rnorm[kMaxBatch];
@@ -81,6 +84,7 @@ struct Fixed {
   int n_merge, merge_job[kMaxOwnUnits][4];  // attention merges this block owes: (b, g, h0, h1)
 };
 constexpr int kActOffset = (sizeof(Fixed) + 127) / 128 * 128;
+static_assert(offsetof(Fixed, mma_part) % 16 == 0, "float4 access to the tensor-core partials");
 
 __device__ __forceinline__ Fixed& fixed() {
   extern __shared__ __align__(128) uint8_t smem_dyn[];
