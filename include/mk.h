@@ -266,10 +266,11 @@ MK_API int mk_sync(mk_ctx* ctx, void* stream);
                               with k = 0 staging done, 1 phase work done, 2 grid
                               barrier released; then [1 + 16*n_layers] lm_head done.
                               After the grid's records, each block's ring log of
-                              2048 stamps at [grid * R + b * 2048]: [2k] the time
-                              the block's k-th weight / KV tile was issued, [2k + 1]
-                              the time the compute warps found it landed (k < 1024).
-                              Size: 8 * grid * (R + 2048) bytes (grid: mk_get_info).
+                              3072 stamps at [grid * R + b * 3072]: for its k-th
+                              weight / KV tile (k < 1024) [3k] issued, [3k + 1]
+                              found landed by the compute warps, [3k + 2] released
+                              by warp 0.  Size: 8 * grid * (R + 3072) bytes (grid:
+                              mk_get_info).
                               Not combinable with MK_DBG_TRACE. */
 MK_API int mk_set_debug(mk_ctx* ctx, uint32_t flags, uint32_t arg, void* trace_dev,
                         size_t trace_bytes, uint32_t spin_limit_us);

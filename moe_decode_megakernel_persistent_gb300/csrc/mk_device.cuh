@@ -62,6 +62,10 @@ __device__ __forceinline__ float4 ld_aux4(const void* p, size_t i4) {
   }
 }
 
+// Fixed-point values (units of 2^-32) of the router sums; the scale is a
+// power of two, so the conversions round only once.
+__device__ __forceinline__ long long to_fixed(float v) { return __float2ll_rn(v * kFixScale); }
+__device__ __forceinline__ float from_fixed(long long q) { return __ll2float_rn(q) * kFixUnit; }
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -129,7 +133,7 @@ __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(k
 // up when another block has recorded an error, or after spin_limit_ns, and
 // then records MK_ERR_BARRIER_TIMEOUT; the caller skips to the exit path.
 // `ok` is a shared-memory word used to broadcast the outcome.
-__device__ __forceinline__ bool grid_barrier(const StepArgs& a, uint32_t& k, volatile int* ok_word) {
+__device__ __noinline__ bool grid_barrier(const StepArgs& a, uint32_t& k, volatile int* ok_word) {
   csync();
   if (threadIdx.x == 0) {
     ++k;
@@ -188,10 +192,11 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the given phase parity: gives up (returns false) when
-// `abort` is set, an error is recorded, or after limit_ns.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, const volatile int* abort,
-                                          int32_t* err, uint64_t limit_ns, int site_detail) {
-  if (mbar_try(b, parity)) return true;
+// `abort` is set, an error is recorded, or after limit_ns.  The first test is
+// inline; the spin loop is one out-of-line copy for every call site (the
+// kernel's code per layer is kept small: it is fetched again every layer).
+__device__ __noinline__ bool mbar_wait_loop(uint64_t* b, uint32_t parity, const volatile int* abort, int32_t* err,
+                                            uint64_t limit_ns, int site_detail) {
   uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try(b, parity)) return true;
@@ -203,6 +208,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, const vo
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, const volatile int* abort,
+                                          int32_t* err, uint64_t limit_ns, int site_detail) {
+  if (mbar_try(b, parity)) return true;
+  return mbar_wait_loop(b, parity, abort, err, limit_ns, site_detail);
 }
 // Bounded wait that ignores abort and errors: used on the exit path, where
 // copies still in flight into shared memory must land before the block ends.

@@ -185,8 +185,8 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
   if ((c->dbg_flags & MK_DBG_TRACE) && c->trace_bytes < mk_trace_bytes(&c->d, n))
     return fail(MK_ERR_INVALID_ARG, "trace buffer is smaller than mk_trace_bytes(rows)");
   if ((c->dbg_flags & MK_DBG_TIMING) &&
-      c->trace_bytes < sizeof(uint64_t) * (size_t)c->grid * (16 * (size_t)c->d.n_layers + 2 + 2 * kRingLog))
-    return fail(MK_ERR_INVALID_ARG, "timing buffer is smaller than 8 * grid * (16 * n_layers + 2 + 2048) bytes");
+      c->trace_bytes < sizeof(uint64_t) * (size_t)c->grid * (16 * (size_t)c->d.n_layers + 2 + 3 * kRingLog))
+    return fail(MK_ERR_INVALID_ARG, "timing buffer is smaller than 8 * grid * (16 * n_layers + 2 + 3072) bytes");
   StepArgs a;
   std::memset(&a, 0, sizeof(a));
   std::vector<std::pair<int, int32_t>> taken;  // (slot, page) handed out by this call

@@ -21,7 +21,8 @@ constexpr int kRlogitGroups = 8;     // copies of the router-logit sums (less at
 // 2^-32): integer addition is associative, so the sum, and with it the expert
 // selection, is the same bits whatever order the blocks' atomics land in.
 // Range: |sum| < 2^31.
-constexpr double kRlogitScale = 4294967296.0;
+constexpr float kFixScale = 4294967296.f;       // 2^32
+constexpr float kFixUnit = 2.3283064365386963e-10f;  // 2^-32
 constexpr int kRingLog = 1024;      // ring items per block whose issue / arrival times MK_DBG_TIMING logs
 constexpr int kMaxUpd = 64;          // block-table updates carried by one launch
 constexpr int kMaxRowsPerBlock = 32; // hidden rows owned by one block (hidden / grid)
@@ -71,7 +72,7 @@ struct Scratch {
   float* attn;       // [kMaxBatch][n_heads*hd] merged attention output
   float* part;       // [max_units][gqa][hd + 2] attention partials (m, l, o[hd])
   long long* rlogit; // [kRlogitGroups][kMaxBatch][E] router logits before the RMS scale, fixed
-                     // point (kRlogitScale): block partials summed into one of kRlogitGroups
+                     // point: block partials summed into one of kRlogitGroups
                      // copies (block id mod groups)
   float* act;        // [kMaxBatch][top_k][Fe] expert activations
   float* dact;       // [kMaxBatch][Fd] dense-MLP activations

@@ -48,7 +48,8 @@ struct Ctx {
   bool tc;         // tensor-core GEMV (plain fp32 staging) for this launch
   float *tr_x, *tr_attn, *tr_rl, *tr_tk, *tr_fin;
   uint64_t* tm;    // this block's timing stamps (thread 0 writes them) or null
-  uint64_t* ring_log;  // this block's ring log: [2k] item k issued, [2k + 1] item k landed (or null)
+  uint64_t* ring_log;  // this block's ring log: [3k] item k issued, [3k + 1] landed (thread 0 saw it),
+                       // [3k + 2] released by warp 0 (or null)
 };
 
 struct Fixed {
@@ -130,12 +131,13 @@ __device__ __forceinline__ const uint8_t* ring_acquire(uint32_t k) {
   const int s = (int)(k % (uint32_t)F.ctx.ns);
   const uint32_t par = (k / (uint32_t)F.ctx.ns) & 1u;
   mbar_wait(&F.full[s], par, &F.abort, F.args.sc.err, F.args.spin_limit_ns, (int)k);
-  if (F.ctx.ring_log && threadIdx.x == 0 && k < (uint32_t)kRingLog) F.ctx.ring_log[2 * k + 1] = globaltimer();
+  if (F.ctx.ring_log && threadIdx.x == 0 && k < (uint32_t)kRingLog) F.ctx.ring_log[3 * k + 1] = globaltimer();
   return F.ctx.ring + (size_t)s * STAGE;
 }
 __device__ __forceinline__ void ring_release(uint32_t k) {
   Fixed& F = fixed();
   __syncwarp();
+  if (F.ctx.ring_log && threadIdx.x == 0 && k < (uint32_t)kRingLog) F.ctx.ring_log[3 * k + 2] = globaltimer();
   if ((threadIdx.x & 31) == 0) mbar_arrive(&F.empty[k % (uint32_t)F.ctx.ns]);
 }
 
@@ -169,7 +171,7 @@ struct Producer {
     }
     stage = F.ctx.ring + (size_t)s * STAGE;
     bar = &F.full[s];
-    if (F.ctx.ring_log && k < (uint32_t)kRingLog) F.ctx.ring_log[2 * k] = globaltimer();
+    if (F.ctx.ring_log && k < (uint32_t)kRingLog) F.ctx.ring_log[3 * k] = globaltimer();
     return true;
   }
   __device__ __forceinline__ void copy(uint32_t off, const void* src, uint32_t bytes) {
@@ -497,7 +499,7 @@ struct Model {
   }
 
   template <int K, int RP, int T, class TK>
-  __device__ static __forceinline__ void run_mma(int ntask, const uint8_t* act_base, const TK& task) {
+  __device__ static __noinline__ void run_mma(int ntask, const uint8_t* act_base, const TK& task) {
     using Gv = Gemv<WDT, K>;
     constexpr int NGR = K / 64;
     constexpr int RB = Gv::ROW_BYTES, AS = plain_stride(K);
@@ -757,7 +759,8 @@ struct Model {
   // One tile of nt positions (K rows at kv, V rows at kv + TT * HD * 2,
   // 32-bit shared addresses): scores, softmax, values.  `o` is the value
   // warps' accumulator (rows g, g + 8 = dims, columns 2q, 2q + 1 = heads).
-  __device__ static __forceinline__ void att_tile(uint32_t kv, int nt, uint8_t* att, float (&o)[4]) {
+  __device__ static __noinline__ float4 att_tile(uint32_t kv, int nt, uint8_t* att, float4 ov) {
+    float o[4] = {ov.x, ov.y, ov.z, ov.w};
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, g = lane >> 2, q = lane & 3;
     float* sc = reinterpret_cast<float*>(att + AO_SC);
     uint16_t* pb = reinterpret_cast<uint16_t*>(att + AO_PB);
@@ -845,6 +848,7 @@ struct Model {
         mma16816(o, a0, a1, a2, a3, bl0, bl1);
       }
     }
+    return make_float4(o[0], o[1], o[2], o[3]);
   }
 
   __device__ static __noinline__ void attention(int l) {
@@ -921,11 +925,11 @@ struct Model {
         asm volatile("cp.async.commit_group;" ::: "memory");
       };
       if (rt1 < t1) stage_new(rt1, min(TT, t1 - rt1));
-      float o[4] = {0.f, 0.f, 0.f, 0.f};
+      float4 ov = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
       for (int tb = t0; tb < rt1; tb += TT, ++k) {
         const uint32_t st = smem_u32(ring_acquire<STAGE>(k));
-        att_tile(st, min(TT, rt1 - tb), att, o);
+        ov = att_tile(st, min(TT, rt1 - tb), att, ov);
         ring_release(k);
       }
 #pragma unroll 1
@@ -937,8 +941,9 @@ struct Model {
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
         csync();
-        att_tile(nt_base, nt, att, o);
+        ov = att_tile(nt_base, nt, att, ov);
       }
+      const float o[4] = {ov.x, ov.y, ov.z, ov.w};
       csync();
       if (u >= a.max_units) set_error(a.sc.err, MK_ERR_DEVICE_INDEX, SITE_UNIT, u);
       float* pu = a.sc.part + (size_t)min(u, a.max_units - 1) * GQA * PR;
@@ -1018,7 +1023,7 @@ struct Model {
 
   // Heads [h0, h1) of (b, g): log-sum-exp merge of the chunk partials into
   // the attention output, in chunk order.
-  __device__ static __forceinline__ void merge(int l, int b, int g, int nch, int h0, int h1) {
+  __device__ static __noinline__ void merge(int l, int b, int g, int nch, int h0, int h1) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
@@ -1117,6 +1122,12 @@ struct Model {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
     const Ctx& c = F.ctx;
+    // the residual rows this block adds to (its own rows of x), loaded in
+    // the same round trip as the attention output
+    for (int i = threadIdx.x; i < c.n * c.nr; i += kThreads) {
+      const int b = i / c.nr, t = i % c.nr;
+      F.hs[b][t] = __ldcg(a.sc.x + b * H + c.r0 + t);
+    }
     {
       const float* at = a.sc.attn;
       stage_block<MODE, WDT, QD, false>(
@@ -1136,7 +1147,7 @@ struct Model {
       const StepArgs* a; Fixed* F; int r0, lane;
       __device__ __forceinline__ ActRange acts(int) const { return {nullptr, 0, a->n}; }
       __device__ __forceinline__ void put(int t, int b, int, float v0, float) const {
-        const float hv = __ldcg(a->sc.x + b * H + r0 + t) + v0;
+        const float hv = F->hs[b][t] + v0;   // residual row staged with the attention output
         a->sc.h[b * H + r0 + t] = hv;
         F->hs[b][t] = hv;
       }
@@ -1157,7 +1168,7 @@ struct Model {
       // after the grid barrier every block sums the copies.  Integer sums do
       // not depend on the order of the additions, so every run and every
       // block get the same logits bit for bit.
-      const long long q = __double2ll_rn((double)s * kRlogitScale);
+      const long long q = to_fixed(s);
       atomicAdd(reinterpret_cast<unsigned long long*>(a.sc.rlogit + (c.bid % kRlogitGroups) * kMaxBatch * E + b * E + e),
                 (unsigned long long)q);
     }
@@ -1171,6 +1182,68 @@ struct Model {
   // streaming warp is told at once so the experts' weights start moving while
   // the norm is computed.  The softmax weights (renormalised over the
   // selection) are formed from the scaled logits.  Dense layers only norm.
+  // Routing of a one-row launch by warp 0 alone, with no block barrier: the
+  // logit sums, the top-k (ranks, ties to the lower id) and the entry tables,
+  // then the streaming warp is signalled.  The other warps go straight on to
+  // the post-attention staging, whose block barriers publish the tables.
+  __device__ static __forceinline__ void route_one(int l) {
+    Fixed& F = fixed();
+    const StepArgs& a = F.args;
+    const int lane = threadIdx.x & 31;
+    float* lg = &F.dots[0][0];
+    {
+      // every lane's loads in one round trip: experts lane and lane + 32
+      constexpr int EPL = (E + 31) / 32;
+      long long q[EPL][kRlogitGroups];
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+#pragma unroll
+        for (int gr = 0; gr < kRlogitGroups; ++gr)
+          q[j][gr] = lane + 32 * j < E ? __ldcg(a.sc.rlogit + gr * kMaxBatch * E + lane + 32 * j) : 0ll;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        unsigned long long v = 0ull;  // wrapping two's-complement sum
+#pragma unroll
+        for (int gr = 0; gr < kRlogitGroups; ++gr) v += (unsigned long long)q[j][gr];
+        if (lane + 32 * j < E) lg[lane + 32 * j] = from_fixed((long long)v);
+      }
+    }
+    __syncwarp();
+    for (int e = lane; e < E; e += 32) {
+      const float v = lg[e];
+      int rank = 0;
+#pragma unroll 8
+      for (int e2 = 0; e2 < E; ++e2) {
+        const float w = lg[e2];
+        rank += (w > v) || (w == v && e2 < e);
+      }
+      if (rank < TOPK) {
+        F.topk_id[0][rank] = e;
+        F.topk_w[0][rank] = v;  // partial logit for now
+      }
+    }
+    __syncwarp();
+    // one entry per slot, the distinct experts in increasing id order
+    if (lane < TOPK) {
+      const int my_e = F.topk_id[0][lane];
+      int pos = 0;
+#pragma unroll
+      for (int j = 0; j < TOPK; ++j) pos += F.topk_id[0][j] < my_e;
+      F.ent_b[pos] = 0;
+      F.ent_j[pos] = (uint8_t)lane;
+      F.ent_of[0][lane] = (uint8_t)pos;
+      F.ue_expert[pos] = (int16_t)my_e;
+      F.ue_start[pos] = (int16_t)pos;
+      F.ue_len[pos] = 1;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      F.n_ue = TOPK;
+      __threadfence_block();
+      F.route_gen = l + 1;
+    }
+  }
+
   __device__ static __noinline__ void route(int l) {
     Fixed& F = fixed();
     const StepArgs& a = F.args;
@@ -1178,6 +1251,10 @@ struct Model {
     const int tid = threadIdx.x;
     const bool moe = l >= a.n_dense;
     const int n = c.n;
+    if (moe && n == 1) {
+      if (tid < 32) route_one(l);
+      return;
+    }
     if (moe) {
       // partial logits into shared memory (F.dots is free between P3 and P5)
       float* lg = &F.dots[0][0];
@@ -1186,7 +1263,7 @@ struct Model {
 #pragma unroll
         for (int gr = 0; gr < kRlogitGroups; ++gr)
           v += (unsigned long long)__ldcg(a.sc.rlogit + gr * kMaxBatch * E + i);
-        lg[i] = (float)((double)(long long)v * (1.0 / kRlogitScale));
+        lg[i] = from_fixed((long long)v);
       }
       for (int i = tid; i < n * TOPK; i += kThreads) F.topk_id[i / TOPK][i % TOPK] = i % TOPK;  // valid ids
       if (tid == 0) F.n_ue = 0;
@@ -1267,7 +1344,7 @@ struct Model {
     MK_STAMP(c, l, 3, 0);
   }
   // Softmax weights of the selection, once the norm factor is known.
-  __device__ static __forceinline__ void route_weights(int l) {
+  __device__ static __noinline__ void route_weights(int l) {
     Fixed& F = fixed();
     const Ctx& c = F.ctx;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -1432,7 +1509,7 @@ struct Model {
         for (int kk = 0; kk < TOPK; ++kk) s = fmaf(F.topk_w[b][kk], F.dots[F.ent_of[b][kk]][rr], s);
       else
         s = F.dots[b][rr];
-      const float xv = __ldcg(a.sc.h + b * H + c.r0 + rr) + s;
+      const float xv = F.hs[b][rr] + s;   // this block's rows of h, kept since o_proj
       a.sc.x[b * H + c.r0 + rr] = xv;
       if (c.tr_x) c.tr_x[((size_t)l * n + b) * H + c.r0 + rr] = xv;
     }
@@ -1759,7 +1836,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     c.tr_tk = a.trace ? c.tr_rl + (size_t)a.n_layers * n * S::E : nullptr;
     c.tr_fin = a.trace ? c.tr_tk + (size_t)a.n_layers * n * 2 * S::TOPK : nullptr;
     c.tm = a.timing ? a.timing + (size_t)blockIdx.x * (16 * a.n_layers + 2) : nullptr;
-    c.ring_log = a.timing ? a.timing + (size_t)c.G * (16 * a.n_layers + 2) + (size_t)blockIdx.x * 2 * kRingLog
+    c.ring_log = a.timing ? a.timing + (size_t)c.G * (16 * a.n_layers + 2) + (size_t)blockIdx.x * 3 * kRingLog
                           : nullptr;
     // attention work units: (row, kv head, chunk), row-major
     int acc = 0;

@@ -143,7 +143,7 @@ class Engine:
         """Per-phase %globaltimer stamps of every block for each following launch."""
         grid = self.info()["grid"]
         R = 16 * self.shape.n_layers + 2
-        self.timing = torch.zeros(grid * (R + 2 * RING_LOG), dtype=torch.int64, device="cuda")
+        self.timing = torch.zeros(grid * (R + 3 * RING_LOG), dtype=torch.int64, device="cuda")
         L.mk_set_debug(self.ctx, L.MK_DBG_TIMING, 0, _ptr(self.timing), 8 * self.timing.numel(), 0)
 
     PHASES = ("qkv", "attention", "oproj", "route+gateup", "down")
@@ -151,15 +151,15 @@ class Engine:
     def timing_stamps(self):
         """The last timed launch's stamps as float64 ns [blocks, 16 * n_layers + 2]."""
         R = 16 * self.shape.n_layers + 2
-        grid = self.timing.numel() // (R + 2 * RING_LOG)
+        grid = self.timing.numel() // (R + 3 * RING_LOG)
         return self.timing[:grid * R].view(grid, R).cpu().numpy().astype("float64")
 
     def ring_log(self):
-        """The last timed launch's ring log as float64 ns [blocks, items, 2]
-        (issued, landed; 0 where no item)."""
+        """The last timed launch's ring log as float64 ns [blocks, items, 3]
+        (issued, landed, released by warp 0; 0 where no item)."""
         R = 16 * self.shape.n_layers + 2
-        grid = self.timing.numel() // (R + 2 * RING_LOG)
-        return self.timing[grid * R:].view(grid, RING_LOG, 2).cpu().numpy().astype("float64")
+        grid = self.timing.numel() // (R + 3 * RING_LOG)
+        return self.timing[grid * R:].view(grid, RING_LOG, 3).cpu().numpy().astype("float64")
 
     def phase_times_us(self, layers=None) -> dict:
         """Per-phase times (us) of the last timed launch, medians over

@@ -45,6 +45,12 @@ from moe_decode_megakernel_persistent_gb300.engine import Engine
 
 TOPK_MARGIN = 1e-3
 TOKEN_MARGIN = 0.05
+# The K/V check pins WHERE the kernel wrote (page and slot): a value in the
+# wrong place differs from the oracle's by a relative error of about sqrt(2).
+# K and V are projections of the normalised hidden state and carry a few
+# times its relative error (up to about 1e-2 at the deep layers of a short
+# full-depth run), so the bound sits between the two.
+KV_TOL = 0.1
 
 
 def tol_for(m) -> float:
@@ -190,12 +196,12 @@ def oracle_kv(kv, start: int, n: int) -> torch.Tensor:
     return torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
 
 
-def check_kv(rep: Report, got: torch.Tensor, want: torch.Tensor, tag: str, positions: int, tol: float):
+def check_kv(rep: Report, got: torch.Tensor, want: torch.Tensor, tag: str, positions: int, tol: float = KV_TOL):
     """The K/V the GPU wrote for each (layer, position) equal the oracle's
-    within the parity tolerance (relative L2 over the position's K and V of
-    every kv head).  A value written to the wrong page or slot differs
-    wholesale (relative error about 1), so this pins the page / slot indices;
-    equal bf16 values are counted as well (the rest are rounding flips)."""
+    within KV_TOL (relative L2 over the position's K and V of every kv head):
+    a value written to the wrong page or slot differs wholesale, so this pins
+    the page / slot indices.  The largest error is reported, and so is the
+    count of unequal bf16 values (rounding flips)."""
     g = got.float().cpu().numpy().astype(np.float64)
     w = want.float().cpu().numpy().astype(np.float64)
     Ln, n = g.shape[0], g.shape[1]
@@ -257,7 +263,7 @@ def run_single(m, prompt_len: int, n_decode: int, *, seed_seq: int = 0, eng: Eng
             rep.failures.append(f"prefill final logits rel_l2 {e:.3e}")
     if teacher:
         check_kv(rep, eng.kv_read(seq_id, prompt_len - rows, rows), oracle_kv(kv, prompt_len - rows, rows),
-                 "prefill", rows, tol)
+                 "prefill", rows)
         eng.kv_write(seq_id, prompt_len - rows, oracle_kv(kv, prompt_len - rows, rows))
     # teacher-forced decode on the oracle's tokens
     cur = tok_o
@@ -274,7 +280,7 @@ def run_single(m, prompt_len: int, n_decode: int, *, seed_seq: int = 0, eng: Eng
         compare_trace(rep, m, tg, tr_o, slice(0, 1), slice(0, 1), tol, f"step {i}", key)
         check_token(rep, int(tout.item()), nxt_o, float(tr_o["top2_margin"][-1]), f"step {i}", key)
         if teacher:
-            check_kv(rep, eng.kv_read(seq_id, pos, 1), oracle_kv(kv, pos, 1), f"step {i}", 1, tol)
+            check_kv(rep, eng.kv_read(seq_id, pos, 1), oracle_kv(kv, pos, 1), f"step {i}", 1)
             eng.kv_write(seq_id, pos, oracle_kv(kv, pos, 1))
         cur = nxt_o
     eng.disable_trace()
