@@ -182,7 +182,17 @@ MK_API int mk_kv_alloc(mk_ctx* ctx, int32_t n_pages);
  * equal the sequence's current length (0 starts a new sequence).
  * tokens_dev: device int32[n].  out_token_dev: device int32[1] that receives
  * the greedy next token after the last position (may be NULL).
- * The chunk runs as launches of up to max_batch positions each.
+ * A chunk of up to 16 positions runs as one launch of the decode kernel.  A
+ * longer chunk runs the model over all of its positions at once, layer by
+ * layer: the projections as tensor-core GEMMs over the chunk's rows (cuBLAS,
+ * fp32 accumulation; activations split into two 16-bit parts; int4 weights
+ * widened exactly to fp16, bf16 weights used in place), attention, norms,
+ * routing, the grouping of rows by expert and the residuals as the library's
+ * kernels.  This path takes its pages up front, makes a workspace of about
+ * 1.2 GB (Flint shape; kept by the context) on its first use, and waits for
+ * the stream once per MoE layer (the expert GEMMs are sized on the host from
+ * the routing counts), so the call returns only when the chunk's last layer
+ * is enqueued.
  * Errors: INVALID_ARG, STATE, NO_PAGES (nothing is launched then), CUDA. */
 MK_API int mk_prefill_chunk(mk_ctx* ctx, int32_t seq_id, const int32_t* tokens_dev,
                             int32_t n, int32_t start_pos, int32_t* out_token_dev,

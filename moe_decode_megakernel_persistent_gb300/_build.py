@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
               "-I" + CSRC]
-SOURCES = ["mk_kernel.cu", "mk_host.cpp", "mk_static.cu", "mk_pack.cu", "mk_kv.cu"]
+SOURCES = ["mk_kernel.cu", "mk_host.cpp", "mk_static.cu", "mk_pack.cu", "mk_kv.cu", "mk_prefill.cu"]
 
 
 def _nvcc() -> str:
@@ -68,7 +68,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    # cuBLAS (the chunked prefill's GEMMs) is found through the toolkit's
+    # library directory
+    cudalib = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-lcublas",
+           "-Xlinker", "-rpath=" + cudalib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")

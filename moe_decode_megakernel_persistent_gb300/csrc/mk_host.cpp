@@ -79,6 +79,8 @@ struct mk_ctx {
   size_t trace_bytes = 0;
   uint64_t spin_limit_ns = 1000000000ull;
   int last_chunk = 0, last_units = 0;
+  std::vector<LayerW> layers_host;   // the layer table (for the chunked prefill)
+  PrefillWork* prefill = nullptr;    // chunked-prefill workspace, made on first use
 };
 
 namespace {
@@ -449,6 +451,8 @@ MK_API int mk_create(const mk_model_desc* d, const mk_weights* w, mk_ctx** out) 
       for (int k = 0; k < NPK; ++k) lw[l].pk[k] = c->packed_dev + pl.layer[l][k];
     c->lm_pk = c->packed_dev + pl.lm;
   }
+  c->layers_host = lw;
+  if (int r = prefill_setup_attributes(*d)) return bail(r);
   e = cudaMalloc(&c->layers_dev, sizeof(LayerW) * d->n_layers);
   if (e != cudaSuccess) return bail(fail(MK_ERR_CUDA, std::string("cudaMalloc(layers): ") + cudaGetErrorString(e)));
   e = cudaMemcpy(c->layers_dev, lw.data(), sizeof(LayerW) * d->n_layers, cudaMemcpyHostToDevice);
@@ -508,6 +512,83 @@ MK_API int mk_kv_alloc(mk_ctx* c, int32_t n_pages) {
   return MK_OK;
 }
 
+// A chunk of more than kMaxBatch positions: pages for all of it are taken
+// and entered in the block table, then mk_prefill.cu runs the model over the
+// chunk's rows layer by layer.
+static int prefill_gemm_chunk(mk_ctx* c, int32_t seq_id, const int32_t* tokens_dev, int32_t n, int32_t start_pos,
+                              int32_t* out_token_dev, cudaStream_t st) {
+  Seq& q = c->seqs[seq_id];
+  const int rows_traced = n - ((n - 1) / kMaxBatch) * kMaxBatch;  // what a launch-by-launch prefill leaves
+  if ((c->dbg_flags & MK_DBG_TRACE) && c->trace_bytes < mk_trace_bytes(&c->d, rows_traced))
+    return fail(MK_ERR_INVALID_ARG, "trace buffer is smaller than mk_trace_bytes(rows)");
+  const int have = (int)q.pages.size();
+  const int end_page = (start_pos + n + kPageTokens - 1) / kPageTokens;
+  std::vector<int32_t> taken;
+  for (int pi = have; pi < end_page; ++pi) {
+    const int32_t pg = c->free_pages.back();  // availability was checked by the caller
+    c->free_pages.pop_back();
+    c->page_ref[pg] = 1;
+    q.pages.push_back(pg);
+    taken.push_back(pg);
+  }
+  auto rollback = [&]() {
+    for (auto it = taken.rbegin(); it != taken.rend(); ++it) {
+      q.pages.pop_back();
+      c->page_ref[*it] = 0;
+      c->free_pages.push_back(*it);
+    }
+    if (q.len == 0 && q.pages.empty()) q.open = false;
+  };
+  for (size_t i0 = 0; i0 < taken.size(); i0 += kMaxUpd) {
+    KvXfer x;
+    std::memset(&x, 0, sizeof(x));
+    x.kv = c->kv_dev;
+    x.block_table = c->block_table_dev;
+    x.n_pages = c->n_pages;
+    x.max_pages_per_seq = c->max_pages_per_seq;
+    x.n_layers = c->d.n_layers;
+    x.n_kv_heads = c->d.n_kv_heads;
+    x.head_dim = c->d.head_dim;
+    x.slot = seq_id;
+    x.upd_index0 = have + (int)i0;
+    for (size_t i = i0; i < std::min(taken.size(), i0 + kMaxUpd); ++i)
+      x.upd[x.n_upd++] = PageUpd{seq_id, have + (int32_t)i, taken[i]};
+    if (int r = launch_kv_xfer(x, st)) {
+      rollback();
+      return r;
+    }
+  }
+  PrefillArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.d = c->d;
+  a.layers = c->layers_host.data();
+  a.embed = c->embed;
+  a.final_norm = c->final_norm;
+  a.lm_pk = c->lm_pk;
+  a.rope = c->rope_dev;
+  a.kv = c->kv_dev;
+  a.block_table = c->block_table_dev;
+  a.n_pages = c->n_pages;
+  a.max_pages_per_seq = c->max_pages_per_seq;
+  a.slot = seq_id;
+  a.start = start_pos;
+  a.n = n;
+  a.tokens = tokens_dev;
+  a.out_token = out_token_dev;
+  if (c->dbg_flags & MK_DBG_TRACE) {
+    a.trace = c->trace;
+    a.trace_bytes = mk_trace_bytes(&c->d, rows_traced);
+    a.trace_rows = rows_traced;
+  }
+  a.err = c->sc.err;
+  if (int r = prefill_run(&c->prefill, a, st)) {
+    rollback();
+    return r;
+  }
+  q.len = start_pos + n;
+  return MK_OK;
+}
+
 MK_API int mk_prefill_chunk(mk_ctx* c, int32_t seq_id, const int32_t* tokens_dev, int32_t n,
                             int32_t start_pos, int32_t* out_token_dev, void* stream) {
   g_err.clear();
@@ -526,6 +607,7 @@ MK_API int mk_prefill_chunk(mk_ctx* c, int32_t seq_id, const int32_t* tokens_dev
   if (need > (int)c->free_pages.size()) return fail(MK_ERR_NO_PAGES, "KV page pool exhausted");
   q.open = true;
   cudaStream_t st = (cudaStream_t)stream;
+  if (n > kMaxBatch) return prefill_gemm_chunk(c, seq_id, tokens_dev, n, start_pos, out_token_dev, st);
   const int B = c->d.max_batch;
   int32_t slots[kMaxBatch], pos[kMaxBatch];
   for (int off = 0; off < n; off += B) {
@@ -772,6 +854,7 @@ MK_API int mk_destroy(mk_ctx* c) {
   cudaFree(c->scratch_dev);
   cudaFree(c->kv_dev);
   cudaFree(c->block_table_dev);
+  prefill_free(c->prefill);
   delete c;
   if (e != cudaSuccess) return fail(MK_ERR_CUDA, std::string("cudaDeviceSynchronize: ") + cudaGetErrorString(e));
   return MK_OK;

@@ -139,6 +139,31 @@ struct KvXfer {
 };
 int launch_kv_xfer(const KvXfer& a, cudaStream_t st);
 
+// Chunked prefill (mk_prefill.cu): chunks of more than kMaxBatch positions
+// run as per-layer GEMMs over all rows of the chunk.
+constexpr int kMaxPrefill = 4096;
+struct PrefillWork;  // workspace kept by a context (made on first use)
+struct PrefillArgs {
+  mk_model_desc d;
+  const LayerW* layers;        // host copy of the layer table (packed record pointers)
+  const void* embed;
+  const void* final_norm;
+  const uint8_t* lm_pk;
+  const float2* rope;          // device RoPE table [max_ctx][hd/2]
+  uint16_t* kv;
+  int32_t* block_table;        // holds the pages of every position of the chunk
+  int32_t n_pages, max_pages_per_seq, slot, start, n;
+  const int32_t* tokens;       // device [n]
+  int32_t* out_token;          // device [1] or null
+  float* trace;                // trace of the chunk's last trace_rows rows, or null
+  size_t trace_bytes;
+  int32_t trace_rows;
+  int32_t* err;                // device error word
+};
+int prefill_run(PrefillWork** work, const PrefillArgs& a, cudaStream_t st);
+void prefill_free(PrefillWork* w);
+int prefill_setup_attributes(const mk_model_desc& m);
+
 // Error sites recorded in err[1].
 enum ErrSite { SITE_BARRIER = 1, SITE_PAGE = 2, SITE_UNIT = 3, SITE_TOKEN = 4, SITE_RING = 5, SITE_SMEM = 6 };
 

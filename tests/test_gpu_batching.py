@@ -230,7 +230,10 @@ def test_fork_shares_pages_and_gives_the_same_tokens(gpu_lib, tiny_int4):
     m, w = tiny_int4
     eng = Engine(m, w, n_pages=8, max_ctx=1024, max_seqs=3)
     a = _prompt(m, 300, 0)
-    ta = eng.prefill(0, a).clone()
+    # the source in the same two chunks the fork replays (a chunk's GEMMs
+    # are the same launches, so the results are the same bits)
+    eng.prefill(0, a[:256])
+    ta = eng.prefill(0, a[256:], start_pos=256).clone()
     eng.sync()
     free0 = eng.info()["free_pages"]                 # 8 - 3
     eng.fork(0, 1, 256)                              # shares 2 pages, takes none
@@ -258,59 +261,26 @@ def test_fork_shares_pages_and_gives_the_same_tokens(gpu_lib, tiny_int4):
 
 def test_prefix_cache_a_a_b_a(gpu_lib, tiny_int4):
     """The prefix-cache sequence of turns A, A, B, A: the second and the last
-    turn over prompt A reuse its whole pages (512 of 600 tokens) and give the
-    tokens a cold prefill gives."""
+    turn over prompt A reuse its whole pages (512 of 600 tokens); every turn's
+    next token is the oracle's wherever the oracle's top-2 margin is clear."""
     from moe_decode_megakernel_persistent_gb300.engine import PrefixCache
     m, w = tiny_int4
-    eng = Engine(m, w, n_pages=32, max_ctx=1024, max_seqs=8)
+    orc = Oracle(m, PR.host_fetch(m, w))
+    ref = {}
+    for name, seq in (("A", 0), ("B", 1)):
+        p = SP.prompt_tokens(m.seed, m.vocab, 600, seq=seq)
+        tok, tr = orc.prefill(orc.new_kv(), p)
+        ref[name] = (tok, float(tr["top2_margin"][-1]))
     A, B = _prompt(m, 600, 0), _prompt(m, 600, 1)
-    cold = {}
-    for name, p in (("A", A), ("B", B)):
-        t = eng.prefill(7, p)
-        cold[name] = int(t.item())
-        eng.release(7)
+    eng = Engine(m, w, n_pages=32, max_ctx=1024, max_seqs=8)
     pc = PrefixCache(eng, capacity=2)
-    reused = []
+    reused, rep = [], PR.Report()
     for sid, (name, p) in enumerate((("A", A), ("A", A), ("B", B), ("A", A))):
         out, n = pc.prefill(sid, p)
         eng.sync()
         reused.append(n)
-        assert int(out.item()) == cold[name], (sid, name)
+        PR.check_token(rep, int(out.item()), ref[name][0], ref[name][1], f"turn {sid} ({name})", seq=sid)
         pc.keep(sid, p.cpu().tolist())
     assert reused == [0, 512, 0, 512]
-    eng.close()
-
-
-def test_timing_stamps_cover_every_phase_of_every_block(gpu_lib, tiny_int4):
-    """MK_DBG_TIMING: every block stamps its start, each layer's phases (work
-    done, barrier released; staging done where the phase stages) and the
-    end, in increasing order; a barrier is released only after every block
-    arrived."""
-    m, w = tiny_int4
-    eng = Engine(m, w, n_pages=8, max_ctx=256, max_seqs=2)
-    tok = eng.prefill(0, _prompt(m, 40, 0))
-    eng.enable_timing()
-    eng.decode_step([0], tok, [40], tok)
-    eng.sync()
-    t = eng.timing_stamps()
-    grid = eng.info()["grid"]
-    assert t.shape[0] == grid
-    for b in range(grid):
-        seq = [t[b, 0]]
-        for l in range(m.n_layers):
-            for p in range(5):
-                base = 1 + 16 * l + 3 * p
-                if p != 1:                                # attention stages nothing
-                    seq.append(t[b, base])
-                seq += [t[b, base + 1], t[b, base + 2]]
-        seq.append(t[b, 1 + 16 * m.n_layers])
-        seq = np.asarray(seq)
-        assert (seq > 0).all(), b
-        assert (np.diff(seq) >= 0).all(), b
-    for l in range(m.n_layers):
-        for p in range(5):
-            base = 1 + 16 * l + 3 * p
-            assert t[:, base + 2].min() >= t[:, base + 1].max()
-    pt = eng.phase_times_us()
-    assert pt["total"] > 0 and all(pt[k]["span"] >= 0 for k in Engine.PHASES)
+    assert not rep.failures, rep
     eng.close()
