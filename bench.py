@@ -234,10 +234,11 @@ def run_ours(args, rank, world):
     gen_s = time.time() - t0
     prompt_len = w.prompt_len
     max_ctx = prompt_len + K + 2 * args.e2e_steps + W + 64
-    B16, P16 = 16, 256
-    ctx16 = P16 + W + 1 + args.batch16_steps + 16
-    pages = 3 * ((max_ctx + 127) // 128) + 8 + B16 * ((ctx16 + 127) // 128)
-    eng = Engine(m, weights, n_pages=pages, max_ctx=max_ctx, max_seqs=4 + B16)
+    pages = 3 * ((max_ctx + 127) // 128) + 8
+    eng = Engine(m, weights, n_pages=pages, max_ctx=max_ctx, max_seqs=4)
+
+    def eng_factory(n_pages, max_ctx16, max_seqs):
+        return Engine(m, weights, n_pages=n_pages, max_ctx=max_ctx16, max_seqs=max_seqs)
     stream = torch.cuda.current_stream()
 
     # warm-up sequence: a short prompt and W decode steps
@@ -295,54 +296,13 @@ def run_ours(args, rank, world):
     e2e_s = time.perf_counter() - t0
     eng.sync()
 
-    # batch 16: sixteen sequences with 256-token prompts decoded together, one
-    # launch per step for all of them
+    # the 16-client workload: 16 sequences, prompt lengths U[256, 8192] and
+    # arrival steps U[0, 64] from the schedule (seed 4), 256 generated tokens
+    # each, continuously batched (one decode launch per step for the active
+    # sequences; arrivals prefilled when they join)
     b16 = None
-    if args.batch16_steps > 0:
-        K16 = args.batch16_steps
-        ids = list(range(4, 4 + B16))
-        toks16 = torch.empty(B16, dtype=torch.int32, device=dev)
-        for j, sid in enumerate(ids):
-            p16 = torch.from_numpy(SP.prompt_tokens(m.seed, m.vocab, P16, seq=100 + j)).to(dev)
-            eng.prefill(sid, p16, out=toks16[j:j + 1])
-        pos = P16
-        for i in range(W):
-            eng.decode_step(ids, toks16, [pos] * B16, toks16)
-            pos += 1
-        # distinct experts per MoE layer, counted on one traced step
-        eng.enable_trace(B16)
-        eng.decode_step(ids, toks16, [pos] * B16, toks16)
-        eng.sync()
-        pos += 1
-        tk = eng.split_trace(B16)["topk"][m.n_dense:, :, :m.top_k].cpu().numpy().astype(int)
-        distinct = float(np.mean([len(np.unique(tk[l])) for l in range(tk.shape[0])]))
-        eng.disable_trace()
-        clocks16 = ClockSampler(torch.cuda.current_device())
-        clocks16.start()
-        time.sleep(0.3)
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for i in range(K16):
-            eng.decode_step(ids, toks16, [pos + i] * B16, toks16)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        clk16 = clocks16.stop()
-        eng.sync()
-        ms16, _ = aggregate_over_ranks(e0.elapsed_time(e1), K16, dev)
-        bytes16 = sum(step_bytes(m, [pos + i + 1] * B16, distinct) for i in range(K16)) / K16
-        ach16 = bytes16 / (ms16 / K16 * 1e-3) / 1e9
-        b16 = {"value": round(world * B16 * K16 / (ms16 / 1e3), 2), "unit": "tok/s",
-               "ms_per_step": round(ms16 / K16, 4), "steps": K16, "sequences": B16,
-               "prompt": P16, "context": [pos + 1, pos + K16],
-               "distinct_experts_per_layer": round(distinct, 2),
-               "roofline": {"bound": "hbm", "achieved": round(ach16, 1),
-                            "frac": round(ach16 / load_peaks()[0]["hbm_gbs"], 4),
-                            "bytes_per_step": int(bytes16)},
-               "clocks": clk16}
+    if args.batch16_steps > 0 and args.config in (3, 5):
+        b16 = run_batch16(eng_factory, m, dev, world, args)
 
     # per-phase timeline of one more decode launch (MK_DBG_TIMING), outside
     # the timed region: medians over the MoE layers
@@ -399,10 +359,76 @@ def run_ours(args, rank, world):
         out["timeline_us"] = timeline
     if b16 is not None:
         out["batch16"] = b16
+        if "full_batch" in b16:
+            fb = b16["full_batch"]
+            # bytes of one full-batch step: 16 rows at the workload's mean
+            # context, the distinct experts of 16 uniformly routed rows
+            sched = __import__("synth").prompts.schedule(__import__("synth").CONFIGS[5])
+            mean_ctx = statistics.mean(L for _, L in sched) + 128
+            distinct = 64 * (1 - (1 - 6 / 64) ** 16)
+            bps = step_bytes(m, [int(mean_ctx)] * 16, distinct)
+            ach = bps / (fb["ms_per_step"] * 1e-3) / 1e9
+            fb["roofline"] = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": round(ach / peaks["hbm_gbs"], 4), "bytes_per_step": int(bps),
+                              "bytes_model": "16 rows at the mean context of the workload + 128, distinct experts "
+                                             "64 (1 - (1 - 6/64)^16) per MoE layer"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(m, weights)
     eng.close()
     return out
+
+
+def run_batch16(eng_factory, m, dev, world, args):
+    """The 16-client workload through the continuous batcher.  Reported:
+    aggregate decode tok/s (generated tokens / summed decode-launch device
+    time), end-to-end tok/s (generated tokens / wall time including every
+    prefill), the finish step, and for the steps with all 16 sequences active
+    their mean time and roofline."""
+    import torch
+    import synth
+    from synth import prompts as SP
+    from moe_decode_megakernel_persistent_gb300.engine import Batcher, Request
+    w5 = synth.CONFIGS[5]
+    sched = SP.schedule(w5)
+    gen = w5.decode_tokens
+    pages = sum((L + gen + 127) // 128 for _, L in sched) + 16
+    eng = eng_factory(pages, max(L for _, L in sched) + gen + 8, 16)
+    reqs = [Request(seq_id=i, prompt=torch.from_numpy(SP.prompt_tokens(m.seed, m.vocab, L, seq=300 + i)).to(dev),
+                    max_new=gen, arrival=a) for i, (a, L) in enumerate(sched)]
+    # warm-up: a short request through the same engine
+    Batcher(eng).run([Request(seq_id=0, prompt=reqs[0].prompt[:64], max_new=4, arrival=0)])
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    out = Batcher(eng).run(reqs, read_back=False, timed=True)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.stop()
+    eng.sync()
+    tokens = sum(r.max_new for r in reqs)
+    full = [t for n, t in out["steps_ms"] if n == 16]
+    # distinct experts per MoE layer of a 16-row launch, from one traced step
+    # over 16 fresh sequences at the workload's mean prompt length
+    eng.close()
+    res = {"workload": f"{w5.name}: 16 sequences, prompt lengths U[256, 8192] and arrival steps U[0, 64] "
+                       f"(seed 4), {gen} greedy tokens each, continuous batching",
+           "value": round(world * tokens / (out["decode_ms"] / 1e3), 2), "unit": "tok/s",
+           "decode_ms_total": round(out["decode_ms"], 1), "launches": out["launches"],
+           "e2e": {"value": round(world * tokens / wall, 2), "unit": "tok/s",
+                   "wall_s": round(wall, 2), "includes": "every prefill and decode launch"},
+           "finish_step": out["finish_step"], "prompt_tokens": sum(L for _, L in sched),
+           "clocks": clocks}
+    if full:
+        ms16 = statistics.median(full)
+        res["full_batch"] = {"steps": len(full), "ms_per_step": round(ms16, 3),
+                             "value": round(world * 16 / (ms16 / 1e3), 2), "unit": "tok/s"}
+    return res
 
 
 class TimedFetch:
@@ -549,8 +575,8 @@ def main():
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--batch16-steps", type=int, default=32,
-                    help="timed decode steps of the 16-sequence batch (0 = skip)")
+    ap.add_argument("--batch16-steps", type=int, default=1,
+                    help="run the 16-client continuous-batching workload (0 = skip)")
     ap.add_argument("--no-timeline", action="store_true", help="skip the per-phase timeline launch")
     ap.add_argument("--timeline-out", default="", help="save the timeline launch's raw stamps (.npz)")
     ap.add_argument("--profile-case", action="store_true",

@@ -301,9 +301,12 @@ class Batcher:
     def __init__(self, engine: Engine):
         self.e = engine
 
-    def run(self, requests: list, read_back: bool = True) -> dict:
+    def run(self, requests: list, read_back: bool = True, timed: bool = False) -> dict:
+        """timed: CUDA events around every decode launch; the result then has
+        "decode_ms" (sum over launches) and "steps_ms" [(active rows, ms)]."""
         e = self.e
         dev = torch.device("cuda")
+        events = []
         pending = sorted(requests, key=lambda r: (r.arrival, r.seq_id))
         active: list = []
         tok_dev = {}           # seq_id -> device int32[1] with its next input token
@@ -321,7 +324,13 @@ class Batcher:
                 pos = [e.seq_length(i) for i in ids]
                 toks = torch.cat([tok_dev[i] for i in ids])
                 outs = torch.empty(len(ids), dtype=torch.int32, device=dev)
+                if timed:
+                    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    ev[0].record(torch.cuda.current_stream())
                 e.decode_step(ids, toks, pos, outs)
+                if timed:
+                    ev[1].record(torch.cuda.current_stream())
+                    events.append((len(ids), ev))
                 steps_run += 1
                 still = []
                 for k, r in enumerate(active):
@@ -338,5 +347,9 @@ class Batcher:
         if read_back:
             for r in requests:
                 r.generated = [int(t.item()) for t in r.generated]
-        return {"steps": step, "launches": steps_run,
-                "finish_step": max(r.finish_step for r in requests)}
+        out = {"steps": step, "launches": steps_run, "finish_step": max(r.finish_step for r in requests)}
+        if timed:
+            torch.cuda.synchronize()
+            out["steps_ms"] = [(n, a.elapsed_time(b)) for n, (a, b) in events]
+            out["decode_ms"] = sum(t for _, t in out["steps_ms"])
+        return out
