@@ -233,7 +233,7 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     gen_s = time.time() - t0
     prompt_len = w.prompt_len
-    max_ctx = prompt_len + K + 2 * args.e2e_steps + W + 64
+    max_ctx = prompt_len + K + 2 * args.e2e_steps + W + 64 + args.split_steps + 2
     pages = 3 * ((max_ctx + 127) // 128) + 8
     eng = Engine(m, weights, n_pages=pages, max_ctx=max_ctx, max_seqs=4)
 
@@ -275,6 +275,37 @@ def run_ours(args, rank, world):
     ms, total_tokens = aggregate_over_ranks(e0.elapsed_time(e1), K, dev)
     ms_per_step = ms / K
 
+    # the same decode step run as one launch per phase group of a layer and
+    # one for lm_head (MK_DBG_SPLIT): kernel boundaries in place of the grid
+    # barriers between groups, on the same device code
+    split = None
+    if args.split_steps > 0:
+        from moe_decode_megakernel_persistent_gb300 import _lib as Lb
+        Ks = args.split_steps
+        pos_s = prompt_len + K
+        Lb.mk_set_debug(eng.ctx, Lb.MK_DBG_SPLIT, 0, 0, 0, 0)
+        for i in range(2):
+            eng.decode_step([0], tok, [pos_s], tok)
+            pos_s += 1
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(Ks):
+            eng.decode_step([0], tok, [pos_s + i], tok)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        Lb.mk_set_debug(eng.ctx, 0, 0, 0, 0, 0)
+        eng.sync()
+        split_ms = e0.elapsed_time(e1) / Ks
+        groups = 4 * m.n_layers
+        split = {"ms_per_step": round(split_ms, 4), "persistent_ms_per_step": round(ms_per_step, 4),
+                 "launches_per_step": groups + 1, "grid_barriers_per_step_persistent": 5 * m.n_layers,
+                 "boundaries_replacing_barriers": groups,
+                 "us_per_boundary_minus_barrier": round((split_ms - ms_per_step) * 1e3 / groups, 3),
+                 "note": "context grows by 2 + K steps before the split run"}
+        K_extra = Ks + 2
+    else:
+        K_extra = 0
+
     # end to end through the public API with host buffers: each step copies
     # its input token from pinned host memory, runs, reads the result back
     E = args.e2e_steps
@@ -309,7 +340,7 @@ def run_ours(args, rank, world):
     timeline = None
     if not args.no_timeline:
         eng.enable_timing()
-        pos_t = prompt_len + K
+        pos_t = prompt_len + K + K_extra
         for _ in range(2):          # the second launch is the one kept
             eng.decode_step([0], tok, [pos_t], tok)
             pos_t += 1
@@ -357,6 +388,8 @@ def run_ours(args, rank, world):
     }
     if timeline is not None:
         out["timeline_us"] = timeline
+    if split is not None:
+        out["dispatch_vs_barrier"] = split
     if b16 is not None:
         out["batch16"] = b16
         if "full_batch" in b16:
@@ -578,6 +611,8 @@ def main():
     ap.add_argument("--batch16-steps", type=int, default=1,
                     help="run the 16-client continuous-batching workload (0 = skip)")
     ap.add_argument("--no-timeline", action="store_true", help="skip the per-phase timeline launch")
+    ap.add_argument("--split-steps", type=int, default=16,
+                    help="decode steps timed as one launch per phase group (0 = skip)")
     ap.add_argument("--timeline-out", default="", help="save the timeline launch's raw stamps (.npz)")
     ap.add_argument("--profile-case", action="store_true",
                     help="prefill + --steps decode launches only (for an ncu capture)")

@@ -268,6 +268,12 @@ MK_API int mk_sync(mk_ctx* ctx, void* stream);
  * Errors: INVALID_ARG. */
 #define MK_DBG_TRACE 1u
 #define MK_DBG_SKIP_ARRIVAL 2u
+#define MK_DBG_SPLIT 8u    /* each decode / prefill launch runs as 4 * n_layers + 1 launches of the
+                              same kernel, one per phase group of a layer (QKV | attention |
+                              o_proj | routing + gate/up + down) and one for lm_head: the kernel
+                              boundary takes the place of the grid barrier between groups.
+                              Results are the same bits; it exists to measure a launch
+                              boundary against a grid barrier on the same device code. */
 #define MK_DBG_TIMING 4u   /* trace_dev receives uint64 %globaltimer stamps (ns) of
                               every block: block b's record of R = 16 * n_layers + 2
                               stamps starts at [b * R]; in it [0] block start; for

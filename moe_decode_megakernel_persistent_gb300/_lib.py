@@ -25,6 +25,7 @@ WDTYPES = {"f32": MK_F32, "bf16": MK_BF16, "int4": MK_INT4_G64}
 MK_DBG_TRACE = 1
 MK_DBG_SKIP_ARRIVAL = 2
 MK_DBG_TIMING = 4
+MK_DBG_SPLIT = 8
 
 
 class MKError(RuntimeError):

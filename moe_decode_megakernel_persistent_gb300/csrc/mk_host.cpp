@@ -263,9 +263,27 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
   a.spin_limit_ns = c->spin_limit_ns;
   // a skipped arrival is a one-shot request
   c->dbg_flags &= ~MK_DBG_SKIP_ARRIVAL;
-  void* args[] = {&a};
-  cudaError_t e = cudaLaunchCooperativeKernel(c->kern.fn, dim3(c->grid), dim3(kBlockThreads), args,
-                                              (size_t)launch_smem_bytes(c->kern, n), st);
+  auto go = [&](int lo, int hi, int lm) {
+    a.slice_lo = lo;
+    a.slice_hi = hi;
+    a.run_lm = lm;
+    void* args[] = {&a};
+    return cudaLaunchCooperativeKernel(c->kern.fn, dim3(c->grid), dim3(kBlockThreads), args,
+                                       (size_t)launch_smem_bytes(c->kern, n), st);
+  };
+  const int groups = 4 * c->d.n_layers;
+  cudaError_t e = cudaSuccess;
+  if (c->dbg_flags & MK_DBG_SPLIT) {
+    // one launch per phase group, then lm_head: kernel boundaries in place of
+    // the grid barriers between groups
+    for (int s = 0; s < groups && e == cudaSuccess; ++s) {
+      e = go(s, s + 1, 0);
+      a.n_upd = 0;  // the first launch entered the new pages
+    }
+    if (e == cudaSuccess) e = go(groups, groups, 1);
+  } else {
+    e = go(0, groups, 1);
+  }
   if (e != cudaSuccess) {
     rollback();
     return fail(MK_ERR_CUDA, std::string("cudaLaunchCooperativeKernel: ") + cudaGetErrorString(e));

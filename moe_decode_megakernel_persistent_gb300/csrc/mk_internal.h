@@ -113,6 +113,10 @@ struct StepArgs {
   int32_t n_upd;
   uint32_t dbg_flags;
   uint32_t dbg_arg;
+  // the phase groups this launch runs: group s is layer s / 4, part s % 4
+  // (0 QKV, 1 attention, 2 o_proj, 3 routing + gate/up + down); a step is
+  // groups [0, 4 * n_layers) and then lm_head (run_lm)
+  int32_t slice_lo, slice_hi, run_lm;
   uint64_t spin_limit_ns;
   int32_t slot[kMaxBatch];
   int32_t pos[kMaxBatch];

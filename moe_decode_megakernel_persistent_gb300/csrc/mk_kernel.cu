@@ -975,7 +975,7 @@ struct Model {
         int old;
         asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
                      : "=r"(old) : "l"(a.sc.merge_cnt + b * NKV + g) : "memory");
-        const int arr = old - l * nch;
+        const int arr = old - (l - F.args.slice_lo / 4) * nch;
         if (arr >= nch - MG) {
           const int r = arr - (nch - MG);
           if (F.n_merge >= kMaxOwnUnits) {  // the host bounds units per block
@@ -996,7 +996,7 @@ struct Model {
       const int b = F.merge_job[jm][0], g = F.merge_job[jm][1];
       const int nch = (a.pos[b] + 1 + a.chunk - 1) / a.chunk;
       if (tid == 0) {
-        const int target = (l + 1) * nch;
+        const int target = (l + 1 - a.slice_lo / 4) * nch;
         const uint64_t ts = globaltimer();
         F.flag = 1;
         for (uint32_t i = 0;; ++i) {
@@ -1660,9 +1660,11 @@ struct Model {
     const Ctx& c = F.ctx;
     const int n = c.n;
 #pragma unroll 1
-    for (int l = 0; l < a.n_layers; ++l) {
+    for (int s = a.slice_lo; s < a.slice_hi; s += 4 - s % 4) {  // one pass per layer touched
+      const int l = s / 4;
+      const int part_lo = s % 4, part_hi = min(4, a.slice_hi - 4 * l);  // parts [part_lo, part_hi) of layer l
       const LayerW Lg = a.layers[l];  // one batch of loads per layer
-      {  // P1: RoPE pair tasks [p0, p1): records 2p, 2p + 1
+      if (part_lo <= 0 && part_hi > 0) {  // P1: RoPE pair tasks [p0, p1): records 2p, 2p + 1
         int p0, p1;
         qkv_range(c, p0, p1);
 #pragma unroll 1
@@ -1672,7 +1674,7 @@ struct Model {
           p.end();
         }
       }
-      {  // P2: cached K/V of this block's units
+      if (part_lo <= 1 && part_hi > 1) {  // P2: cached K/V of this block's units
         int k = 0;
 #pragma unroll 1
         for (int u = c.bid; u < a.n_units; u += c.G, ++k) {
@@ -1701,12 +1703,15 @@ struct Model {
         }
       }
       // P3: o_proj rows [r0, r0 + nr)
+      if (part_lo <= 2 && part_hi > 2) {
 #pragma unroll 1
-      for (int t0 = 0; t0 < c.nr; t0 += T_O) {
-        if (!p.template begin<STAGE>()) return;
-        put_recs(p, 0, min(T_O, c.nr - t0), Lg.pk[PK_O] + (size_t)(c.r0 + t0) * REC_Q, REC_Q);
-        p.end();
+        for (int t0 = 0; t0 < c.nr; t0 += T_O) {
+          if (!p.template begin<STAGE>()) return;
+          put_recs(p, 0, min(T_O, c.nr - t0), Lg.pk[PK_O] + (size_t)(c.r0 + t0) * REC_Q, REC_Q);
+          p.end();
+        }
       }
+      if (part_hi <= 3) continue;
       if (l >= a.n_dense) {
         // P4/P5 need the layer's routing
         {
@@ -1780,7 +1785,7 @@ struct Model {
         }
       }
     }
-    if (a.out_first < n) {
+    if (a.run_lm && a.out_first < n) {
       int v0, v1;
       gu_range(c, a.vocab, v0, v1);
 #pragma unroll 1
@@ -1891,48 +1896,65 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
                      : "memory");
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    load_lw(0);
+    load_lw(a.slice_lo / 4 < a.n_layers ? a.slice_lo / 4 : 0);
     asm volatile("cp.async.wait_all;" ::: "memory");
     csync();
-    for (int l = 0; ok && l < a.n_layers; ++l) {
+    // phase groups [slice_lo, slice_hi): a whole step, or one group per launch
+    // (MK_DBG_SPLIT), where state a group keeps in shared memory for a later
+    // group is reloaded from global memory at the start of the launch
+    for (int s = a.slice_lo; ok && s < a.slice_hi; ++s) {
+      const int l = s / 4, part = s % 4;
+      // a later group, or lm_head (which reads every block's rows of x),
+      // follows in this launch: the group ends with a grid barrier
+      const bool more = s + 1 < a.slice_hi || (a.run_lm && a.out_first < n);
+      const bool first = s == a.slice_lo;
       const int sm = M::stage_mode(c, true);
-      if (sm == 0) M::template qkv_stage<0>(l);
-      else if (sm == 1) M::template qkv_stage<1>(l);
-      else M::template qkv_stage<2>(l);
-      M::qkv(l);
-      MK_STAMP(c, l, 0, 1);
-      if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
-      MK_STAMP(c, l, 0, 2);
-      M::attention(l);
-      MK_STAMP(c, l, 1, 1);
-      if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
-      MK_STAMP(c, l, 1, 2);
-      if (sm == 0) M::template oproj_stage<0>(l);
-      else if (sm == 1) M::template oproj_stage<1>(l);
-      else M::template oproj_stage<2>(l);
-      M::oproj(l);
-      MK_STAMP(c, l, 2, 1);
-      if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
-      MK_STAMP(c, l, 2, 2);
-      M::route(l);
-      {
-        const int fm = M::stage_mode(c, l < a.n_dense);
-        if (fm == 0) M::template ffn_stage<0>(l);
-        else if (fm == 1) M::template ffn_stage<1>(l);
-        else M::template ffn_stage<2>(l);
+      if (part == 0) {
+        if (sm == 0) M::template qkv_stage<0>(l);
+        else if (sm == 1) M::template qkv_stage<1>(l);
+        else M::template qkv_stage<2>(l);
+        M::qkv(l);
+        MK_STAMP(c, l, 0, 1);
+        if (more && !(ok = grid_barrier(a, nbar, &F.ok_word))) break;
+        MK_STAMP(c, l, 0, 2);
+      } else if (part == 1) {
+        M::attention(l);
+        MK_STAMP(c, l, 1, 1);
+        if (more && !(ok = grid_barrier(a, nbar, &F.ok_word))) break;
+        MK_STAMP(c, l, 1, 2);
+      } else if (part == 2) {
+        if (first && l >= a.n_dense) M::fetch_router_slice(F.lw);  // fetched by the QKV group otherwise
+        if (sm == 0) M::template oproj_stage<0>(l);
+        else if (sm == 1) M::template oproj_stage<1>(l);
+        else M::template oproj_stage<2>(l);
+        M::oproj(l);
+        MK_STAMP(c, l, 2, 1);
+        if (more && !(ok = grid_barrier(a, nbar, &F.ok_word))) break;
+        MK_STAMP(c, l, 2, 2);
+      } else {
+        if (first)  // this block's rows of h, kept by the o_proj group otherwise
+          for (int i = tid; i < n * c.nr; i += kThreads)
+            F.hs[i / c.nr][i % c.nr] = __ldcg(a.sc.h + (i / c.nr) * S::H + c.r0 + i % c.nr);
+        M::route(l);
+        {
+          const int fm = M::stage_mode(c, l < a.n_dense);
+          if (fm == 0) M::template ffn_stage<0>(l);
+          else if (fm == 1) M::template ffn_stage<1>(l);
+          else M::template ffn_stage<2>(l);
+        }
+        if (l + 1 < a.n_layers) load_lw(l + 1);
+        M::gateup(l);
+        MK_STAMP(c, l, 3, 1);
+        if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
+        MK_STAMP(c, l, 3, 2);
+        if (l >= a.n_dense) M::template down<true>(l);
+        else M::template down<false>(l);
+        MK_STAMP(c, l, 4, 1);
+        if (more && !(ok = grid_barrier(a, nbar, &F.ok_word))) break;
+        MK_STAMP(c, l, 4, 2);
       }
-      if (l + 1 < a.n_layers) load_lw(l + 1);
-      M::gateup(l);
-      MK_STAMP(c, l, 3, 1);
-      if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
-      MK_STAMP(c, l, 3, 2);
-      if (l >= a.n_dense) M::template down<true>(l);
-      else M::template down<false>(l);
-      MK_STAMP(c, l, 4, 1);
-      if (!(ok = grid_barrier(a, nbar, &F.ok_word))) break;
-      MK_STAMP(c, l, 4, 2);
     }
-    if (ok && a.out_first < n) {
+    if (ok && a.run_lm && a.out_first < n) {
       // rows from out_first on: one row alone takes the one-row variant
       const int lm = c.tc ? 2 : (n - a.out_first == 1 ? 0 : 1);
       if (lm == 0) M::template lm_stage<0>();
@@ -1941,6 +1963,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
       M::lm_head();
     }
     if (c.tm && tid == 0) c.tm[1 + 16 * a.n_layers] = globaltimer();
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no copy into shared memory outlives the block
     csync();
     if (tid == 0 && !ok) F.abort = 1;
   }

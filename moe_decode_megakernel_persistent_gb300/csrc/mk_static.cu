@@ -210,6 +210,9 @@ extern "C" MK_API int mk_decode_step_static(
   a.out_first = 0;
   a.max_units = max_units;
   a.spin_limit_ns = 1000000000ull;
+  a.slice_lo = 0;
+  a.slice_hi = 4 * d->n_layers;
+  a.run_lm = 1;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: counters, merge counts and

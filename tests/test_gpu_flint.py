@@ -239,3 +239,38 @@ def test_flint_int4_long_context_batched_equals_solo(gpu_lib):
     eng.close()
     del w
     torch.cuda.empty_cache()
+
+
+def test_split_launches_give_the_same_bits(gpu_lib, flint4_int4):
+    """MK_DBG_SPLIT runs a decode step as one launch per phase group of a
+    layer (QKV | attention | o_proj | routing + gate/up + down) plus one for
+    lm_head, the kernel boundary in place of the grid barrier: the same device
+    code on the same inputs, so the same trace and tokens, bit for bit, at one
+    row and at three."""
+    from moe_decode_megakernel_persistent_gb300 import _lib as L
+    m, w = flint4_int4
+    lens = [300, 129, 40]
+    prompts = [torch.from_numpy(SP.prompt_tokens(m.seed, m.vocab, n, seq=10 + s)).cuda() for s, n in enumerate(lens)]
+
+    def run(split):
+        eng = Engine(m, w, n_pages=16, max_ctx=1024, max_seqs=4)
+        toks = torch.empty(3, dtype=torch.int32, device="cuda")
+        for s, p in enumerate(prompts):
+            eng.prefill(s, p, out=toks[s:s + 1])
+        traces = []
+        for rows in (1, 3):
+            nbytes = L.mk_trace_bytes(eng.desc, rows)
+            tr = torch.zeros(nbytes // 4, dtype=torch.float32, device="cuda")
+            L.mk_set_debug(eng.ctx, L.MK_DBG_TRACE | (L.MK_DBG_SPLIT if split else 0), 0, tr.data_ptr(), nbytes, 0)
+            ids = [0, 1, 2][:rows]
+            eng.decode_step(ids, toks[:rows], [eng.seq_length(s) for s in ids], toks[:rows])
+            eng.sync()
+            traces.append(tr)
+        eng.close()
+        return traces, toks.cpu()
+
+    a, ta = run(False)
+    b, tb = run(True)
+    assert torch.equal(ta, tb)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
