@@ -572,9 +572,12 @@ def run_reference(args, rank, world):
 
 
 def run_profile_case(args):
-    """A short run for an ncu capture of the decode launch at the bench's
-    full size: prefill of the workload's prompt (ceil(prompt / 16) launches),
-    then --steps decode launches; nothing else (no CPU baseline, no e2e)."""
+    """A short run for ncu captures of the decode launch: --rows sequences
+    with the workload's prompt (rows > 1: the first 2048 tokens of it)
+    prefilled, then --steps decode launches of all rows; nothing else (no
+    CPU baseline, no e2e).  --layers keeps the first layers of the model (the
+    same layer weights; a reduced-depth case for captures that must stay
+    small)."""
     import torch
     import synth
     from synth import prompts as SP
@@ -585,17 +588,21 @@ def run_profile_case(args):
     _build.build()
     dev = torch.device("cuda", torch.cuda.current_device())
     w = synth.CONFIGS[args.config]
-    m = w.model
+    m = w.model if not args.layers else w.model.with_(n_layers=args.layers)
     weights = SW.model_torch(m, dev)
-    prompt_len = w.prompt_len
+    rows = args.rows
+    prompt_len = w.prompt_len if rows == 1 else min(2048, w.prompt_len or 2048)
     max_ctx = prompt_len + args.steps + 16
-    eng = Engine(m, weights, n_pages=(max_ctx + 127) // 128 + 2, max_ctx=max_ctx, max_seqs=2)
-    prompt = torch.from_numpy(SP.prompt_tokens(m.seed, m.vocab, prompt_len)).to(dev)
-    tok = eng.prefill(0, prompt)
+    eng = Engine(m, weights, n_pages=rows * ((max_ctx + 127) // 128 + 1), max_ctx=max_ctx, max_seqs=rows)
+    toks = torch.empty(rows, dtype=torch.int32, device=dev)
+    for r in range(rows):
+        prompt = torch.from_numpy(SP.prompt_tokens(m.seed, m.vocab, prompt_len, seq=r)).to(dev)
+        eng.prefill(r, prompt, out=toks[r:r + 1])
+    ids = list(range(rows))
     for i in range(args.steps):
-        eng.decode_step([0], tok, [prompt_len + i], tok)
+        eng.decode_step(ids, toks, [prompt_len + i] * rows, toks)
     eng.sync()
-    print(json.dumps({"profile_case": w.name, "prefill_launches": (prompt_len + 15) // 16,
+    print(json.dumps({"profile_case": w.name, "layers": m.n_layers, "rows": rows, "prompt": prompt_len,
                       "decode_launches": args.steps}))
 
 
@@ -616,6 +623,8 @@ def main():
     ap.add_argument("--timeline-out", default="", help="save the timeline launch's raw stamps (.npz)")
     ap.add_argument("--profile-case", action="store_true",
                     help="prefill + --steps decode launches only (for an ncu capture)")
+    ap.add_argument("--layers", type=int, default=0, help="profile case: keep the first N layers")
+    ap.add_argument("--rows", type=int, default=1, help="profile case: rows per decode launch")
     args = ap.parse_args()
     if args.profile_case:
         import torch
