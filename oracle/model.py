@@ -210,7 +210,7 @@ class Oracle:
     n_heads, n_kv_heads, head_dim, vocab, n_dense, dense_ffn, n_experts, top_k,
     expert_ffn, rope_theta, rms_eps).
     fetch(name, layer, expert) -> (raw, dtype): a stored tensor and its format
-    ('f32', 'bf16', 'int4').  Names: embed, final_norm, lm_head; per layer
+    ('f32', 'bf16', 'int4', 'int3').  Names: embed, final_norm, lm_head; per layer
     attn_norm, wq, wk, wv, wo, ffn_norm, and gate/up/down (dense layers) or
     router and exp_gate/exp_up/exp_down (MoE layers, per expert).
     cache_bytes: float64 weights kept after dequantisation (LRU).

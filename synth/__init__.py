@@ -7,5 +7,5 @@ quantises the seeded bf16 weights into the symmetric int4 (group 64) storage
 format that defines the int4 model.  Both sides consume what it produces; the
 oracle dequantises and computes on its own, the CUDA library on its own.
 """
-from .configs import CONFIGS, ModelShape, get_config  # noqa: F401
+from .configs import CONFIGS, EXTRA, FLINT_INT4_E3, ModelShape, get_config  # noqa: F401
 from . import weights, prompts  # noqa: F401

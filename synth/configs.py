@@ -30,6 +30,12 @@ class ModelShape:
     rms_eps: float
     wdtype: str           # "f32" | "bf16" | "int4": dtype of the linear layers
     seed: int             # weight seed
+    expert_dtype: Optional[str] = None  # "int3": the experts' format; None: wdtype
+
+    @property
+    def xdtype(self) -> str:
+        """Storage dtype of the expert matrices (gate, up, down of every expert)."""
+        return self.expert_dtype or self.wdtype
 
     @property
     def aux_dtype(self) -> str:
@@ -60,6 +66,11 @@ FLINT_BF16 = ModelShape(n_layers=49, hidden=2048, n_heads=16, n_kv_heads=4,
 
 FLINT_INT4 = FLINT_BF16.with_(wdtype="int4")
 
+# The lower-bit expert variant ("rec Megakernel and Tempo9 Compared", §5 Method:
+# rec serves the Flint model with INT3 experts): the same seeded weights, the
+# expert matrices in symmetric int3 (group 64), everything else in int4.
+FLINT_INT4_E3 = FLINT_INT4.with_(expert_dtype="int3")
+
 
 @dataclasses.dataclass(frozen=True)
 class Workload:
@@ -84,6 +95,14 @@ CONFIGS = {
     5: Workload(5, "flint-int4-cb16", FLINT_INT4, prompt_len=0, decode_tokens=256,
                 batch=16, n_seqs=16, len_range=(256, 8192), arrival_range=(0, 64),
                 sched_seed=4),
+}
+
+
+# Workloads beyond the five configurations: the int3-expert model on the
+# shape and context of configuration 3.
+EXTRA = {
+    "flint-int4e3-ctx2048": Workload(6, "flint-int4e3-ctx2048", FLINT_INT4_E3, prompt_len=2048,
+                                     decode_tokens=256),
 }
 
 

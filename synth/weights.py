@@ -13,8 +13,15 @@ Storage formats (the logical layout handed to the library and the oracle):
                an all-zero group gets s = 0, q = 0; packed two's-complement
                nibbles [rows, K/2] uint8 with the even k in the low nibble,
                scales [rows, K/64] bf16.
-The quantiser is part of defining the int4 model (its weights ARE the int4
-codes and scales); dequantisation is left to each consumer.
+  int3         (expert matrices of a model with expert_dtype "int3") symmetric,
+               groups of 64 consecutive K elements per row:
+               s = bf16_rne(fp32(max|w_g|) / 3); q = clamp(rint(w / s), -4, 3),
+               an all-zero group gets s = 0, q = 0; codes [rows, 3K/8] uint8:
+               every 8 consecutive k form one 24-bit little-endian word (3
+               bytes) holding the 3-bit two's-complement code of k at bits
+               3 (k % 8) .. 3 (k % 8) + 2; scales [rows, K/64] bf16.
+The quantisers are part of defining the int4 / int3 models (their weights ARE
+the codes and scales); dequantisation is left to each consumer.
 """
 from __future__ import annotations
 
@@ -64,8 +71,13 @@ def layer_tensor_names(m: ModelShape, layer: int) -> list:
     return names
 
 
+EXPERT_NAMES = ("exp_gate", "exp_up", "exp_down")
+
+
 def storage_dtype(m: ModelShape, name: str) -> str:
-    """'f32', 'bf16' or 'int4' for a tensor of model m."""
+    """'f32', 'bf16', 'int4' or 'int3' for a tensor of model m."""
+    if name in EXPERT_NAMES:
+        return m.xdtype
     if name in LINEAR_NAMES:
         return m.wdtype
     return m.aux_dtype
@@ -159,13 +171,53 @@ def quantize_int4_np(w_bits: np.ndarray):
     return packed, s_bits
 
 
+def _int3_codes_np(w_bits: np.ndarray):
+    """bf16 bits [R, K] -> (int3 codes q int8 [R, K] in [-4, 3], scale bits [R, K/64])."""
+    R, K = w_bits.shape
+    assert K % 64 == 0
+    w = bf16_bits_to_f32(w_bits).reshape(R, K // 64, 64)
+    amax = np.abs(w).max(axis=2)
+    s_bits = f32_to_bf16_bits((amax / np.float32(3.0)).astype(np.float32))
+    s = bf16_bits_to_f32(s_bits)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(s[:, :, None] > 0, np.rint(w / s[:, :, None]), 0.0)
+    return np.clip(q, -4, 3).astype(np.int8).reshape(R, K), s_bits
+
+
+def pack_int3_np(q: np.ndarray) -> np.ndarray:
+    """int3 codes [R, K] (values in [-4, 3]) -> packed uint8 [R, 3K/8]: each 8
+    consecutive codes as one little-endian 24-bit word, code j at bits 3j."""
+    R, K = q.shape
+    assert K % 8 == 0
+    u = (q.astype(np.int16) & 0x7).astype(np.uint32).reshape(R, K // 8, 8)
+    word = np.zeros((R, K // 8), dtype=np.uint32)
+    for j in range(8):
+        word |= u[:, :, j] << np.uint32(3 * j)
+    out = np.empty((R, K // 8, 3), dtype=np.uint8)
+    for b in range(3):
+        out[:, :, b] = (word >> np.uint32(8 * b)) & np.uint32(0xFF)
+    return out.reshape(R, 3 * K // 8)
+
+
+def quantize_int3_np(w_bits: np.ndarray):
+    """bf16 bits [R, K] -> (packed uint8 [R, 3K/8], scale bf16 bits uint16 [R, K/64])."""
+    q, s_bits = _int3_codes_np(w_bits)
+    return pack_int3_np(q), s_bits
+
+
+def quantize_np(w_bits: np.ndarray, storage: str):
+    if storage == "int4":
+        return quantize_int4_np(w_bits)
+    if storage == "int3":
+        return quantize_int3_np(w_bits)
+    return w_bits
+
+
 def linear_np(m: ModelShape, name: str, layer: int = -1, expert=None, rows=None):
     """A linear weight in its storage format: an array (f32 values / bf16 bits),
-    or for int4 a (packed, scale_bits) pair."""
+    or for int4 / int3 a (packed, scale_bits) pair."""
     raw = raw_np(m, name, layer, expert, rows)
-    if storage_dtype(m, name) == "int4":
-        return quantize_int4_np(raw)
-    return raw
+    return quantize_np(raw, storage_dtype(m, name))
 
 
 # ---------------------------------------------------------------- torch
@@ -226,20 +278,50 @@ def quantize_int4_torch(w, rows_per_chunk: int = 8192):
     return packed, scales
 
 
+def quantize_int3_torch(w, rows_per_chunk: int = 8192):
+    """torch bfloat16 [R, K] -> (packed uint8 [R, 3K/8], scales bfloat16 [R, K/64]);
+    bit-identical to quantize_int3_np."""
+    import torch
+    R, K = w.shape
+    packed = torch.empty(R, 3 * K // 8, dtype=torch.uint8, device=w.device)
+    scales = torch.empty(R, K // 64, dtype=torch.bfloat16, device=w.device)
+    for r0 in range(0, R, rows_per_chunk):
+        r1 = min(R, r0 + rows_per_chunk)
+        wf = w[r0:r1].float().view(r1 - r0, K // 64, 64)
+        amax = wf.abs().amax(dim=2)
+        sb = _bf16_rne_torch(amax / 3.0)
+        s = sb.float()
+        q = torch.where(s[:, :, None] > 0, torch.round(wf / s[:, :, None]),
+                        torch.zeros_like(wf))
+        u = (q.clamp(-4, 3).to(torch.int32).view(r1 - r0, K // 8, 8) & 0x7)
+        word = torch.zeros(r1 - r0, K // 8, dtype=torch.int32, device=w.device)
+        for j in range(8):
+            word |= u[:, :, j] << (3 * j)
+        for b in range(3):
+            packed[r0:r1].view(r1 - r0, K // 8, 3)[:, :, b] = ((word >> (8 * b)) & 0xFF).to(torch.uint8)
+        scales[r0:r1] = sb
+    return packed, scales
+
+
+def quantize_torch(w, storage: str):
+    if storage == "int4":
+        return quantize_int4_torch(w)
+    if storage == "int3":
+        return quantize_int3_torch(w)
+    return w
+
+
 def linear_torch(m: ModelShape, name: str, layer: int = -1, device="cpu"):
     """Whole linear tensor in storage format on `device` (experts stacked)."""
     storage = storage_dtype(m, name)
     shape = tensor_shape(m, name)
     if len(shape) == 3:
         parts = [raw_torch(m, name, layer, e, device) for e in range(shape[0])]
-        if storage != "int4":
+        if storage not in ("int4", "int3"):
             return torch_stack(parts)
-        qs = [quantize_int4_torch(p) for p in parts]
+        qs = [quantize_torch(p, storage) for p in parts]
         return torch_stack([a for a, _ in qs]), torch_stack([b for _, b in qs])
-    raw = raw_torch(m, name, layer, None, device)
-    if storage == "int4":
-        return quantize_int4_torch(raw)
-    return raw
+    return quantize_torch(raw_torch(m, name, layer, None, device), storage)
 
 
 def torch_stack(xs):
@@ -271,7 +353,7 @@ def linear_fast(m: ModelShape, name: str, layer: int = -1, expert=None):
         t = raw_torch(m, name, layer, expert, "cpu")
         return t.numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy().view(np.uint16)
     t = raw_torch(m, name, layer, expert, "cpu")
-    if storage_dtype(m, name) == "int4":
-        p, s = quantize_int4_torch(t)
+    if storage_dtype(m, name) in ("int4", "int3"):
+        p, s = quantize_torch(t, storage_dtype(m, name))
         return p.numpy(), s.view(torch.int16).numpy().view(np.uint16)
     return t.numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy().view(np.uint16)

@@ -20,7 +20,7 @@ def synth_fetch(m: ModelShape):
             if name in ("embed", "attn_norm", "ffn_norm", "final_norm", "router"):
                 cache[key] = (SW.raw_np(m, name, layer, expert), m.aux_dtype)
             else:
-                cache[key] = (SW.linear_np(m, name, layer, expert), m.wdtype)
+                cache[key] = (SW.linear_np(m, name, layer, expert), SW.storage_dtype(m, name))
         return cache[key]
     return fetch
 

@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 from oracle import model as O
-from oracle.numerics import dequant_int4, round_bf16, bf16_bits_to_f64
+from oracle.numerics import dequant_int3, dequant_int4, round_bf16, bf16_bits_to_f64
 from tests._models import Dims, dict_fetch, random_tensors
 
 
@@ -373,6 +373,50 @@ def test_int4_quantiser_error_bound_and_exact_grid():
     assert np.array_equal(bf16_bits_to_f64(gbits), wgrid)
     p2, s2 = SW.quantize_int4_np(gbits)
     np.testing.assert_array_equal(dequant_int4(p2, s2), wgrid)
+    np.testing.assert_array_equal(bf16_bits_to_f64(s2), 2.0 ** e)
+
+
+def test_int3_dequant_of_hand_packed_words():
+    # 0o76543210 holds the codes 0..7 in order (code j at bits 3j): as bytes,
+    # little-endian, 0x88 0xC6 0xFA; read as two's complement, 0 1 2 3 -4 -3 -2 -1.
+    # 0o01234567 = 0x053977 holds them reversed; 0o77777777 is eight -1 codes.
+    up = [0x88, 0xC6, 0xFA]
+    down = [0x77, 0x39, 0x05]
+    ones = [0xFF, 0xFF, 0xFF]
+    packed = np.array([up * 4 + down * 4 + ones * 8], dtype=np.uint8)   # K = 128
+    assert packed.shape == (1, 48)
+    s_bits = np.array([[0x3F80, 0x4040]], dtype=np.uint16)               # 1.0, 3.0
+    w = dequant_int3(packed, s_bits)
+    inc = [0, 1, 2, 3, -4, -3, -2, -1]
+    np.testing.assert_array_equal(w[0, :32], np.tile(inc, 4))
+    np.testing.assert_array_equal(w[0, 32:64], np.tile(inc[::-1], 4))
+    np.testing.assert_array_equal(w[0, 64:], np.full(64, -3.0))
+
+
+def test_int3_quantiser_error_bound_and_exact_grid():
+    from synth import weights as SW
+    from synth.configs import FLINT_INT4_E3
+    assert SW.storage_dtype(FLINT_INT4_E3, "exp_down") == "int3"
+    assert SW.storage_dtype(FLINT_INT4_E3, "down") == "int4"
+    raw = SW.raw_np(FLINT_INT4_E3, "exp_gate", 3, expert=5, rows=(0, 64))
+    packed, s_bits = SW.quantize_int3_np(raw)
+    assert packed.shape == (64, 3 * 2048 // 8) and s_bits.shape == (64, 32)
+    w = bf16_bits_to_f64(raw)
+    deq = dequant_int3(packed, s_bits)
+    s = np.repeat(bf16_bits_to_f64(s_bits), 64, axis=1)
+    assert np.all(np.abs(deq - w) <= s / 2 + 1e-12)
+    # every code is within the symmetric range the quantiser produces
+    assert np.all(np.abs(deq) <= 3 * s + 1e-12)
+    # grid values with power-of-two scales are exact in bf16 and come back exactly
+    rng = np.random.default_rng(22)
+    q = rng.integers(-3, 4, size=(4, 128))
+    q[:, 0] = 3
+    q[:, 64] = -3                                    # every group reaches |q| = 3
+    e = np.array([[-7, -3], [0, 2], [-12, -9], [1, -1]])
+    wgrid = q * np.repeat(2.0 ** e, 64, axis=1)
+    gbits = (np.asarray(wgrid, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    p2, s2 = SW.quantize_int3_np(gbits)
+    np.testing.assert_array_equal(dequant_int3(p2, s2), wgrid)
     np.testing.assert_array_equal(bf16_bits_to_f64(s2), 2.0 ** e)
 
 

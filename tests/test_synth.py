@@ -45,6 +45,10 @@ def test_weights_numpy_equals_torch_and_are_deterministic(cfg):
         pt, st = SW.quantize_int4_torch(t)
         assert np.array_equal(pa, pt.numpy())
         assert np.array_equal(sa.astype(np.int16), st.view(torch.int16).numpy())
+        pa, sa = SW.quantize_int3_np(a)
+        pt, st = SW.quantize_int3_torch(t)
+        assert np.array_equal(pa, pt.numpy())
+        assert np.array_equal(sa.astype(np.int16), st.view(torch.int16).numpy())
 
 
 def test_row_ranges_and_experts_are_consistent_slices():
@@ -60,6 +64,16 @@ def test_int4_configs_share_the_bf16_source_weights():
     a = SW.raw_np(synth.CONFIGS[2].model, "wq", 0, rows=(0, 4))
     b = SW.raw_np(synth.CONFIGS[3].model, "wq", 0, rows=(0, 4))
     assert np.array_equal(a, b)
+    # the int3-expert model: the same source weights, experts in int3 only
+    e3 = synth.FLINT_INT4_E3
+    for name, kw in (("wq", {}), ("exp_gate", {"expert": 7}), ("down", {})):
+        layer = 0 if name == "down" else 4
+        x = SW.raw_np(synth.CONFIGS[3].model, name, layer, rows=(0, 4), **kw)
+        y = SW.raw_np(e3, name, layer, rows=(0, 4), **kw)
+        assert np.array_equal(x, y)
+    assert isinstance(SW.linear_np(e3, "exp_down", 4, expert=1), tuple)
+    assert SW.linear_np(e3, "exp_down", 4, expert=1)[0].shape == (2048, 288)
+    assert SW.linear_np(e3, "wo", 4)[0].shape == (2048, 1024)
 
 
 def test_prompts_and_schedule():
