@@ -55,17 +55,17 @@ def step_bytes(m, ctxs, distinct_experts_per_layer) -> int:
     dense MLPs, lm_head, the embedding rows) + the KV cache read (all cached
     positions incl. the new one) + the KV written."""
     H, E = m.hidden, m.n_experts
-    if m.wdtype == "int4":
-        def lin(rows, K):
-            return rows * K // 2 + rows * (K // 64) * 2
-    else:
-        bpe = 2 if m.wdtype == "bf16" else 4
 
-        def lin(rows, K):
-            return rows * K * bpe
+    def lin(rows, K, fmt=m.wdtype):
+        if fmt == "int4":
+            return rows * K // 2 + rows * (K // 64) * 2
+        if fmt == "int3":
+            return rows * 3 * K // 8 + rows * (K // 64) * 2
+        return rows * K * (2 if fmt == "bf16" else 4)
     aux = 2 if m.aux_dtype == "bf16" else 4
     attn = lin(m.q_dim, H) + 2 * lin(m.kv_dim, H) + lin(H, m.q_dim) + 2 * H * aux
-    expert = 2 * lin(m.expert_ffn, H) + lin(H, m.expert_ffn)
+    xd = getattr(m, "xdtype", m.wdtype)
+    expert = 2 * lin(m.expert_ffn, H, xd) + lin(H, m.expert_ffn, xd)
     dense = 2 * lin(m.dense_ffn, H) + lin(H, m.dense_ffn)
     total = 0
     for l in range(m.n_layers):
@@ -408,7 +408,66 @@ def run_ours(args, rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(m, weights)
     eng.close()
+    if args.int3_steps > 0 and args.config == 3:
+        del weights
+        torch.cuda.empty_cache()
+        out["int3_experts"] = run_int3(args, dev)
     return out
+
+
+def run_int3(args, dev):
+    """The lower-bit expert variant: the same Flint model and workload as the
+    batch-1 line (2048-token prompt, greedy decode), the expert matrices in
+    int3 and every other linear layer in int4."""
+    import torch
+    import synth
+    from synth import prompts as SP
+    from synth import weights as SW
+    from moe_decode_megakernel_persistent_gb300.engine import Engine
+    wl = synth.EXTRA["flint-int4e3-ctx2048"]
+    m, K, W = wl.model, args.int3_steps, max(args.warmup, 3)
+    weights = SW.model_torch(m, dev)
+    prompt_len = wl.prompt_len
+    max_ctx = prompt_len + K + W + 72
+    eng = Engine(m, weights, n_pages=2 * ((max_ctx + 127) // 128) + 8, max_ctx=max_ctx, max_seqs=4)
+    stream = torch.cuda.current_stream()
+    wtok = torch.from_numpy(SP.prompt_tokens(m.seed, m.vocab, 64, seq=1)).to(dev)
+    tok1 = eng.prefill(1, wtok)
+    for i in range(W):
+        eng.decode_step([1], tok1, [64 + i], tok1)
+    eng.sync()
+    eng.release(1)
+    prompt = torch.from_numpy(SP.prompt_tokens(m.seed, m.vocab, prompt_len)).to(dev)
+    t0 = time.time()
+    tok = eng.prefill(0, prompt)
+    eng.sync()
+    prefill_s = time.time() - t0
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        eng.decode_step([0], tok, [prompt_len + i], tok)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    eng.sync()
+    eng.close()
+    ms = e0.elapsed_time(e1) / K
+    ctxs = [prompt_len + i + 1 for i in range(K)]
+    bytes_avg = sum(step_bytes(m, [c], m.top_k) for c in ctxs) / K
+    peaks, peak_kind = load_peaks()
+    achieved = bytes_avg / (ms * 1e-3) / 1e9
+    return {"workload": f"{wl.name}: the batch-1 workload with int3 experts (group 64), int4 elsewhere",
+            "value": round(1e3 / ms, 2), "unit": "tok/s", "steps": K, "ms_per_step": round(ms, 4),
+            "gpu_launches": K, "setup_s": {"prefill": round(prefill_s, 3)},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": peak_kind,
+                         "bytes_per_step": int(bytes_avg)},
+            "clocks": clk}
 
 
 def run_batch16(eng_factory, m, dev, world, args):
@@ -618,6 +677,8 @@ def main():
     ap.add_argument("--batch16-steps", type=int, default=1,
                     help="run the 16-client continuous-batching workload (0 = skip)")
     ap.add_argument("--no-timeline", action="store_true", help="skip the per-phase timeline launch")
+    ap.add_argument("--int3-steps", type=int, default=64,
+                    help="decode steps timed on the int3-expert model (0 = skip)")
     ap.add_argument("--split-steps", type=int, default=16,
                     help="decode steps timed as one launch per phase group (0 = skip)")
     ap.add_argument("--timeline-out", default="", help="save the timeline launch's raw stamps (.npz)")

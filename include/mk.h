@@ -59,6 +59,11 @@ extern "C" {
 #define MK_INT4_G64 2   /* symmetric int4: codes [rows, K/2] uint8, two's-complement
                            nibbles with the even k in the low nibble; scales
                            [rows, K/64] bfloat16; w[r,k] = q[r,k] * s[r,k/64] */
+#define MK_INT3_G64 3   /* symmetric int3 (expert matrices only): codes [rows, 3K/8]
+                           uint8, each 3 bytes one little-endian 24-bit word of 8
+                           consecutive k, the 3-bit two's-complement code of k at
+                           bits 3(k%8) .. 3(k%8)+2; scales [rows, K/64] bfloat16;
+                           w[r,k] = q[r,k] * s[r,k/64] */
 
 /* Model description.  The library compiles the decode step for fixed layer
  * shapes; mk_create() answers MK_ERR_UNSUPPORTED for others.  Compiled shapes:
@@ -87,9 +92,12 @@ typedef struct mk_model_desc {
   int32_t max_batch;    /* rows per launch, 1..16 */
   int32_t max_ctx;      /* largest position + 1 any sequence may reach */
   int32_t max_seqs;     /* sequence ids are 0 .. max_seqs-1 */
+  int32_t expert_wdtype;  /* format of exp_gate / exp_up / exp_down: equal to wdtype, or
+                             MK_INT3_G64 with wdtype MK_INT4_G64 (int3 experts, int4
+                             elsewhere); anything else is MK_ERR_INVALID_ARG */
 } mk_model_desc;
 
-/* A linear weight: `w` points at the codes / values; `scales` only for int4. */
+/* A linear weight: `w` points at the codes / values; `scales` only for int4 / int3. */
 typedef struct mk_linear {
   const void* w;
   const void* scales;
@@ -104,7 +112,7 @@ typedef struct mk_linear {
  *   dense layers (index < n_dense): gate, up [dense_ffn, hidden], down [hidden, dense_ffn]
  *   MoE layers: router [n_experts, hidden]; exp_gate, exp_up
  *   [n_experts, expert_ffn, hidden]; exp_down [n_experts, hidden, expert_ffn]
- *   (int4 scales stacked the same way).  Unused fields may be NULL. */
+ *   (int4 / int3 scales stacked the same way).  Unused fields may be NULL. */
 typedef struct mk_layer_weights {
   const void* attn_norm;
   mk_linear wq, wk, wv, wo;
@@ -154,9 +162,11 @@ MK_API int mk_create(const mk_model_desc* d, const mk_weights* w, mk_ctx** out);
 
 /* Bytes of the packed linear weights of a model (0 if d is invalid).  The
  * packed layout is the library's own: one 16-byte aligned record per output
- * row (codes, then the int4 group scales), the rows a decode task reads
- * together adjacent (the two RoPE rows of a q/k/v pair, the gate and up rows
- * of an FFN row).  The paper has no counterpart: it exists so that the
+ * row (codes, then the int4 / int3 group scales), the rows a decode task
+ * reads together adjacent (the two RoPE rows of a q/k/v pair, the gate and up
+ * rows of an FFN row).  An int3 record holds, per 32-value chunk, two words of
+ * 2-bit fields and one word of 1-bit fields (the codes plus 4), in the byte
+ * order of the kernel's dot products.  The paper has no counterpart: it exists so that the
  * allocation-free entry point can run on weights its caller packed. */
 MK_API size_t mk_packed_bytes(const mk_model_desc* d);
 
@@ -185,8 +195,8 @@ MK_API int mk_kv_alloc(mk_ctx* ctx, int32_t n_pages);
  * A chunk of up to 16 positions runs as one launch of the decode kernel.  A
  * longer chunk runs the model over all of its positions at once, layer by
  * layer: the projections as tensor-core GEMMs over the chunk's rows (cuBLAS,
- * fp32 accumulation; activations split into two 16-bit parts; int4 weights
- * widened exactly to fp16, bf16 weights used in place), attention, norms,
+ * fp32 accumulation; activations split into two 16-bit parts; int4 and int3
+ * weights widened exactly to fp16, bf16 weights used in place), attention, norms,
  * routing, the grouping of rows by expert and the residuals as the library's
  * kernels.  This path takes its pages up front, makes a workspace of about
  * 1.2 GB (Flint shape; kept by the context) on its first use, and waits for

@@ -1,7 +1,8 @@
 """In-tree build of libmk.so (the C-ABI library) with nvcc for sm_103a.
 
-The kernel translation unit and the host translation unit compile in
-parallel; the shared object lands next to this file.  Rebuilds only when a
+The translation units compile in parallel (the decode kernel's file once
+per group of its instantiations, MK_KERNEL_PART 0..3); the shared object
+lands next to this file.  Rebuilds only when a
 source or header is newer than the library.
 """
 from __future__ import annotations
@@ -21,7 +22,9 @@ BUILD = os.path.join(PKG, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
               "-I" + CSRC]
-SOURCES = ["mk_kernel.cu", "mk_host.cpp", "mk_static.cu", "mk_pack.cu", "mk_kv.cu", "mk_prefill.cu"]
+# (source, object name, extra flags)
+SOURCES = [("mk_kernel.cu", f"mk_kernel_p{p}", [f"-DMK_KERNEL_PART={p}"]) for p in range(4)] + [
+    (f, os.path.splitext(f)[0], []) for f in ("mk_host.cpp", "mk_static.cu", "mk_pack.cu", "mk_kv.cu", "mk_prefill.cu")]
 
 
 def _nvcc() -> str:
@@ -52,9 +55,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
 
-    def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS]
+    def compile_one(item):
+        src, name, extra = item
+        obj = os.path.join(BUILD, name + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra]
         if src.endswith(".cu") and verbose:
             cmd += ["-Xptxas", "-v"]
         cmd += ["-c", os.path.join(CSRC, src), "-o", obj]

@@ -20,8 +20,8 @@ MK_ERR_DEVICE_INDEX = 7
 ERR_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "NO_PAGES", 3: "STATE", 4: "CUDA",
              5: "UNSUPPORTED", 6: "BARRIER_TIMEOUT", 7: "DEVICE_INDEX"}
 
-MK_F32, MK_BF16, MK_INT4_G64 = 0, 1, 2
-WDTYPES = {"f32": MK_F32, "bf16": MK_BF16, "int4": MK_INT4_G64}
+MK_F32, MK_BF16, MK_INT4_G64, MK_INT3_G64 = 0, 1, 2, 3
+WDTYPES = {"f32": MK_F32, "bf16": MK_BF16, "int4": MK_INT4_G64, "int3": MK_INT3_G64}
 MK_DBG_TRACE = 1
 MK_DBG_SKIP_ARRIVAL = 2
 MK_DBG_TIMING = 4
@@ -40,7 +40,8 @@ class mk_model_desc(C.Structure):
                 ("n_dense", C.c_int32), ("dense_ffn", C.c_int32), ("n_experts", C.c_int32),
                 ("top_k", C.c_int32), ("expert_ffn", C.c_int32), ("rope_theta", C.c_float),
                 ("rms_eps", C.c_float), ("wdtype", C.c_int32), ("page_tokens", C.c_int32),
-                ("max_batch", C.c_int32), ("max_ctx", C.c_int32), ("max_seqs", C.c_int32)]
+                ("max_batch", C.c_int32), ("max_ctx", C.c_int32), ("max_seqs", C.c_int32),
+                ("expert_wdtype", C.c_int32)]
 
 
 class mk_linear(C.Structure):

@@ -8,7 +8,7 @@
 
 namespace mk {
 
-enum { WF32 = 0, WBF16 = 1, WINT4 = 2 };
+enum { WF32 = 0, WBF16 = 1, WINT4 = 2, WINT3 = 3 };
 
 // ------------------------------------------------------------------ shapes
 // The layer shapes the kernel is compiled for.  Flint: the model of "rec
@@ -32,6 +32,16 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(smem_u32(p)));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(const void* p) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p)));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
   return v;
 }
 __device__ __forceinline__ uint32_t lds16(const void* p) {
@@ -133,7 +143,7 @@ __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(k
 // up when another block has recorded an error, or after spin_limit_ns, and
 // then records MK_ERR_BARRIER_TIMEOUT; the caller skips to the exit path.
 // `ok` is a shared-memory word used to broadcast the outcome.
-__device__ __noinline__ bool grid_barrier(const StepArgs& a, uint32_t& k, volatile int* ok_word) {
+static __device__ __noinline__ bool grid_barrier(const StepArgs& a, uint32_t& k, volatile int* ok_word) {
   csync();
   if (threadIdx.x == 0) {
     ++k;
@@ -195,7 +205,7 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
 // `abort` is set, an error is recorded, or after limit_ns.  The first test is
 // inline; the spin loop is one out-of-line copy for every call site (the
 // kernel's code per layer is kept small: it is fetched again every layer).
-__device__ __noinline__ bool mbar_wait_loop(uint64_t* b, uint32_t parity, const volatile int* abort, int32_t* err,
+static __device__ __noinline__ bool mbar_wait_loop(uint64_t* b, uint32_t parity, const volatile int* abort, int32_t* err,
                                             uint64_t limit_ns, int site_detail) {
   uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
@@ -280,16 +290,56 @@ __device__ __forceinline__ float int4_chunk_dot(const uint4 w4, const uint4 (&p)
   return fmaf((float)(d2 - m.y), 65536.f, (float)lowmid);
 }
 
+// int3 weights: chunk = 32 codes in 12 bytes of a row's two planes.  The
+// row's low plane holds, per chunk, two words L0, L1 of 2-bit fields; its
+// high plane one word Hh of 1-bit fields.  Value 8t + 2i + e of the chunk
+// (t = 0..3, i = 0..3, e = 0..1, as in the staged activation's pieces) has
+// the offset code u = q + 4 in [0, 7]: its low two bits in byte i of
+// L[t / 2] at bit 2 (2 (t % 2) + e), its high bit in byte i of Hh at bit
+// 2t + e.  So one shift and mask of each plane gives the four codes of a
+// staged activation word, and the dot product is formed with dp4a as for
+// int4, corrected with 4 (not 8) times the plane sums.
+__device__ __forceinline__ float int3_chunk_dot(const uint4 w, const uint4 (&p)[6], const int4 m) {
+  const uint32_t L[2] = {w.x, w.y}, hh = w.z;
+  const uint32_t p0[4] = {p[0].x, p[0].y, p[0].z, p[0].w}, p1[4] = {p[1].x, p[1].y, p[1].z, p[1].w};
+  const uint32_t p2[4] = {p[2].x, p[2].y, p[2].z, p[2].w}, p3[4] = {p[3].x, p[3].y, p[3].z, p[3].w};
+  const uint32_t p4[4] = {p[4].x, p[4].y, p[4].z, p[4].w}, p5[4] = {p[5].x, p[5].y, p[5].z, p[5].w};
+  uint32_t d0 = 0, d1 = 0;
+  int d2 = 0;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    uint32_t u[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int fl = 2 * (2 * (t & 1) + e), fh = 2 * t + e;
+      const uint32_t hi = fh >= 2 ? (hh >> (fh - 2)) : (hh << (2 - fh));
+      u[e] = ((L[t >> 1] >> fl) & 0x03030303u) | (hi & 0x04040404u);
+    }
+    asm("dp4a.u32.u32 %0, %1, %2, %0;" : "+r"(d0) : "r"(p0[t]), "r"(u[0]));
+    asm("dp4a.u32.u32 %0, %1, %2, %0;" : "+r"(d0) : "r"(p1[t]), "r"(u[1]));
+    asm("dp4a.u32.u32 %0, %1, %2, %0;" : "+r"(d1) : "r"(p2[t]), "r"(u[0]));
+    asm("dp4a.u32.u32 %0, %1, %2, %0;" : "+r"(d1) : "r"(p3[t]), "r"(u[1]));
+    asm("dp4a.s32.u32 %0, %1, %2, %0;" : "+r"(d2) : "r"(p4[t]), "r"(u[0]));
+    asm("dp4a.s32.u32 %0, %1, %2, %0;" : "+r"(d2) : "r"(p5[t]), "r"(u[1]));
+  }
+  // sum y (q + 4) - 4 sum y = sum y q per plane (the metadata holds 8 sum y)
+  const int lowmid = ((int)d1 - (m.z >> 1)) * 256 + ((int)d0 - (m.w >> 1));
+  return fmaf((float)(d2 - (m.y >> 1)), 65536.f, (float)lowmid);
+}
+
 template <int WDT, int K>
 struct Gemv {
-  static constexpr int VPC = WDT == WINT4 ? 32 : (WDT == WBF16 ? 8 : 4);
+  // int4 and int3 rows share the 32-value chunk and the staged fixed-point
+  // activation (a model with int3 experts stages one form for both)
+  static constexpr bool QNT = WDT == WINT4 || WDT == WINT3;
+  static constexpr int VPC = QNT ? 32 : (WDT == WBF16 ? 8 : 4);
   static constexpr int NCH = K / VPC;
   static constexpr int CPL = (NCH + 31) / 32;
-  static constexpr int SUBS = WDT == WINT4 ? 6 : VPC / 4;  // 16-byte pieces of a staged chunk
-  static constexpr int META = WDT == WINT4 ? 16 : 0;
+  static constexpr int SUBS = QNT ? 6 : VPC / 4;  // 16-byte pieces of a staged chunk
+  static constexpr int META = QNT ? 16 : 0;
   static constexpr int ACT_BYTES = NCH * SUBS * 16 + NCH * META;
-  static constexpr int ROW_BYTES = WDT == WINT4 ? K / 2 : (WDT == WBF16 ? 2 * K : 4 * K);
-  static constexpr int SCALE_BYTES = WDT == WINT4 ? K / 64 * 2 : 0;
+  static constexpr int ROW_BYTES = WDT == WINT4 ? K / 2 : (WDT == WINT3 ? 3 * K / 8 : (WDT == WBF16 ? 2 * K : 4 * K));
+  static constexpr int SCALE_BYTES = QNT ? K / 64 * 2 : 0;
   // rows per aligned group: A rows of scales are a multiple of 16 bytes
   static constexpr int A = SCALE_BYTES == 0 ? 1
                          : (SCALE_BYTES % 16 == 0 ? 1 : (SCALE_BYTES % 8 == 0 ? 2 : (SCALE_BYTES % 4 == 0 ? 4 : 8)));
@@ -299,7 +349,7 @@ struct Gemv {
   static constexpr bool ACT_REGS = CPL <= 2;
   static constexpr int AR = ACT_REGS ? CPL : 1;
   static_assert(K % VPC == 0, "K must be a multiple of the chunk");
-  static_assert(WDT != WINT4 || K % 64 == 0, "int4 rows are whole scale groups");
+  static_assert(!QNT || K % 64 == 0, "int4 / int3 rows are whole scale groups");
   static_assert(ACT_BYTES % 16 == 0 && ROW_BYTES % 16 == 0, "16-byte aligned rows and vectors");
 
   struct Act {
@@ -315,7 +365,7 @@ struct Gemv {
         if (NCH % 32 == 0 || c < NCH) {
 #pragma unroll
           for (int t = 0; t < SUBS; ++t) a.v[j][t] = lds128(base + (t * NCH + c) * 16);
-          if constexpr (WDT == WINT4) {
+          if constexpr (QNT) {
             const uint4 m = lds128(base + NCH * SUBS * 16 + c * 16);
             a.m[j] = make_int4((int)m.x, (int)m.y, (int)m.z, (int)m.w);
           }
@@ -330,6 +380,8 @@ struct Gemv {
                                                 float acc) {
     if constexpr (WDT == WINT4) {
       return fmaf(int4_chunk_dot(w, p, m), __int_as_float(m.x) * sc, acc);
+    } else if constexpr (WDT == WINT3) {
+      return fmaf(int3_chunk_dot(w, p, m), __int_as_float(m.x) * sc, acc);
     } else if constexpr (WDT == WBF16) {
       const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
       const float av[8] = {__uint_as_float(p[0].x), __uint_as_float(p[0].y), __uint_as_float(p[0].z),
@@ -368,8 +420,13 @@ struct Gemv {
         float sc[2] = {1.f, 1.f};
 #pragma unroll
         for (int r = 0; r < RP; ++r) {
-          wv[r] = lds128(w[r] + 16 * c);
-          if constexpr (WDT == WINT4) sc[r] = bf16_to_f(lds16(s[r] + 2 * (c >> 1)));
+          if constexpr (WDT == WINT3) {
+            const uint2 lo = lds64(w[r] + 8 * c);
+            wv[r] = make_uint4(lo.x, lo.y, lds32(w[r] + 8 * NCH + 4 * c), 0u);
+          } else {
+            wv[r] = lds128(w[r] + 16 * c);
+          }
+          if constexpr (QNT) sc[r] = bf16_to_f(lds16(s[r] + 2 * (c >> 1)));
         }
         if constexpr (REGS) {
 #pragma unroll
@@ -379,7 +436,7 @@ struct Gemv {
 #pragma unroll
           for (int t = 0; t < SUBS; ++t) p[t] = lds128(base + (t * NCH + c) * 16);
           int4 m = make_int4(0, 0, 0, 0);
-          if constexpr (WDT == WINT4) {
+          if constexpr (QNT) {
             const uint4 mm = lds128(base + NCH * SUBS * 16 + c * 16);
             m = make_int4((int)mm.x, (int)mm.y, (int)mm.z, (int)mm.w);
           }

@@ -97,6 +97,8 @@ int validate_desc(const mk_model_desc* d, int* shape) {
   if (d->max_ctx < 1 || d->max_seqs < 1) return fail(MK_ERR_INVALID_ARG, "max_ctx / max_seqs must be >= 1");
   if (d->wdtype != MK_F32 && d->wdtype != MK_BF16 && d->wdtype != MK_INT4_G64)
     return fail(MK_ERR_INVALID_ARG, "unknown wdtype");
+  if (d->expert_wdtype != d->wdtype && !(d->wdtype == MK_INT4_G64 && d->expert_wdtype == MK_INT3_G64))
+    return fail(MK_ERR_INVALID_ARG, "expert_wdtype must equal wdtype, or be MK_INT3_G64 with MK_INT4_G64");
   if (!(d->rms_eps >= 0.f) || !(d->rope_theta > 0.f))
     return fail(MK_ERR_INVALID_ARG, "rms_eps must be >= 0 and rope_theta > 0");
   for (const ShapeRow& s : kShapes)
@@ -109,8 +111,10 @@ int validate_desc(const mk_model_desc* d, int* shape) {
   return fail(MK_ERR_UNSUPPORTED, "layer shape is not compiled into this library");
 }
 
-int check_lin(const mk_linear& l, bool int4, const char* what, int layer) {
-  if (!l.w || !aligned16(l.w) || (int4 && (!l.scales || !aligned16(l.scales))))
+bool quantised(int fmt) { return fmt == MK_INT4_G64 || fmt == MK_INT3_G64; }
+
+int check_lin(const mk_linear& l, bool scaled, const char* what, int layer) {
+  if (!l.w || !aligned16(l.w) || (scaled && (!l.scales || !aligned16(l.scales))))
     return fail(MK_ERR_INVALID_ARG, std::string("weight ") + what + " of layer " +
                                         std::to_string(layer) + " is NULL or not 16-byte aligned");
   return MK_OK;
@@ -331,9 +335,10 @@ int host_check_model(const mk_model_desc* d, const mk_weights* w, int* shape, La
     for (int k = 0; k < NLIN; ++k) {
       const bool used = k <= WO || (dense ? (k >= GATE && k <= DOWN) : k >= EGATE);
       if (!used) continue;
-      if (int r = check_lin(*lin[k], int4, names[k], l)) return r;
+      const bool scaled = quantised(k >= EGATE ? d->expert_wdtype : d->wdtype);
+      if (int r = check_lin(*lin[k], scaled, names[k], l)) return r;
       o.w[k] = lin[k]->w;
-      o.s[k] = int4 ? lin[k]->scales : nullptr;
+      o.s[k] = scaled ? lin[k]->scales : nullptr;
     }
     if (!dense) {
       if (int r = check_aux(L.router, "router", l)) return r;
@@ -365,42 +370,14 @@ MK_API int mk_create(const mk_model_desc* d, const mk_weights* w, mk_ctx** out) 
   *out = nullptr;
   int shape = -1;
   if (int r = validate_desc(d, &shape)) return r;
-  if (!w || !w->layers) return fail(MK_ERR_INVALID_ARG, "weights or weights->layers is NULL");
-  const bool int4 = d->wdtype == MK_INT4_G64;
-  if (int r = check_aux(w->embed, "embed", -1)) return r;
-  if (int r = check_aux(w->final_norm, "final_norm", -1)) return r;
-  if (int r = check_lin(w->lm_head, int4, "lm_head", -1)) return r;
   std::vector<LayerW> lw(d->n_layers);
-  for (int l = 0; l < d->n_layers; ++l) {
-    const mk_layer_weights& L = w->layers[l];
-    LayerW& o = lw[l];
-    std::memset(&o, 0, sizeof(o));
-    if (int r = check_aux(L.attn_norm, "attn_norm", l)) return r;
-    if (int r = check_aux(L.ffn_norm, "ffn_norm", l)) return r;
-    const mk_linear* lin[NLIN] = {&L.wq, &L.wk, &L.wv, &L.wo, &L.gate, &L.up, &L.down,
-                                  &L.exp_gate, &L.exp_up, &L.exp_down};
-    static const char* names[NLIN] = {"wq", "wk", "wv", "wo", "gate", "up", "down",
-                                      "exp_gate", "exp_up", "exp_down"};
-    const bool dense = l < d->n_dense;
-    for (int k = 0; k < NLIN; ++k) {
-      const bool used = k <= WO || (dense ? (k >= GATE && k <= DOWN) : k >= EGATE);
-      if (!used) continue;
-      if (int r = check_lin(*lin[k], int4, names[k], l)) return r;
-      o.w[k] = lin[k]->w;
-      o.s[k] = int4 ? lin[k]->scales : nullptr;
-    }
-    if (!dense) {
-      if (int r = check_aux(L.router, "router", l)) return r;
-      o.router = L.router;
-    }
-    o.attn_norm = L.attn_norm;
-    o.ffn_norm = L.ffn_norm;
-  }
+  if (int r = host_check_model(d, w, &shape, lw.data())) return r;
+  const bool int4 = d->wdtype == MK_INT4_G64;
 
   mk_ctx* c = new mk_ctx();
   c->d = *d;
   c->shape = shape;
-  c->kern = get_kernel(shape, d->wdtype);
+  c->kern = get_kernel(shape, d->wdtype, d->expert_wdtype);
   auto bail = [&](int code) {
     mk_destroy(c);
     return code;

@@ -182,8 +182,23 @@ struct KernelInfo {
 };
 inline int launch_smem_bytes(const KernelInfo& k, int rows) { return rows == 1 ? k.smem_single : k.smem_bytes; }
 
-// Returns the kernel for (shape, wdtype) or fn == nullptr if not compiled.
-KernelInfo get_kernel(int shape, int wdtype);
+// The kernel variants, by translation unit (mk_kernel.cu is compiled once per
+// part); each returns fn == nullptr for the variants it does not hold.
+KernelInfo get_kernel_part0(int shape, int wdtype, int xdtype);
+KernelInfo get_kernel_part1(int shape, int wdtype, int xdtype);
+KernelInfo get_kernel_part2(int shape, int wdtype, int xdtype);
+KernelInfo get_kernel_part3(int shape, int wdtype, int xdtype);
+// Returns the kernel for (shape, linear-layer format, expert format) or
+// fn == nullptr if not compiled.
+inline KernelInfo get_kernel(int shape, int wdtype, int xdtype) {
+  KernelInfo (*const parts[4])(int, int, int) = {get_kernel_part0, get_kernel_part1, get_kernel_part2,
+                                                 get_kernel_part3};
+  for (auto f : parts) {
+    const KernelInfo k = f(shape, wdtype, xdtype);
+    if (k.fn) return k;
+  }
+  return {nullptr, 0, 0, 0};
+}
 
 // Host helpers of mk_host.cpp shared with the allocation-free entry point.
 // host_check_model: validates the description and weight pointers and fills

@@ -193,23 +193,15 @@ struct Producer {
   }
 };
 
-__device__ __forceinline__ uint2 lds64(const void* p) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p)));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds32(const void* p) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
-  return v;
-}
 
 struct ActRange {
   const uint8_t* list;   // staged index of the i-th activation: list ? list[start + i] : start + i
   int start, count;
 };
 
-template <class S, int WDT>
+// WDT: the format of the linear layers; XDT: the format of the expert
+// matrices (WDT, or int3 experts in an int4 model)
+template <class S, int WDT, int XDT = WDT>
 struct Model {
   static constexpr int AUX = WDT == WF32 ? WF32 : WBF16;
   static constexpr int H = S::H, NH = S::NH, NKV = S::NKV, HD = S::HD, E = S::E, TOPK = S::TOPK;
@@ -219,17 +211,23 @@ struct Model {
   using GQ = Gemv<WDT, QD>;
   using GE = Gemv<WDT, FE>;
   using GD = Gemv<WDT, FD>;
+  using GXH = Gemv<XDT, H>;   // expert gate / up rows
+  using GXE = Gemv<XDT, FE>;  // expert down rows
+  static_assert(XDT == WDT || (WDT == WINT4 && XDT == WINT3), "int3 experts come with int4 layers");
+  static_assert(GXH::ACT_BYTES == GH::ACT_BYTES && GXE::ACT_BYTES == GE::ACT_BYTES,
+                "expert rows read the layers' staged activations");
 
   // ring stage: 17 KB for int4 (16 KB of codes + their scales), 32 KB for
   // bf16 and 16 KB for fp32 weights
   static constexpr int STAGE = WDT == WINT4 ? 17408 : (WDT == WBF16 ? 32768 : 16384);
   __host__ __device__ static constexpr int cmax(int a, int b) { return a > b ? a : b; }
   // a packed weight record: one row's codes, then its scales, 16-byte aligned
-  template <int K>
+  template <int K, int FMT = WDT>
   __host__ __device__ static constexpr int rec() {
-    return (Gemv<WDT, K>::ROW_BYTES + Gemv<WDT, K>::SCALE_BYTES + 15) / 16 * 16;
+    return (Gemv<FMT, K>::ROW_BYTES + Gemv<FMT, K>::SCALE_BYTES + 15) / 16 * 16;
   }
   static constexpr int REC_H = rec<H>(), REC_Q = rec<QD>(), REC_E = rec<FE>(), REC_D = rec<FD>();
+  static constexpr int REC_XH = rec<H, XDT>(), REC_XE = rec<FE, XDT>();
   // hidden rows go to blocks in groups of 2, so a block's slice of a bf16 row
   // (router, norm) starts and ends on a 4-byte boundary
   static constexpr int A_Q = 1;
@@ -237,11 +235,13 @@ struct Model {
   // tasks per tile (RP records each)
   static constexpr int T_QKV = STAGE / (2 * REC_H);
   static constexpr int T_O = STAGE / REC_Q;
-  static constexpr int T_GU = STAGE / (2 * REC_H);
-  static constexpr int T_DN = STAGE / REC_E;
+  static constexpr int T_GU = STAGE / (2 * REC_H);   // dense gate / up
+  static constexpr int T_XGU = STAGE / (2 * REC_XH); // expert gate / up
+  static constexpr int T_XDN = STAGE / REC_XE;       // expert down
   static constexpr int T_DD = STAGE / REC_D;
   static constexpr int T_LM = STAGE / REC_H;
-  static_assert(T_QKV >= 1 && T_O >= 1 && T_GU >= 1 && T_DN >= 1 && T_DD >= 1 && T_LM >= 1, "tile sizes");
+  static_assert(T_QKV >= 1 && T_O >= 1 && T_GU >= 1 && T_XGU >= 1 && T_XDN >= 1 && T_DD >= 1 && T_LM >= 1,
+                "tile sizes");
   static constexpr int TU = STAGE / (4 * HD) / kWarps;  // positions per warp per stage
   static constexpr int TT = TU * kWarps;              // cached positions per stage (K and V rows, bf16)
   static_assert(TU >= 1, "a stage holds a position per warp");
@@ -345,7 +345,7 @@ struct Model {
   // one warp, whose activation registers then reload rarely).  TK provides
   //   ActRange acts(t) and void put(t, ai, i, v0, v1) (one lane writes the
   //   results of task t for activation ai, the i-th of the task's list).
-  template <int K, int RP, int T, bool REGS, bool CONTIG, bool MMA, class TK>
+  template <int K, int RP, int T, bool REGS, bool CONTIG, bool MMA, int FMT = WDT, class TK>
   __device__ static __forceinline__ void run_gemv(int ntask, const uint8_t* act_base, const TK& task) {
     if constexpr (TC && MMA) {
       if (fixed().ctx.tc) {
@@ -353,7 +353,7 @@ struct Model {
         return;
       }
     }
-    using Gv = Gemv<WDT, K>;
+    using Gv = Gemv<FMT, K>;
     Fixed& F = fixed();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     uint32_t k = F.kc;
@@ -369,7 +369,7 @@ struct Model {
 #pragma unroll 1
       for (int j = j_first; j < j_end;) {
         const int t = t0 + j;
-        constexpr int RC = rec<K>();
+        constexpr int RC = rec<K, FMT>();
         const ActRange ar = task.acts(t);
         // one-row tasks of a contiguous block: two consecutive rows that share
         // an activation list are dotted together (two independent chains)
@@ -1399,7 +1399,7 @@ struct Model {
           a->sc.act[(b * TOPK + j) * FE + f] = silu(v0) * v1;
         }
       } task{&a, &F, u0, lane};
-      run_gemv<H, 2, T_GU, false, false, false>(u1 - u0, c.act, task);
+      run_gemv<H, 2, T_XGU, false, false, false, XDT>(u1 - u0, c.act, task);
     } else {
       int f0, f1;
       gu_range(c, FD, f0, f1);
@@ -1478,7 +1478,7 @@ struct Model {
           F->dots[e0 + ai][t % nr] = v0;
         }
       } task{&F, u, nr, e0, lane};
-      run_gemv<FE, 1, T_DN, GE::ACT_REGS, true, false>((ub - u) * nr, c.act, task);
+      run_gemv<FE, 1, T_XDN, GXE::ACT_REGS, true, false, XDT>((ub - u) * nr, c.act, task);
     } else {
       const int cnt = min(ub, c.n) - u;
       struct {
@@ -1731,14 +1731,14 @@ struct Model {
         int u0, u1;
         gu_range(c, F.n_ue * FE, u0, u1);
 #pragma unroll 1
-        for (int ta = u0; ta < u1; ta += T_GU) {
+        for (int ta = u0; ta < u1; ta += T_XGU) {
           if (!p.template begin<STAGE>()) return;
-          const int tb = min(u1, ta + T_GU);
+          const int tb = min(u1, ta + T_XGU);
 #pragma unroll 1
           for (int q0 = ta; q0 < tb;) {  // a run stays inside one expert: records 2t, 2t + 1
             const int q1 = min(tb, (q0 / FE + 1) * FE);
             const size_t t = (size_t)F.ue_expert[q0 / FE] * FE + q0 % FE;
-            put_recs(p, 2 * (q0 - ta), 2 * (q1 - q0), Lg.pk[PK_GU] + 2 * t * REC_H, REC_H);
+            put_recs(p, 2 * (q0 - ta), 2 * (q1 - q0), Lg.pk[PK_GU] + 2 * t * REC_XH, REC_XH);
             q0 = q1;
           }
           p.end();
@@ -1750,14 +1750,14 @@ struct Model {
           const int ub = moe_round_end(F, ua, cap);
           const int ntask = (ub - ua) * nr;
 #pragma unroll 1
-          for (int ta = 0; ta < ntask; ta += T_DN) {
+          for (int ta = 0; ta < ntask; ta += T_XDN) {
             if (!p.template begin<STAGE>()) return;
-            const int tb = min(ntask, ta + T_DN);
+            const int tb = min(ntask, ta + T_XDN);
 #pragma unroll 1
             for (int q0 = ta; q0 < tb;) {  // a run stays inside one expert
               const int q1 = min(tb, (q0 / nr + 1) * nr);
               const size_t row = (size_t)F.ue_expert[ua + q0 / nr] * H + c.r0 + q0 % nr;
-              put_recs(p, q0 - ta, q1 - q0, Lg.pk[PK_DN] + row * REC_E, REC_E);
+              put_recs(p, q0 - ta, q1 - q0, Lg.pk[PK_DN] + row * REC_XE, REC_XE);
               q0 = q1;
             }
             p.end();
@@ -1798,9 +1798,9 @@ struct Model {
   }
 };
 
-template <class S, int WDT>
+template <class S, int WDT, int XDT>
 __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_constant__ StepArgs a) {
-  using M = Model<S, WDT>;
+  using M = Model<S, WDT, XDT>;
   extern __shared__ __align__(128) uint8_t smem[];
   Fixed& F = *reinterpret_cast<Fixed*>(smem);
   const int tid = threadIdx.x;
@@ -1990,22 +1990,39 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
   }
 }
 
-template <class S, int WDT>
+template <class S, int WDT, int XDT = WDT>
 static KernelInfo make() {
-  return {reinterpret_cast<const void*>(&step_kernel<S, WDT>), kSmemBytes, Model<S, WDT>::TT,
-          Model<S, WDT>::SMEM_SINGLE};
+  return {reinterpret_cast<const void*>(&step_kernel<S, WDT, XDT>), kSmemBytes, Model<S, WDT, XDT>::TT,
+          Model<S, WDT, XDT>::SMEM_SINGLE};
 }
 
-KernelInfo get_kernel(int shape, int wdtype) {
-  if (shape == SHAPE_FLINT) {
-    if (wdtype == MK_INT4_G64) return make<ShapeFlint, WINT4>();
-    if (wdtype == MK_BF16) return make<ShapeFlint, WBF16>();
-  } else if (shape == SHAPE_TINY) {
-    if (wdtype == MK_INT4_G64) return make<ShapeTiny, WINT4>();
-    if (wdtype == MK_BF16) return make<ShapeTiny, WBF16>();
-    if (wdtype == MK_F32) return make<ShapeTiny, WF32>();
-  }
-  return {nullptr, 0, 0};
+// The instantiations are spread over translation units (this file compiled
+// once per value of MK_KERNEL_PART), which build in parallel.
+#if MK_KERNEL_PART == 0
+KernelInfo get_kernel_part0(int shape, int wdtype, int xdtype) {
+  if (shape == SHAPE_FLINT && wdtype == MK_INT4_G64 && xdtype == wdtype) return make<ShapeFlint, WINT4>();
+  return {nullptr, 0, 0, 0};
 }
+#elif MK_KERNEL_PART == 1
+KernelInfo get_kernel_part1(int shape, int wdtype, int xdtype) {
+  if (shape == SHAPE_FLINT && wdtype == MK_BF16 && xdtype == wdtype) return make<ShapeFlint, WBF16>();
+  return {nullptr, 0, 0, 0};
+}
+#elif MK_KERNEL_PART == 2
+KernelInfo get_kernel_part2(int shape, int wdtype, int xdtype) {
+  if (shape == SHAPE_FLINT && wdtype == MK_INT4_G64 && xdtype == MK_INT3_G64) return make<ShapeFlint, WINT4, WINT3>();
+  return {nullptr, 0, 0, 0};
+}
+#else
+KernelInfo get_kernel_part3(int shape, int wdtype, int xdtype) {
+  if (shape == SHAPE_TINY) {
+    if (wdtype == MK_INT4_G64 && xdtype == wdtype) return make<ShapeTiny, WINT4>();
+    if (wdtype == MK_INT4_G64 && xdtype == MK_INT3_G64) return make<ShapeTiny, WINT4, WINT3>();
+    if (wdtype == MK_BF16 && xdtype == wdtype) return make<ShapeTiny, WBF16>();
+    if (wdtype == MK_F32 && xdtype == wdtype) return make<ShapeTiny, WF32>();
+  }
+  return {nullptr, 0, 0, 0};
+}
+#endif
 
 }  // namespace mk

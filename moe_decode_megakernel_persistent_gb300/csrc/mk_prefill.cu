@@ -6,7 +6,7 @@
 //
 // The linear layers are dense contractions over the chunk's rows and run as
 // tensor-core GEMMs (cuBLAS, fp32 accumulation).  bf16 weights are used in
-// place with bf16 activation operands.  int4 weights are widened, per layer,
+// place with bf16 activation operands.  int4 and int3 weights are widened, per layer,
 // from the library's packed records to fp16, which holds code * group scale
 // exactly (a 3-bit code times an 8-bit bf16 scale needs at most 11 significant
 // bits), with fp16 activation operands.  Every activation is split into two
@@ -158,6 +158,24 @@ __global__ void k_widen_int4(const uint8_t* rec, int rec_bytes, int K, long long
     const int q1 = (int)(b >> 4) - ((b & 0x80) ? 16 : 0);
     out[(size_t)r * K + 2 * j] = f2h((float)q0 * s);
     out[(size_t)r * K + 2 * j + 1] = f2h((float)q1 * s);
+  }
+}
+
+// int3 records (the kernel's bit planes, then bf16 group scales; see
+// mk_pack.cu) -> fp16 rows [rows][K]: exact as for int4 (|q| <= 4).
+__global__ void k_widen_int3(const uint8_t* rec, int rec_bytes, int K, long long rows, uint16_t* out) {
+  const int nch = K / 32;
+  const long long total = rows * K;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / K;
+    const int k = (int)(i % K), c = k / 32, v = k % 32;
+    const int t = v / 8, bi = (v % 8) / 2, e = v % 2;
+    const uint8_t* p = rec + (size_t)r * rec_bytes;
+    const uint32_t lw = reinterpret_cast<const uint32_t*>(p + 8 * c)[t / 2];
+    const uint32_t hw = reinterpret_cast<const uint32_t*>(p + 8 * nch)[c];
+    const int u = (int)(((lw >> (8 * bi + 2 * (2 * (t % 2) + e))) & 3u) | (((hw >> (8 * bi + 2 * t + e)) & 1u) << 2));
+    const float s = bf2f(reinterpret_cast<const uint16_t*>(p + 3 * K / 8)[k / 64]);
+    out[(size_t)r * K + k] = f2h((float)(u - 4) * s);
   }
 }
 
@@ -545,6 +563,7 @@ struct Dims {
   int H, NH, NKV, HD, QD, KD, NQKV, E, K, FE, FD, V;
   bool aux_f32;
   int wdtype;
+  int xdtype;  // the expert matrices' format
   int fmt;    // activation operand format
   int esz;    // bytes of one operand element (4 fp32, 2 bf16 / fp16)
 };
@@ -571,12 +590,19 @@ int gemm(PrefillWork& w, const Dims& d, int M, int N, int Kd, const void* W, int
                   "cublasGemmEx");
 }
 
-// The operand of `rows` packed records of width Kd: int4 widened into the
-// scratch, bf16 / fp32 records used in place (a record is exactly one row).
-const void* weight_rows(PrefillWork& w, const Dims& d, const uint8_t* rec, long long rows, int Kd, cudaStream_t st) {
-  if (d.wdtype != MK_INT4_G64) return rec;
-  k_widen_int4<<<grid_for(rows * Kd / 2), 256, 0, st>>>(rec, pack_rec_bytes(d.wdtype, Kd), Kd, rows, w.Wb);
-  return w.Wb;
+// The operand of `rows` packed records of width Kd in format fmt: int4 /
+// int3 widened into the scratch, bf16 / fp32 records used in place (a record
+// is exactly one row).
+const void* weight_rows(PrefillWork& w, int fmt, const uint8_t* rec, long long rows, int Kd, cudaStream_t st) {
+  if (fmt == MK_INT4_G64) {
+    k_widen_int4<<<grid_for(rows * Kd / 2), 256, 0, st>>>(rec, pack_rec_bytes(fmt, Kd), Kd, rows, w.Wb);
+    return w.Wb;
+  }
+  if (fmt == MK_INT3_G64) {
+    k_widen_int3<<<grid_for(rows * Kd), 256, 0, st>>>(rec, pack_rec_bytes(fmt, Kd), Kd, rows, w.Wb);
+    return w.Wb;
+  }
+  return rec;
 }
 
 }  // namespace
@@ -596,6 +622,7 @@ int prefill_run(PrefillWork** pw, const PrefillArgs& a, cudaStream_t st) {
   d.H = m.hidden; d.NH = m.n_heads; d.NKV = m.n_kv_heads; d.HD = m.head_dim; d.QD = m.n_heads * m.head_dim;
   d.KD = m.n_kv_heads * m.head_dim; d.NQKV = d.QD + 2 * d.KD; d.E = m.n_experts; d.K = m.top_k;
   d.FE = m.expert_ffn; d.FD = m.dense_ffn; d.V = m.vocab; d.wdtype = m.wdtype;
+  d.xdtype = m.expert_wdtype;
   d.aux_f32 = m.wdtype == MK_F32;
   d.fmt = m.wdtype == MK_F32 ? ACT_F32 : (m.wdtype == MK_BF16 ? ACT_BF16 : ACT_F16);
   d.esz = d.fmt == ACT_F32 ? 4 : 2;
@@ -613,7 +640,7 @@ int prefill_run(PrefillWork** pw, const PrefillArgs& a, cudaStream_t st) {
     const size_t kmax = std::max({H, QD, (size_t)d.FD, (size_t)d.FE});
     w->a_elems = std::max({ent * H, MM * kmax, ent * (size_t)d.FE});
     w->c_elems = std::max({MM * d.NQKV, MM * 2 * (size_t)d.FD, ent * 2 * (size_t)d.FE, MM * H, MM * E});
-    w->wb_elems = d.wdtype == MK_INT4_G64
+    w->wb_elems = d.wdtype == MK_INT4_G64 || d.xdtype == MK_INT3_G64
                       ? std::max({E * 2 * d.FE * H, E * H * d.FE, 2 * (size_t)d.FD * H, H * (size_t)d.FD,
                                   (size_t)d.NQKV * H, H * QD})
                       : 0;
@@ -664,7 +691,7 @@ int prefill_run(PrefillWork** pw, const PrefillArgs& a, cudaStream_t st) {
     // attention block
     k_norm_act<<<M, TB, 0, st>>>(w.X, nullptr, nullptr, Lw.attn_norm, d.aux_f32, m.rms_eps, d.H, w.A, lo, d.fmt,
                                  nullptr);
-    const void* W = weight_rows(w, d, Lw.pk[PK_QKV], d.NQKV, d.H, st);
+    const void* W = weight_rows(w, d.wdtype, Lw.pk[PK_QKV], d.NQKV, d.H, st);
     if (int r = gemm(w, d, M, d.NQKV, d.H, W, d.H, w.A, lo, w.C, d.NQKV)) return r;
     k_qkv_epi<<<grid_for((long long)M * d.NQKV / 2), TB, 0, st>>>(w.C, d.NQKV, d.NH, d.NKV, d.HD, a.rope, a.start, M,
                                                                    w.Q, a.kv, a.block_table, a.slot,
@@ -684,16 +711,16 @@ int prefill_run(PrefillWork** pw, const PrefillArgs& a, cudaStream_t st) {
     if (a.trace)
       k_trace_rows<<<32, TB, 0, st>>>(w.O, d.QD, tr0, tr_rows, d.QD, tr_attn + (size_t)l * tr_rows * d.QD);
     k_norm_act<<<M, TB, 0, st>>>(w.O, nullptr, nullptr, nullptr, d.aux_f32, 0.f, d.QD, w.A, lo, d.fmt, nullptr);
-    W = weight_rows(w, d, Lw.pk[PK_O], d.H, d.QD, st);
+    W = weight_rows(w, d.wdtype, Lw.pk[PK_O], d.H, d.QD, st);
     if (int r = gemm(w, d, M, d.H, d.QD, W, d.QD, w.A, lo, w.C, d.H)) return r;
     // h = x + attention; the FFN input
     k_norm_act<<<M, TB, 0, st>>>(w.X, w.C, w.Hr, Lw.ffn_norm, d.aux_f32, m.rms_eps, d.H, w.A, lo, d.fmt,
                                  dense ? nullptr : w.Z);
     if (dense) {
-      W = weight_rows(w, d, Lw.pk[PK_GU], 2LL * d.FD, d.H, st);
+      W = weight_rows(w, d.wdtype, Lw.pk[PK_GU], 2LL * d.FD, d.H, st);
       if (int r = gemm(w, d, M, 2 * d.FD, d.H, W, d.H, w.A, lo, w.C, 2 * d.FD)) return r;
       k_silu_act<<<grid_for((long long)M * d.FD), TB, 0, st>>>(w.C, M, d.FD, w.A, lo, d.fmt);
-      W = weight_rows(w, d, Lw.pk[PK_DN], d.H, d.FD, st);
+      W = weight_rows(w, d.wdtype, Lw.pk[PK_DN], d.H, d.FD, st);
       if (int r = gemm(w, d, M, d.H, d.FD, W, d.FD, w.A, lo, w.C, d.H)) return r;
       k_add<<<grid_for((long long)M * d.H), TB, 0, st>>>(w.Hr, w.C, w.X, (long long)M * d.H);
     } else {
@@ -721,7 +748,7 @@ int prefill_run(PrefillWork** pw, const PrefillArgs& a, cudaStream_t st) {
                         cudaMemcpyDeviceToDevice, st);
       k_gather<<<grid_for((long long)n_ent * d.H), TB, 0, st>>>(w.D, (size_t)M * d.H, G, lo, w.ent, n_ent, d.H, d.fmt);
       // gate/up of every expert, then SiLU
-      W = weight_rows(w, d, Lw.pk[PK_GU], 2LL * d.E * d.FE, d.H, st);
+      W = weight_rows(w, d.xdtype, Lw.pk[PK_GU], 2LL * d.E * d.FE, d.H, st);
       const size_t wrow = d.esz;
       for (int x = 0; x < d.E; ++x) {
         const int mx = off[x + 1] - off[x];
@@ -732,7 +759,7 @@ int prefill_run(PrefillWork** pw, const PrefillArgs& a, cudaStream_t st) {
           return r;
       }
       k_silu_act<<<grid_for((long long)n_ent * d.FE), TB, 0, st>>>(w.C, n_ent, d.FE, w.A, lo, d.fmt);
-      W = weight_rows(w, d, Lw.pk[PK_DN], (long long)d.E * d.H, d.FE, st);
+      W = weight_rows(w, d.xdtype, Lw.pk[PK_DN], (long long)d.E * d.H, d.FE, st);
       for (int x = 0; x < d.E; ++x) {
         const int mx = off[x + 1] - off[x];
         if (!mx) continue;

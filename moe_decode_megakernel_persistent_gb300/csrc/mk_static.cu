@@ -146,7 +146,7 @@ extern "C" MK_API int mk_decode_step_static(
     if (pages_host[i] < 0 || pages_host[i] >= n_pages)
       return host_fail(MK_ERR_INVALID_ARG, "page out of range [0, n_pages)");
   }
-  const KernelInfo kern = get_kernel(shape, d->wdtype);
+  const KernelInfo kern = get_kernel(shape, d->wdtype, d->expert_wdtype);
   if (!kern.fn) return host_fail(MK_ERR_UNSUPPORTED, "no kernel for this shape and dtype");
 
   int dev = 0, sms = 0;

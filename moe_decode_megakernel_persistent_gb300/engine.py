@@ -10,7 +10,9 @@ logical layouts of include/mk.h:
     ("wq"|"wk"|"wv"|"wo", l)                   W or (codes, scales)
     dense layers: ("gate"|"up"|"down", l)      W or (codes, scales)
     MoE layers:   ("router", l) [E, H]
-                  ("exp_gate"|"exp_up"|"exp_down", l)  stacked over experts
+                  ("exp_gate"|"exp_up"|"exp_down", l)  stacked over experts (W or
+                  (codes, scales) in the experts' format: int3 experts with int4
+                  elsewhere, or the layers' format)
 """
 from __future__ import annotations
 
@@ -36,14 +38,17 @@ def _lin(x) -> L.mk_linear:
 
 
 def make_desc(shape, max_batch: int = 16, max_ctx: int = 16384, max_seqs: int = 64) -> L.mk_model_desc:
-    """mk_model_desc from an object with the model fields (n_layers, hidden, ...)."""
+    """mk_model_desc from an object with the model fields (n_layers, hidden, ...;
+    `xdtype`, the experts' format, if it has one)."""
+    xdtype = getattr(shape, "xdtype", shape.wdtype)
     return L.mk_model_desc(
         n_layers=shape.n_layers, hidden=shape.hidden, n_heads=shape.n_heads,
         n_kv_heads=shape.n_kv_heads, head_dim=shape.head_dim, vocab=shape.vocab,
         n_dense=shape.n_dense, dense_ffn=shape.dense_ffn, n_experts=shape.n_experts,
         top_k=shape.top_k, expert_ffn=shape.expert_ffn, rope_theta=shape.rope_theta,
         rms_eps=shape.rms_eps, wdtype=L.WDTYPES[shape.wdtype], page_tokens=128,
-        max_batch=max_batch, max_ctx=max_ctx, max_seqs=max_seqs)
+        max_batch=max_batch, max_ctx=max_ctx, max_seqs=max_seqs,
+        expert_wdtype=L.WDTYPES[xdtype])
 
 
 class Engine:

@@ -9,6 +9,30 @@ from synth import weights as SW
 from synth.configs import ModelShape
 
 
+def weights_struct(m: ModelShape, w: dict):
+    """The C ABI's mk_weights over a dict of device tensors (the Engine's
+    weight dict format); returns (weights, layers), the second to be kept
+    alive with the first."""
+    from moe_decode_megakernel_persistent_gb300 import _lib as L
+    from moe_decode_megakernel_persistent_gb300.engine import _lin, _ptr
+    layers = (L.mk_layer_weights * m.n_layers)()
+    for l in range(m.n_layers):
+        lw = layers[l]
+        lw.attn_norm = _ptr(w[("attn_norm", l)])
+        lw.ffn_norm = _ptr(w[("ffn_norm", l)])
+        for name in ("wq", "wk", "wv", "wo"):
+            setattr(lw, name, _lin(w[(name, l)]))
+        if l < m.n_dense:
+            for name in ("gate", "up", "down"):
+                setattr(lw, name, _lin(w[(name, l)]))
+        else:
+            lw.router = _ptr(w[("router", l)])
+            for name in ("exp_gate", "exp_up", "exp_down"):
+                setattr(lw, name, _lin(w[(name, l)]))
+    return L.mk_weights(embed=_ptr(w[("embed",)]), final_norm=_ptr(w[("final_norm",)]),
+                        lm_head=_lin(w[("lm_head",)]), layers=layers), layers
+
+
 def synth_fetch(m: ModelShape):
     """fetch(name, layer, expert) -> (raw, dtype) from the seeded generator,
     keeping the storage-format tensors it has produced."""

@@ -80,7 +80,7 @@ def host_fetch(m, w):
             t = (t[0][expert], t[1][expert]) if isinstance(t, tuple) else t[expert]
         if isinstance(t, tuple):
             raw = (to_np(t[0]), to_np(t[1]))
-            dt = "int4"
+            dt = SW.storage_dtype(m, name)
         else:
             raw = to_np(t)
             dt = "f32" if t.dtype == torch.float32 else "bf16"

@@ -71,6 +71,28 @@ def test_create_rejects_misaligned_weights(lib):
     assert "attn_norm" in L.mk_last_error()
 
 
+def test_expert_format_is_validated_and_sizes_the_packed_weights(lib):
+    out = C.c_void_p()
+    w = L.mk_weights()
+    # int3 experts only come with int4 layers
+    assert lib.mk_create(C.byref(_desc(expert_wdtype=L.MK_INT3_G64)), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    assert "expert_wdtype" in L.mk_last_error()
+    assert lib.mk_create(C.byref(_desc(expert_wdtype=L.MK_BF16)), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    assert "expert_wdtype" in L.mk_last_error()
+    # a valid mixed description gets past the description to the weights
+    d = make_desc(synth.FLINT_INT4_E3)
+    assert d.expert_wdtype == L.MK_INT3_G64 and d.wdtype == L.MK_INT4_G64
+    assert lib.mk_create(C.byref(d), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    assert "NULL" in L.mk_last_error()
+    # packed bytes by hand: per MoE layer the gate/up records (2 x 64 x 768 rows
+    # of K = 2048) shrink from 1024 + 64 to 768 + 64 bytes, the down records
+    # (64 x 2048 rows of K = 768) from 384 + 24 -> 416 to 288 + 24 -> 320 bytes
+    n4 = L.mk_packed_bytes(make_desc(synth.CONFIGS[3].model))
+    n3 = L.mk_packed_bytes(d)
+    per_layer = 2 * 64 * 768 * (1088 - 832) + 64 * 2048 * (416 - 320)
+    assert n4 - n3 == 47 * per_layer
+
+
 def test_null_context_calls_fail_cleanly(lib):
     assert lib.mk_kv_alloc(None, 4) == L.MK_ERR_INVALID_ARG
     ids = (C.c_int32 * 1)(0)

@@ -28,6 +28,17 @@ def test_step_bytes_of_the_flint_int4_step_by_hand():
     assert kv_pos == 100352
 
 
+def test_step_bytes_of_the_int3_expert_step_by_hand():
+    # int3 experts: a row of K values is 3K/8 bytes of codes + K/64 bf16
+    # scales = K * 13/32 bytes; every other linear layer as in the int4 model
+    m4, m3 = synth.CONFIGS[3].model, synth.FLINT_INT4_E3
+    row4 = lambda rows, K: rows * K * 17 // 32  # noqa: E731
+    row3 = lambda rows, K: rows * K * 13 // 32  # noqa: E731
+    per_layer = 6 * 3 * (row4(768, 2048) - row3(768, 2048))
+    for ctx in (1, 2049):
+        assert bench.step_bytes(m4, [ctx], 6) - bench.step_bytes(m3, [ctx], 6) == 47 * per_layer
+
+
 def test_reported_traffic_follows_the_kernel_source(monkeypatch):
     wl = "flint-int4-ctx2048"
     with open(os.path.join(ROOT, "profiles", f"step_kernel_{wl}.md")) as fh:

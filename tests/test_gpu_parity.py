@@ -12,11 +12,13 @@ pytestmark = pytest.mark.gpu
 TINY = synth.CONFIGS[1].model
 
 
-@pytest.mark.parametrize("wdtype", ["f32", "bf16", "int4"])
+@pytest.mark.parametrize("wdtype", ["f32", "bf16", "int4", "int4e3"])
 def test_tiny_config_prefill_and_decode(gpu_lib, wdtype):
     """Config 1 (64 cached prompt tokens, 16 decode steps), and the same tiny
-    model with bf16 and int4 linear layers."""
-    m = TINY.with_(wdtype=wdtype)
+    model with bf16 and int4 linear layers, and with int3 experts in the int4
+    model (int4e3).  The 64-token prompt runs through the chunked prefill's
+    GEMMs, the decode steps through the decode kernel."""
+    m = TINY.with_(wdtype="int4", expert_dtype="int3") if wdtype == "int4e3" else TINY.with_(wdtype=wdtype)
     rep = PR.run_single(m, prompt_len=64, n_decode=16)
     print(rep)
     assert not rep.failures, rep

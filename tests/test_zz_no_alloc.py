@@ -20,31 +20,13 @@ import synth
 from synth import prompts as SP
 from synth import weights as SW
 from moe_decode_megakernel_persistent_gb300 import _lib as L
-from moe_decode_megakernel_persistent_gb300.engine import Engine, _lin, _ptr
+from moe_decode_megakernel_persistent_gb300.engine import Engine, _ptr
+from tests._models import weights_struct as _weights_struct
 
 pytestmark = pytest.mark.gpu
 
 PROMPT = 140          # crosses the 128-position page boundary
 DECODE = 2            # two calls in a row after the prompt
-
-
-def _weights_struct(m, w):
-    layers = (L.mk_layer_weights * m.n_layers)()
-    for l in range(m.n_layers):
-        lw = layers[l]
-        lw.attn_norm = _ptr(w[("attn_norm", l)])
-        lw.ffn_norm = _ptr(w[("ffn_norm", l)])
-        for name in ("wq", "wk", "wv", "wo"):
-            setattr(lw, name, _lin(w[(name, l)]))
-        if l < m.n_dense:
-            for name in ("gate", "up", "down"):
-                setattr(lw, name, _lin(w[(name, l)]))
-        else:
-            lw.router = _ptr(w[("router", l)])
-            for name in ("exp_gate", "exp_up", "exp_down"):
-                setattr(lw, name, _lin(w[(name, l)]))
-    return L.mk_weights(embed=_ptr(w[("embed",)]), final_norm=_ptr(w[("final_norm",)]),
-                        lm_head=_lin(w[("lm_head",)]), layers=layers), layers
 
 
 @pytest.mark.parametrize("wdtype", ["f32", "int4"])
