@@ -290,7 +290,8 @@ MK_API int mk_sync(mk_ctx* ctx, void* stream);
                               layer l and phase p (0 qkv, 1 attention, 2 o_proj,
                               3 routing and gate/up, 4 down) [1 + 16*l + 3*p + k]
                               with k = 0 staging done, 1 phase work done, 2 grid
-                              barrier released; then [1 + 16*n_layers] lm_head done.
+                              barrier released; [1 + 16*l + 15] the routing of MoE
+                              layer l ready; then [1 + 16*n_layers] lm_head done.
                               After the grid's records, each block's ring log of
                               3072 stamps at [grid * R + b * 3072]: for its k-th
                               weight / KV tile (k < 1024) [3k] issued, [3k + 1]

@@ -143,6 +143,43 @@ __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(k
 // up when another block has recorded an error, or after spin_limit_ns, and
 // then records MK_ERR_BARRIER_TIMEOUT; the caller skips to the exit path.
 // `ok` is a shared-memory word used to broadcast the outcome.
+// Every bounded wait polls its own condition and, while it waits, the global
+// error word (another block gave up).  Reading the error word is an L2 round
+// trip during which the condition goes unseen, so a wait reads it only after
+// kErrPollNs of waiting and then once per kErrPollNs: a wait that ends within
+// that time never reads it.
+constexpr uint64_t kErrPollNs = 8000;
+struct WaitClock {
+  uint64_t t0, next;
+  __device__ __forceinline__ void start() {
+    t0 = globaltimer();
+    next = t0 + kErrPollNs;
+  }
+  // 0 keep waiting, 1 an error is recorded, 2 this wait ran past limit_ns
+  __device__ __forceinline__ int check(const int32_t* err, uint64_t limit_ns) {
+    const uint64_t now = globaltimer();
+    if (now < next) return 0;
+    next = now + kErrPollNs;
+    if (*(const volatile int32_t*)err != 0) return 1;
+    return now - t0 > limit_ns ? 2 : 0;
+  }
+};
+
+// ------------------------------------------------------------------ flagged words
+// A value exchanged between blocks without a grid barrier travels with its
+// tag in one 64-bit word (value bits low, tag high), written by one 64-bit
+// store, which is single-copy atomic: a reader that sees the tag it expects
+// sees the value that came with it.  Tags are unique per launch and layer, so
+// a word left from an earlier layer or launch never matches.
+__device__ __forceinline__ void flag_put(uint64_t* p, float v, uint32_t tag) {
+  const uint64_t w = ((uint64_t)tag << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+// The four values at p (32-byte aligned) once all four carry `tag`.  The wait
+// is bounded like the others: on an error or a timeout it records the error
+// and returns zeros (the step is then reported failed).
+__device__ __forceinline__ float4 flag_get4(const uint64_t* p, uint32_t tag, const StepArgs& a);
+
 static __device__ __noinline__ bool grid_barrier(const StepArgs& a, uint32_t& k, volatile int* ok_word) {
   csync();
   if (threadIdx.x == 0) {
@@ -153,26 +190,46 @@ static __device__ __noinline__ bool grid_barrier(const StepArgs& a, uint32_t& k,
     if (!skip) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(1u) : "memory");
     const uint32_t target = k * gridDim.x;
     int ok = 1;
-    uint64_t t0 = 0;
-    for (uint32_t spins = 0;; ++spins) {
+    WaitClock wc;
+    wc.start();
+    for (;;) {
       uint32_t v;
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
       if (v >= target) break;
-      if ((spins & 31u) == 0) {
-        if (*(volatile int32_t*)a.sc.err != 0) { ok = 0; break; }
-        uint64_t now = globaltimer();
-        if (spins == 0) t0 = now;
-        else if (now - t0 > a.spin_limit_ns) {
-          set_error(a.sc.err, MK_ERR_BARRIER_TIMEOUT, SITE_BARRIER, (int)k);
-          ok = 0;
-          break;
-        }
+      const int r = wc.check(a.sc.err, a.spin_limit_ns);
+      if (r) {
+        if (r == 2) set_error(a.sc.err, MK_ERR_BARRIER_TIMEOUT, SITE_BARRIER, (int)k);
+        ok = 0;
+        break;
       }
     }
     *ok_word = ok;
   }
   csync();
   return *ok_word != 0;
+}
+
+__device__ __forceinline__ float4 flag_get4(const uint64_t* p, uint32_t tag, const StepArgs& a) {
+  uint64_t w0, w1, w2, w3;
+  WaitClock wc;
+  bool waited = false;
+  for (;;) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(w2), "=l"(w3) : "l"(p + 2) : "memory");
+    if ((uint32_t)(w0 >> 32) == tag && (uint32_t)(w1 >> 32) == tag && (uint32_t)(w2 >> 32) == tag &&
+        (uint32_t)(w3 >> 32) == tag)
+      break;
+    if (!waited) {
+      wc.start();
+      waited = true;
+    }
+    if (const int r = wc.check(a.sc.err, a.spin_limit_ns)) {
+      if (r == 2) set_error(a.sc.err, MK_ERR_BARRIER_TIMEOUT, SITE_FLAG, (int)(tag & 0xFFu));
+      return make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  return make_float4(__uint_as_float((uint32_t)w0), __uint_as_float((uint32_t)w1), __uint_as_float((uint32_t)w2),
+                     __uint_as_float((uint32_t)w3));
 }
 
 // ------------------------------------------------------------------ weight ring
@@ -207,12 +264,15 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
 // kernel's code per layer is kept small: it is fetched again every layer).
 static __device__ __noinline__ bool mbar_wait_loop(uint64_t* b, uint32_t parity, const volatile int* abort, int32_t* err,
                                             uint64_t limit_ns, int site_detail) {
-  uint64_t t0 = globaltimer();
+  WaitClock wc;
+  wc.start();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try(b, parity)) return true;
-    if ((i & 15u) == 0) {
-      if (*abort || *(volatile int32_t*)err != 0) return false;
-      if (globaltimer() - t0 > limit_ns) {
+    if ((i & 3u) == 0) {
+      if (*abort) return false;
+      const int r = wc.check(err, limit_ns);
+      if (r == 1) return false;
+      if (r == 2) {
         set_error(err, MK_ERR_BARRIER_TIMEOUT, SITE_RING, site_detail);
         return false;
       }

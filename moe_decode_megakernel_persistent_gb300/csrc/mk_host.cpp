@@ -149,6 +149,7 @@ size_t carve_scratch(const mk_model_desc& d, int grid, int max_units, char* base
   s.amax_i = (int32_t*)take(sizeof(int32_t) * (size_t)grid * kMaxBatch);
   s.merge_cnt = (int32_t*)take(sizeof(int32_t) * kMaxBatch * d.n_kv_heads);
   s.sync = (uint32_t*)take(sizeof(uint32_t) * 128);
+  s.xll = (uint64_t*)take(sizeof(uint64_t) * 2 * kMaxBatch * H);
   s.err = (int32_t*)take(sizeof(int32_t) * 4);
   if (sc) *sc = s;
   return off;

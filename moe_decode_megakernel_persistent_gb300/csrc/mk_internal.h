@@ -80,7 +80,9 @@ struct Scratch {
   int32_t* amax_i;   // [grid][kMaxBatch] per-block best token
   int32_t* merge_cnt;   // [kMaxBatch][n_kv] attention merge arrivals
   uint32_t* sync;       // counters, one per 128-byte line: [0] barrier, [32] exit,
-                        // [96] argmax reduce
+                        // [64] launch epoch (advanced by every launch), [96] argmax reduce
+  uint64_t* xll;        // [2][kMaxBatch][H] the residual as flagged words (value, tag),
+                        // double-buffered by layer parity
   int32_t* err;         // [0] status, [1] site, [2] detail
 };
 
@@ -169,7 +171,9 @@ void prefill_free(PrefillWork* w);
 int prefill_setup_attributes(const mk_model_desc& m);
 
 // Error sites recorded in err[1].
-enum ErrSite { SITE_BARRIER = 1, SITE_PAGE = 2, SITE_UNIT = 3, SITE_TOKEN = 4, SITE_RING = 5, SITE_SMEM = 6 };
+enum ErrSite {
+  SITE_BARRIER = 1, SITE_PAGE = 2, SITE_UNIT = 3, SITE_TOKEN = 4, SITE_RING = 5, SITE_SMEM = 6, SITE_FLAG = 7
+};
 
 // Kernel variants compiled into the library.
 enum ShapeId { SHAPE_FLINT = 0, SHAPE_TINY = 1, NSHAPE };

@@ -46,6 +46,9 @@ struct Ctx {
   int G, bid, n;
   int r0, nr;      // hidden rows owned by this block
   bool tc;         // tensor-core GEMV (plain fp32 staging) for this launch
+  bool flagged;    // one-row launch of a whole step: the residual reaches the next
+                   // layer's QKV as flagged words, with no grid barrier
+  uint32_t tag0;   // this launch's epoch * 256: the tag of layer l's words is tag0 + l + 1
   float *tr_x, *tr_attn, *tr_rl, *tr_tk, *tr_fin;
   uint64_t* tm;    // this block's timing stamps (thread 0 writes them) or null
   uint64_t* ring_log;  // this block's ring log: [3k] item k issued, [3k + 1] landed (thread 0 saw it),
@@ -119,6 +122,7 @@ struct Kv {
 
 // Timing record layout (uint64 ns): [0] start; per layer l and phase p:
 // [1 + 16 l + 3 p + k], k = 0 staging done, 1 work done, 2 barrier released;
+// [1 + 16 l + 15] the layer's routing tables ready (MoE layers);
 // [1 + 16 L] lm_head done.
 #define MK_STAMP(c, l, p, k) \
   if ((c).tm && threadIdx.x == 0) (c).tm[1 + 16 * (l) + 3 * (p) + (k)] = globaltimer()
@@ -664,10 +668,15 @@ struct Model {
       const float* x = a.sc.x;
       const int* tok = F.tok;
       const bool first = l == 0;
+      // the previous layer's residual: flagged words (one-row step), else
+      // plain rows behind the grid barrier
+      const uint64_t* xw = c.flagged && !first ? a.sc.xll + (size_t)((l - 1) & 1) * kMaxBatch * H : nullptr;
+      const uint32_t tag = c.tag0 + l;
       stage_block<MODE, WDT, H, true>(
           c.act, n,
           [&](int r, int f4) -> float4 {
             return first ? ld_aux4<AUX>(embed, (size_t)tok[r] * (H / 4) + f4)
+                   : xw  ? flag_get4(xw + (size_t)r * H + 4 * f4, tag, a)
                          : __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4);
           },
           a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
@@ -997,13 +1006,14 @@ struct Model {
       const int nch = (a.pos[b] + 1 + a.chunk - 1) / a.chunk;
       if (tid == 0) {
         const int target = (l + 1 - a.slice_lo / 4) * nch;
-        const uint64_t ts = globaltimer();
+        WaitClock wc;
+        wc.start();
         F.flag = 1;
-        for (uint32_t i = 0;; ++i) {
+        for (;;) {
           int v;
           asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(a.sc.merge_cnt + b * NKV + g) : "memory");
           if (v >= target) break;
-          if ((i & 31u) == 0 && (*(volatile int32_t*)a.sc.err != 0 || globaltimer() - ts > a.spin_limit_ns)) {
+          if (wc.check(a.sc.err, a.spin_limit_ns)) {
             set_error(a.sc.err, MK_ERR_BARRIER_TIMEOUT, SITE_UNIT, b * NKV + g);
             F.flag = 0;
             break;
@@ -1191,9 +1201,10 @@ struct Model {
     const StepArgs& a = F.args;
     const int lane = threadIdx.x & 31;
     float* lg = &F.dots[0][0];
+    // every lane's loads in one round trip: experts lane and lane + 32
+    constexpr int EPL = (E + 31) / 32;
+    float v[EPL];
     {
-      // every lane's loads in one round trip: experts lane and lane + 32
-      constexpr int EPL = (E + 31) / 32;
       long long q[EPL][kRlogitGroups];
 #pragma unroll
       for (int j = 0; j < EPL; ++j)
@@ -1202,26 +1213,34 @@ struct Model {
           q[j][gr] = lane + 32 * j < E ? __ldcg(a.sc.rlogit + gr * kMaxBatch * E + lane + 32 * j) : 0ll;
 #pragma unroll
       for (int j = 0; j < EPL; ++j) {
-        unsigned long long v = 0ull;  // wrapping two's-complement sum
+        unsigned long long s = 0ull;  // wrapping two's-complement sum
 #pragma unroll
-        for (int gr = 0; gr < kRlogitGroups; ++gr) v += (unsigned long long)q[j][gr];
-        if (lane + 32 * j < E) lg[lane + 32 * j] = from_fixed((long long)v);
+        for (int gr = 0; gr < kRlogitGroups; ++gr) s += (unsigned long long)q[j][gr];
+        v[j] = from_fixed((long long)s);
+        if (lane + 32 * j < E) lg[lane + 32 * j] = v[j];
       }
     }
-    __syncwarp();
-    for (int e = lane; e < E; e += 32) {
-      const float v = lg[e];
-      int rank = 0;
-#pragma unroll 8
-      for (int e2 = 0; e2 < E; ++e2) {
-        const float w = lg[e2];
-        rank += (w > v) || (w == v && e2 < e);
+    // rank of each expert = experts with a larger logit, ties to the lower id,
+    // counted over register values passed round the warp
+    int rank[EPL];
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) rank[j] = 0;
+#pragma unroll
+    for (int src = 0; src < 32; ++src)
+#pragma unroll
+      for (int j2 = 0; j2 < EPL; ++j2) {
+        const float w = __shfl_sync(0xffffffffu, v[j2], src);
+        const int e2 = src + 32 * j2;
+        if (e2 < E)
+#pragma unroll
+          for (int j = 0; j < EPL; ++j) rank[j] += (w > v[j]) || (w == v[j] && e2 < lane + 32 * j);
       }
-      if (rank < TOPK) {
-        F.topk_id[0][rank] = e;
-        F.topk_w[0][rank] = v;  // partial logit for now
+#pragma unroll
+    for (int j = 0; j < EPL; ++j)
+      if (lane + 32 * j < E && rank[j] < TOPK) {
+        F.topk_id[0][rank[j]] = lane + 32 * j;
+        F.topk_w[0][rank[j]] = v[j];  // partial logit for now
       }
-    }
     __syncwarp();
     // one entry per slot, the distinct experts in increasing id order
     if (lane < TOPK) {
@@ -1242,6 +1261,7 @@ struct Model {
       __threadfence_block();
       F.route_gen = l + 1;
     }
+    MK_STAMP(F.ctx, l, 5, 0);
   }
 
   __device__ static __noinline__ void route(int l) {
@@ -1326,6 +1346,7 @@ struct Model {
         __threadfence_block();
         F.route_gen = l + 1;
       }
+      MK_STAMP(c, l, 5, 0);
     }
   }
   template <int MODE>
@@ -1511,6 +1532,7 @@ struct Model {
         s = F.dots[b][rr];
       const float xv = F.hs[b][rr] + s;   // this block's rows of h, kept since o_proj
       a.sc.x[b * H + c.r0 + rr] = xv;
+      if (c.flagged) flag_put(a.sc.xll + ((size_t)(l & 1) * kMaxBatch + b) * H + c.r0 + rr, xv, c.tag0 + l + 1);
       if (c.tr_x) c.tr_x[((size_t)l * n + b) * H + c.r0 + rr] = xv;
     }
   }
@@ -1715,15 +1737,15 @@ struct Model {
       if (l >= a.n_dense) {
         // P4/P5 need the layer's routing
         {
-          const uint64_t t_start = globaltimer();
+          WaitClock wc;
+          wc.start();
           uint32_t i = 0;
           while (F.route_gen < l + 1) {
             if ((++i & 15u) == 0) {
-              if (F.abort || *(volatile int32_t*)a.sc.err != 0) return;
-              if (globaltimer() - t_start > a.spin_limit_ns) {
-                set_error(a.sc.err, MK_ERR_BARRIER_TIMEOUT, SITE_RING, l);
-                return;
-              }
+              if (F.abort) return;
+              const int r = wc.check(a.sc.err, a.spin_limit_ns);
+              if (r == 2) set_error(a.sc.err, MK_ERR_BARRIER_TIMEOUT, SITE_RING, l);
+              if (r) return;
             }
           }
           __threadfence_block();
@@ -1828,6 +1850,8 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
     asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dsz));
     const int avail = (int)dsz - kActOffset;
     c.tc = M::TC && n >= 2;
+    c.flagged = n == 1 && a.slice_lo == 0 && a.slice_hi == 4 * a.n_layers;
+    c.tag0 = *(volatile uint32_t*)(a.sc.sync + 64) * 256u;
     int act = M::act_base_bytes(n, c.tc);
     const int want = n * S::TOPK * M::moe_entry_bytes(c);
     if (want > act) act = max(act, min(want, avail - 3 * M::STAGE));
@@ -1950,7 +1974,9 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
         if (l >= a.n_dense) M::template down<true>(l);
         else M::template down<false>(l);
         MK_STAMP(c, l, 4, 1);
-        if (more && !(ok = grid_barrier(a, nbar, &F.ok_word))) break;
+        // the next layer's QKV waits for the flagged residual words instead
+        const bool by_flags = c.flagged && s + 1 < a.slice_hi;
+        if (more && !by_flags && !(ok = grid_barrier(a, nbar, &F.ok_word))) break;
         MK_STAMP(c, l, 4, 2);
       }
     }
@@ -1983,6 +2009,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const __grid_con
       // every block has left its work: reset the launch-scoped counters
       a.sc.sync[0] = 0;
       a.sc.sync[96] = 0;
+      a.sc.sync[64] += 1;  // the next launch's epoch
       for (int i = 0; i < kMaxBatch * S::NKV; ++i) a.sc.merge_cnt[i] = 0;
       __threadfence();
       a.sc.sync[32] = 0;

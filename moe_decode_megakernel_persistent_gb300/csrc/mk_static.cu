@@ -216,9 +216,11 @@ extern "C" MK_API int mk_decode_step_static(
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: counters, merge counts and
-  // the error word must start at zero
+  // the error word must start at zero; the launch epoch (sync[64], the tag of
+  // the flagged residual words) must not, or a stale word would match
   e = cudaMemsetAsync(a.sc.merge_cnt, 0, sizeof(int32_t) * kMaxBatch * d->n_kv_heads, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(a.sc.sync, 0, sizeof(uint32_t) * 128, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(a.sc.sync, 0, sizeof(uint32_t) * 64, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(a.sc.sync + 96, 0, sizeof(uint32_t) * 32, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(a.sc.err, 0, sizeof(int32_t) * 4, st);
   if (e != cudaSuccess) return host_fail(MK_ERR_CUDA, cudaGetErrorString(e));
   void* args[] = {&a};
