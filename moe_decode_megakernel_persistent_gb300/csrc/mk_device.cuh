@@ -683,6 +683,55 @@ __device__ __forceinline__ void stage_block(uint8_t* dst, int rows, LD ld, float
   else stage_rows<WDT, K, NORM, RGM, false>(dst, rows, ld, eps, wt, red, rscale);
 }
 
+// Plain fp32 rows for the tensor-core path (rows of `ld` floats at src),
+// staged with one round of 16-byte asynchronous copies: the plain layout is
+// the rows' own values plus padding, so the bytes land as they are, in one L2
+// round trip for all rows.  With NORM they are then RMS-normalised in place:
+// one warp per row sums the squares in a fixed order (every block gets the
+// same scale), then every value is multiplied by scale x norm weight.
+// red: shared scratch of at least `rows` floats; rscale as in stage_rows.
+template <int AUX, int K, bool NORM>
+__device__ __forceinline__ void stage_plain_async(uint8_t* dst, int rows, const float* src, int ld, float eps,
+                                                  const void* w, float* red, float* rscale) {
+  constexpr int C4 = K / 4;  // 16-byte pieces of a row
+  constexpr int PS = plain_stride(K);
+  static_assert(K % 4 == 0, "whole 16-byte pieces");
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  for (int idx = tid; idx < rows * C4; idx += kThreads) {
+    const int r = idx / C4, c = idx % C4;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + r * PS + 16 * c)),
+                 "l"(src + (size_t)r * ld + 4 * c)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  csync();
+  if constexpr (NORM) {
+    for (int r = wid; r < rows; r += kWarps) {
+      float s = 0.f;
+      for (int c = lane; c < C4; c += 32) {
+        const float4 v = *reinterpret_cast<const float4*>(dst + r * PS + 16 * c);
+        s += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+      }
+      s = warp_sum(s);
+      if (lane == 0) {
+        const float rs = rsqrtf(s / K + eps);
+        red[r] = rs;
+        if (rscale) rscale[r] = rs;
+      }
+    }
+    csync();
+    for (int idx = tid; idx < rows * C4; idx += kThreads) {
+      const int r = idx / C4, c = idx % C4;
+      float4* p = reinterpret_cast<float4*>(dst + r * PS + 16 * c);
+      const float4 v = *p, wv = ld_aux4<AUX>(w, c);
+      const float rs = red[r];
+      *p = make_float4(v.x * (rs * wv.x), v.y * (rs * wv.y), v.z * (rs * wv.z), v.w * (rs * wv.w));
+    }
+    csync();
+  }
+}
+
 __device__ __forceinline__ void split_range(int n, int parts, int idx, int& lo, int& hi) {
   lo = (int)(((long long)n * idx) / parts);
   hi = (int)(((long long)n * (idx + 1)) / parts);

@@ -672,14 +672,17 @@ struct Model {
       // plain rows behind the grid barrier
       const uint64_t* xw = c.flagged && !first ? a.sc.xll + (size_t)((l - 1) & 1) * kMaxBatch * H : nullptr;
       const uint32_t tag = c.tag0 + l;
-      stage_block<MODE, WDT, H, true>(
-          c.act, n,
-          [&](int r, int f4) -> float4 {
-            return first ? ld_aux4<AUX>(embed, (size_t)tok[r] * (H / 4) + f4)
-                   : xw  ? flag_get4(xw + (size_t)r * H + 4 * f4, tag, a)
-                         : __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4);
-          },
-          a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
+      if (MODE == 2 && !first)  // plain rows of x: one round of asynchronous copies
+        stage_plain_async<AUX, H, true>(c.act, n, x, H, a.eps, nw, F.red, nullptr);
+      else
+        stage_block<MODE, WDT, H, true>(
+            c.act, n,
+            [&](int r, int f4) -> float4 {
+              return first ? ld_aux4<AUX>(embed, (size_t)tok[r] * (H / 4) + f4)
+                     : xw  ? flag_get4(xw + (size_t)r * H + 4 * f4, tag, a)
+                           : __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4);
+            },
+            a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
     }
     if (l == 0)  // residual rows this block reads back in P3
       for (int i = tid; i < n * c.nr; i += kThreads) {
@@ -1140,9 +1143,12 @@ struct Model {
     }
     {
       const float* at = a.sc.attn;
-      stage_block<MODE, WDT, QD, false>(
-          c.act, c.n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(at + r * QD) + f4); },
-          0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
+      if constexpr (MODE == 2)
+        stage_plain_async<AUX, QD, false>(c.act, c.n, at, QD, 0.f, nullptr, F.red, nullptr);
+      else
+        stage_block<MODE, WDT, QD, false>(
+            c.act, c.n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(at + r * QD) + f4); },
+            0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
     }
     csync();
     MK_STAMP(c, l, 2, 0);
@@ -1357,9 +1363,12 @@ struct Model {
     {
       const void* nw = F.lw.ffn_norm;
       const float* hp = a.sc.h;
-      stage_block<MODE, WDT, H, true>(
-          c.act, c.n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(hp + r * H) + f4); },
-          a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, F.rnorm);
+      if constexpr (MODE == 2)
+        stage_plain_async<AUX, H, true>(c.act, c.n, hp, H, a.eps, nw, F.red, F.rnorm);
+      else
+        stage_block<MODE, WDT, H, true>(
+            c.act, c.n, [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(hp + r * H) + f4); },
+            a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, F.rnorm);
     }
     csync();
     MK_STAMP(c, l, 3, 0);
@@ -1472,10 +1481,13 @@ struct Model {
     } else {
       const int cnt = min(ub, c.n) - u;
       const float* dact = a.sc.dact;
-      stage_block<MODE, WDT, FD, false>(
-          c.act, cnt,
-          [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(dact + (u + r) * FD) + f4); },
-          0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
+      if constexpr (MODE == 2)
+        stage_plain_async<AUX, FD, false>(c.act, cnt, dact + (size_t)u * FD, FD, 0.f, nullptr, F.red, nullptr);
+      else
+        stage_block<MODE, WDT, FD, false>(
+            c.act, cnt,
+            [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(dact + (u + r) * FD) + f4); },
+            0.f, [&](int) { return make_float4(1.f, 1.f, 1.f, 1.f); }, F.red, nullptr);
     }
     csync();
     MK_STAMP(c, l, 4, 0);
@@ -1570,10 +1582,14 @@ struct Model {
     {
       const void* nw = a.final_norm;
       const float* x = a.sc.x + a.out_first * H;
-      stage_block<MODE, WDT, H, true>(
-          c.act + a.out_first * (MODE == 2 ? plain_stride(H) : GH::ACT_BYTES), c.n - a.out_first,
-          [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4); },
-          a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
+      if constexpr (MODE == 2)
+        stage_plain_async<AUX, H, true>(c.act + a.out_first * plain_stride(H), c.n - a.out_first, x, H, a.eps, nw,
+                                        F.red, nullptr);
+      else
+        stage_block<MODE, WDT, H, true>(
+            c.act + a.out_first * (MODE == 2 ? plain_stride(H) : GH::ACT_BYTES), c.n - a.out_first,
+            [&](int r, int f4) { return __ldcg(reinterpret_cast<const float4*>(x + r * H) + f4); },
+            a.eps, [&](int f4) { return ld_aux4<AUX>(nw, f4); }, F.red, nullptr);
     }
     if (threadIdx.x < kMaxBatch) F.best_key[threadIdx.x] = 0ull;
     csync();
