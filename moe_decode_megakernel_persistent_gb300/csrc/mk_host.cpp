@@ -155,9 +155,9 @@ size_t carve_scratch(const mk_model_desc& d, int grid, int max_units, char* base
   return off;
 }
 
-// Split of the attention work: (row, kv head, chunk) units that roughly fill
-// the grid once, with chunks a whole number of ring tiles (tile_tokens
-// cached positions each) and at most kMaxChunks chunks per row.
+// Split of the attention work into (row, kv head, chunk of positions) units,
+// with chunks a whole number of ring tiles (tile_tokens cached positions
+// each) and at most kMaxChunks chunks per row.
 void host_attention_split_impl(int n_kv_heads, int grid, int tile_tokens, const int32_t* pos, int n, int* chunk,
                                int* units) {
   long long total = 0, longest = 0;
@@ -165,19 +165,38 @@ void host_attention_split_impl(int n_kv_heads, int grid, int tile_tokens, const 
     total += pos[i] + 1;
     longest = std::max<long long>(longest, pos[i] + 1);
   }
+  (void)total;
   const long long tt = std::max(1, tile_tokens);
-  long long ch = (n_kv_heads * total + grid - 1) / grid;
-  ch = std::max(ch, (longest + kMaxChunks - 1) / kMaxChunks);  // at most kMaxChunks chunks per row
-  ch = std::max<long long>(8, (ch + tt - 1) / tt * tt);
-  long long u = 0;
-  for (;;) {  // a block takes at most kMaxOwnUnits units
-    u = 0;
+  // chunks are whole ring tiles, at most kMaxChunks per row
+  const long long lo = std::max(tt, ((longest + kMaxChunks - 1) / kMaxChunks + tt - 1) / tt * tt);
+  // Blocks take units round-robin, so the attention phase lasts about
+  // ceil(units / grid) x (chunk + a unit's fixed cost, about 1.5 ring tiles:
+  // the query staging, the partial written, the merge share).  Take the chunk
+  // that minimises it; on a tie the larger chunk (fewer units and merges).
+  // A block takes at most kMaxOwnUnits units, and the partials' buffer holds
+  // grid + n_kv_heads * kMaxBatch units.
+  const long long ovh = tt + tt / 2;
+  const long long cap = std::min<long long>((long long)kMaxOwnUnits * grid, (long long)grid + n_kv_heads * kMaxBatch);
+  long long best_ch = -1, best_u = 0, best_cost = 0;
+  for (long long ch = lo;; ch += tt) {
+    long long u = 0;
     for (int i = 0; i < n; ++i) u += n_kv_heads * ((pos[i] + 1 + ch - 1) / ch);
-    if (u <= (long long)kMaxOwnUnits * grid || ch >= longest) break;
-    ch += tt;
+    if (u <= cap) {
+      const long long cost = (u + grid - 1) / grid * (ch + ovh);
+      if (best_ch < 0 || cost <= best_cost) {
+        best_ch = ch;
+        best_u = u;
+        best_cost = cost;
+      }
+    }
+    if (ch >= longest) break;
   }
-  *chunk = (int)ch;
-  *units = (int)u;
+  if (best_ch < 0) {  // not reachable: one chunk per row gives n * n_kv_heads units
+    best_ch = std::max(lo, (longest + tt - 1) / tt * tt);
+    best_u = (long long)n * n_kv_heads;
+  }
+  *chunk = (int)best_ch;
+  *units = (int)best_u;
 }
 
 void attention_split(const mk_ctx* c, const int32_t* pos, int n, int* chunk, int* units) {
