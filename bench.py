@@ -298,10 +298,14 @@ def run_ours(args, rank, world):
         split_ms = e0.elapsed_time(e1) / Ks
         groups = 4 * m.n_layers
         split = {"ms_per_step": round(split_ms, 4), "persistent_ms_per_step": round(ms_per_step, 4),
-                 "launches_per_step": groups + 1, "grid_barriers_per_step_persistent": 5 * m.n_layers,
+                 "launches_per_step": groups + 1,
+                 # one-row persistent step: four grid barriers per layer, the residual
+                 # passed to the next layer by flagged words, one barrier before lm_head
+                 "grid_barriers_per_step_persistent": 4 * m.n_layers + 1,
                  "boundaries_replacing_barriers": groups,
                  "us_per_boundary_minus_barrier": round((split_ms - ms_per_step) * 1e3 / groups, 3),
-                 "note": "context grows by 2 + K steps before the split run"}
+                 "note": "context grows by 2 + K steps before the split run; a boundary replaces a "
+                         "grid barrier or, after a layer's down phase, the flagged-word exchange"}
         K_extra = Ks + 2
     else:
         K_extra = 0
