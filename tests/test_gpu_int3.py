@@ -7,9 +7,9 @@ in int4, against the oracle on the same codes.
 - The tiny model in a 16-row launch, each row against the oracle (the expert
   GEMV with several activations per tile).
 - The Flint shape, layers 0-3: a 2048-token context with teacher-forced
-  decode in the launch configuration the bench times, and a free-running
+  decode in the launch configuration the bench times, a free-running
   64-token prompt through the chunked prefill's GEMMs (int3 widened to fp16)
-  followed by decode.
+  followed by decode, and four sequences in one launch.
 
 Integer rules as everywhere: top-k ids where the oracle's margin exceeds
 1e-3, tokens where its top-2 margin exceeds 0.05, exact.
@@ -184,3 +184,37 @@ def test_flint_int3_experts_chunked_prefill_then_decode(gpu_lib, flint4_e3):
     m, w = flint4_e3
     rep = PR.run_single(m, prompt_len=64, n_decode=8, w=w, n_pages=8)
     _check(rep, min_topk=20)
+
+
+def test_flint_int3_experts_four_rows_match_the_oracle(gpu_lib, flint4_e3):
+    """Four sequences of different lengths in one launch on the Flint shape:
+    the dense projections on the tensor-core path, the int3 expert rows with
+    several activations per tile; every row against the oracle."""
+    m, w = flint4_e3
+    lens = [17, 40, 90, 130]
+    eng = Engine(m, w, n_pages=16, max_ctx=256, max_seqs=4)
+    orc = Oracle(m, PR.host_fetch(m, w), cache_bytes=8 << 30)
+    toks = torch.empty(4, dtype=torch.int32, device="cuda")
+    kvs, nxt = [], []
+    for s, n in enumerate(lens):
+        p = SP.prompt_tokens(m.seed, m.vocab, n, seq=40 + s)
+        kv = orc.new_kv()
+        t, _ = orc.prefill(kv, p)
+        kvs.append(kv)
+        nxt.append(t)
+        eng.prefill(s, torch.from_numpy(p).cuda(), out=toks[s:s + 1])
+    toks.copy_(torch.tensor(nxt, dtype=torch.int32))
+    eng.enable_trace(4)
+    eng.decode_step([0, 1, 2, 3], toks, lens, toks)
+    eng.sync()
+    tr = eng.split_trace(4)
+    rep = PR.Report()
+    for s in range(4):
+        _, tro = orc.decode(kvs[s], nxt[s], lens[s])
+        PR.compare_trace(rep, m, tr, tro, slice(s, s + 1), slice(0, 1), PR.tol_for(m), f"seq {s}", seq=s)
+        PR.check_token(rep, int(toks[s].item()), int(tro["next_token"][-1]), float(tro["top2_margin"][-1]),
+                       f"seq {s}", seq=s)
+    print(rep)
+    assert not rep.failures, rep
+    assert rep.topk_checked >= 6, rep
+    eng.close()
