@@ -81,11 +81,17 @@ def step_bytes(m, ctxs, distinct_experts_per_layer) -> int:
     return int(total)
 
 
+# the decode kernel's own sources: its translation unit and the library headers
+# that hold its code and data structures (host-only code, the prefill and the
+# packer do not change the kernel the DRAM traffic figure was measured on)
+KERNEL_SOURCES = ("csrc/mk_kernel.cu", "csrc/mk_device.cuh", "csrc/mk_internal.h")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "moe_decode_megakernel_persistent_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
+    pkg = os.path.join(ROOT, "moe_decode_megakernel_persistent_gb300")
+    for f in KERNEL_SOURCES:
+        with open(os.path.normpath(os.path.join(pkg, f)), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 

@@ -310,6 +310,18 @@ MK_API int mk_set_debug(mk_ctx* ctx, uint32_t flags, uint32_t arg, void* trace_d
  *   final  [rows][vocab]                lm_head logits (rows with an output) */
 MK_API size_t mk_trace_bytes(const mk_model_desc* d, int32_t rows);
 
+/* The attention split a decode launch uses for rows whose new positions are
+ * positions_host[0..n) (host int32, each >= 0; n in 1..16): every (row, kv
+ * head) is cut into chunks of *chunk_out cached positions (a whole number of
+ * tile_tokens, the kernel's cached positions per ring tile: mk_info
+ * tile_tokens), giving *units_out (row, kv head, chunk) units over `grid`
+ * blocks.  The chunk minimises ceil(units / grid) x (chunk + 1.5 tiles of fixed
+ * cost per unit), the larger chunk on a tie, with at most 64 chunks per row,
+ * 4 units per block and grid + 16 x n_kv_heads units.  Host only, no device
+ * work.  Errors: INVALID_ARG. */
+MK_API int mk_attention_plan(int32_t n_kv_heads, int32_t grid, int32_t tile_tokens, const int32_t* positions_host,
+                             int32_t n, int32_t* chunk_out, int32_t* units_out);
+
 MK_API int mk_get_info(mk_ctx* ctx, mk_info* info);
 
 /* Release every resource of the context (waits for its device work). */

@@ -86,6 +86,8 @@ SIGNATURES = {
                                C.c_uint32]),
     "mk_trace_bytes": (C.c_size_t, [C.POINTER(mk_model_desc), C.c_int32]),
     "mk_get_info": (C.c_int, [C.c_void_p, C.POINTER(mk_info)]),
+    "mk_attention_plan": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, C.POINTER(C.c_int32), C.c_int32,
+                                    C.POINTER(C.c_int32), C.POINTER(C.c_int32)]),
     "mk_destroy": (C.c_int, [C.c_void_p]),
     "mk_last_error": (C.c_char_p, []),
     "mk_packed_bytes": (C.c_size_t, [C.POINTER(mk_model_desc)]),
@@ -183,6 +185,14 @@ def mk_set_debug(ctx: int, flags: int, arg: int = 0, trace_dev: int = 0, trace_b
 
 def mk_trace_bytes(desc: mk_model_desc, rows: int) -> int:
     return load().mk_trace_bytes(C.byref(desc), rows)
+
+
+def mk_attention_plan(n_kv_heads: int, grid: int, tile_tokens: int, positions) -> tuple:
+    """(chunk, units) of the attention split for rows at these new positions."""
+    pos = (C.c_int32 * len(positions))(*positions)
+    ch, u = C.c_int32(), C.c_int32()
+    _check(load().mk_attention_plan(n_kv_heads, grid, tile_tokens, pos, len(positions), C.byref(ch), C.byref(u)))
+    return ch.value, u.value
 
 
 def mk_get_info(ctx: int) -> dict:

@@ -842,6 +842,21 @@ MK_API int mk_set_debug(mk_ctx* c, uint32_t flags, uint32_t arg, void* trace_dev
   return MK_OK;
 }
 
+MK_API int mk_attention_plan(int32_t n_kv_heads, int32_t grid, int32_t tile_tokens, const int32_t* positions_host,
+                             int32_t n, int32_t* chunk_out, int32_t* units_out) {
+  g_err.clear();
+  if (!positions_host || !chunk_out || !units_out) return fail(MK_ERR_INVALID_ARG, "NULL argument");
+  if (n_kv_heads < 1 || grid < 1 || tile_tokens < 1 || n < 1 || n > kMaxBatch)
+    return fail(MK_ERR_INVALID_ARG, "n_kv_heads, grid, tile_tokens >= 1 and n in 1..16");
+  for (int i = 0; i < n; ++i)
+    if (positions_host[i] < 0) return fail(MK_ERR_INVALID_ARG, "negative position");
+  int ch = 0, u = 0;
+  host_attention_split_impl(n_kv_heads, grid, tile_tokens, positions_host, n, &ch, &u);
+  *chunk_out = ch;
+  *units_out = u;
+  return MK_OK;
+}
+
 MK_API int mk_get_info(mk_ctx* c, mk_info* info) {
   g_err.clear();
   if (!c || !info) return fail(MK_ERR_INVALID_ARG, "NULL argument");
