@@ -49,9 +49,9 @@ def test_the_16_client_workload_takes_one_unit_per_block():
 
 def test_plan_invariants_and_optimality_on_random_batches():
     rng = random.Random(8)
-    for _ in range(300):
+    for _ in range(120):
         nkv = rng.choice([1, 2, 4, 8])
-        tile = rng.choice([8, 30, 60])
+        tile = rng.choice([16, 30, 60])
         grid = rng.choice([1, 7, 152])
         positions = [rng.randrange(0, rng.choice([40, 2000, 9000])) for _ in range(rng.randrange(1, 17))]
         chunk, units = L.mk_attention_plan(nkv, grid, tile, positions)
