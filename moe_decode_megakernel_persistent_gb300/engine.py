@@ -310,7 +310,7 @@ class Batcher:
         """timed: CUDA events around every decode launch; the result then has
         "decode_ms" (sum over launches) and "steps_ms" [(active rows, ms)]."""
         e = self.e
-        dev = torch.device("cuda")
+        dev = getattr(e, "out_device", None) or torch.device("cuda")  # where the step's tokens live
         events = []
         pending = sorted(requests, key=lambda r: (r.arrival, r.seq_id))
         active: list = []
@@ -323,7 +323,11 @@ class Batcher:
                 out = e.prefill(r.seq_id, r.prompt)
                 tok_dev[r.seq_id] = out
                 r.generated.append(out)  # first generated token (device)
-                active.append(r)
+                if len(r.generated) >= r.max_new:  # the prefill's token was all it asked for
+                    r.finish_step = step
+                    e.release(r.seq_id)
+                else:
+                    active.append(r)
             if active:
                 ids = [r.seq_id for r in active]
                 pos = [e.seq_length(i) for i in ids]
