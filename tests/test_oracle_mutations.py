@@ -102,3 +102,49 @@ def test_transposed_operand_is_caught(monkeypatch):
     monkeypatch.setattr(O.Oracle, "w", transposed)
     with pytest.raises((AssertionError, ValueError)):
         pins.test_decode_step_matches_scalar_brute_force()
+
+
+# ---- the int3 storage format: plausible misreadings of the packed words
+
+def _int3_decode(packed, scale_bits, order=lambda j: j, signed=True, little=True, group=64):
+    from oracle.numerics import bf16_bits_to_f64
+    packed = np.asarray(packed, dtype=np.uint8)
+    R, nb = packed.shape
+    K = nb // 3 * 8
+    b = packed.reshape(R, K // 8, 3).astype(np.int64)
+    word = (b[:, :, 0] + 256 * b[:, :, 1] + 65536 * b[:, :, 2]) if little else \
+           (b[:, :, 2] + 256 * b[:, :, 1] + 65536 * b[:, :, 0])
+    q = np.empty((R, K // 8, 8), dtype=np.int64)
+    for j in range(8):
+        q[:, :, j] = (word // (8 ** order(j))) % 8
+    q = q.reshape(R, K)
+    if signed:
+        q = np.where(q >= 4, q - 8, q)
+    s = np.repeat(bf16_bits_to_f64(scale_bits), 64, axis=1)[:, :K]
+    if group != 64:
+        s = np.repeat(bf16_bits_to_f64(scale_bits), group, axis=1)[:, :K]
+    return q.astype(np.float64) * s
+
+
+INT3_MUTANTS = [
+    ("reversed code order", lambda p, s: _int3_decode(p, s, order=lambda j: 7 - j)),
+    ("unsigned codes", lambda p, s: _int3_decode(p, s, signed=False)),
+    ("big-endian words", lambda p, s: _int3_decode(p, s, little=False)),
+    ("one scale per 128 values", lambda p, s: _int3_decode(p, s, group=128)),
+]
+
+
+@pytest.mark.parametrize("label,fn", INT3_MUTANTS, ids=[m[0] for m in INT3_MUTANTS])
+def test_int3_pins_catch_misread_words(monkeypatch, label, fn):
+    # the correct decoder passes both pins ...
+    pins.test_int3_dequant_of_hand_packed_words()
+    pins.test_int3_quantiser_error_bound_and_exact_grid()
+    # ... a misreading fails at least one
+    monkeypatch.setattr(pins, "dequant_int3", fn)
+    failed = 0
+    for pin in (pins.test_int3_dequant_of_hand_packed_words, pins.test_int3_quantiser_error_bound_and_exact_grid):
+        try:
+            pin()
+        except (AssertionError, ValueError):
+            failed += 1
+    assert failed >= 1, label
