@@ -358,10 +358,11 @@ MK_API int mk_destroy(mk_ctx* ctx);
  * later call whose model differs (weights, n_layers, rope_theta, head_dim)
  * first waits for the whole device to go idle (cudaDeviceSynchronize: an
  * earlier call on any stream may still read the tables), then rewrites the
- * tables the same way.  A call with the same model as the previous one only
- * enqueues on `stream`: three memsets that clear the counters and the error
- * word (the array keeps the last call's contents), the launch and the
- * optional status copy.
+ * tables the same way and clears the kernel scratch (synchronous memset, then
+ * another wait).  A call with the same model as the previous one only
+ * enqueues on `stream`: four memsets that clear the counters (all but the
+ * launch epoch) and the error word (the array keeps the last call's
+ * contents), the launch and the optional status copy.
  * Every call shares the one array: calls that overlap on the GPU, on any
  * stream, race, and so does a call that changes the model while another
  * thread's call is being enqueued.

@@ -54,9 +54,13 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 // With device `dev` current: the first call resolves the array's device
 // address.  When the RoPE parameters or the layer table differ from what the
 // array holds, the device is first drained (an earlier call, on any stream,
-// may still be reading them) and the tables are rewritten with synchronous
-// copies.  Calls with the same model reach neither step.
-int setup(int dev, const mk_model_desc& d, const LayerW* layers, size_t off_layers, char** base) {
+// may still be reading them), the tables are rewritten with synchronous
+// copies, and the kernel scratch [off_scratch, off_scratch + scratch_bytes)
+// is cleared: another model's scratch may have left, where this model keeps
+// its flagged residual words, bytes whose tag half could match a current tag.
+// Calls with the same model reach none of these steps.
+int setup(int dev, const mk_model_desc& d, const LayerW* layers, size_t off_layers, size_t off_scratch,
+          size_t scratch_bytes, char** base) {
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& s = g_dev[dev];
   if (!s.ready) {
@@ -94,6 +98,12 @@ int setup(int dev, const mk_model_desc& d, const LayerW* layers, size_t off_laye
     if (e != cudaSuccess) {
       s.n_layers = 0;
       return host_fail(MK_ERR_CUDA, (std::string("layer table upload: ") + cudaGetErrorString(e)).c_str());
+    }
+    e = cudaMemset(s.base + off_scratch, 0, scratch_bytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      s.n_layers = 0;
+      return host_fail(MK_ERR_CUDA, (std::string("scratch clear: ") + cudaGetErrorString(e)).c_str());
     }
     s.n_layers = d.n_layers;
     s.off_layers = off_layers;
@@ -170,7 +180,7 @@ extern "C" MK_API int mk_decode_step_static(
 
   if (d->head_dim / 2 > kMaxStaticHalf) return host_fail(MK_ERR_UNSUPPORTED, "head_dim above 128");
   char* base = nullptr;
-  if (int r = setup(dev, *d, layers, off_layers, &base)) return r;
+  if (int r = setup(dev, *d, layers, off_layers, off_scratch, need - off_scratch, &base)) return r;
   e = cudaFuncSetAttribute(kern.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kern.smem_bytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kern.fn, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxL1);
