@@ -166,8 +166,9 @@ MK_API int mk_create(const mk_model_desc* d, const mk_weights* w, mk_ctx** out);
  * reads together adjacent (the two RoPE rows of a q/k/v pair, the gate and up
  * rows of an FFN row).  An int3 record holds, per 32-value chunk, two words of
  * 2-bit fields and one word of 1-bit fields (the codes plus 4), in the byte
- * order of the kernel's dot products.  The paper has no counterpart: it exists so that the
- * allocation-free entry point can run on weights its caller packed. */
+ * order of the kernel's dot products.  The method itself has no such call: it
+ * exists so that the allocation-free entry point can run on weights its caller
+ * packed. */
 MK_API size_t mk_packed_bytes(const mk_model_desc* d);
 
 /* Pack the linear weights of w (logical layouts above) into dst_dev, a
@@ -327,8 +328,8 @@ MK_API int mk_get_info(mk_ctx* ctx, mk_info* info);
 /* Release every resource of the context (waits for its device work). */
 MK_API int mk_destroy(mk_ctx* ctx);
 
-/* Decode step that allocates no device memory.  The paper has no
- * counterpart.  It is for callers that cannot call cudaMalloc: a host that
+/* Decode step that allocates no device memory.  The method itself has no
+ * such call.  It is for callers that cannot call cudaMalloc: a host that
  * gives the library a fixed memory budget carved by its own allocator (and
  * so must not see allocations it did not plan), or a loop that must not take
  * the device-wide synchronisation that cudaMalloc / cudaFree can bring.
@@ -373,6 +374,15 @@ MK_API int mk_decode_step_static(const mk_model_desc* d, const mk_weights* w, co
                                  const int32_t* positions_host, const int32_t* pages_host,
                                  int32_t n, const int32_t* tokens_dev, int32_t* out_tokens_dev,
                                  int32_t* status_dev, void* stream);
+
+/* Bytes of the static array that mk_decode_step_static needs for model d on
+ * a device of `grid` SMs (the launch takes one block per SM): the RoPE table,
+ * the layer table and the kernel scratch, each 256-byte aligned
+ * (*need_out), and the array's size (*capacity_out, 8 MiB).  A model with
+ * *need_out > *capacity_out is one that mk_decode_step_static rejects with
+ * MK_ERR_UNSUPPORTED.  Host only, no device work.
+ * Errors: INVALID_ARG, UNSUPPORTED (as mk_create's description checks). */
+MK_API int mk_static_bytes(const mk_model_desc* d, int32_t grid, int64_t* need_out, int64_t* capacity_out);
 
 /* Message of the calling thread's last failure ("" if none). */
 MK_API const char* mk_last_error(void);

@@ -97,6 +97,8 @@ SIGNATURES = {
                                         C.c_void_p, C.c_int32, C.c_void_p, C.c_int32, C.POINTER(C.c_int32),
                                         C.POINTER(C.c_int32), C.POINTER(C.c_int32), C.c_int32,
                                         C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "mk_static_bytes": (C.c_int, [C.POINTER(mk_model_desc), C.c_int32, C.POINTER(C.c_int64),
+                                  C.POINTER(C.c_int64)]),
 }
 
 _lib = None
@@ -207,6 +209,14 @@ def mk_destroy(ctx: int):
 
 def mk_packed_bytes(desc: mk_model_desc) -> int:
     return int(load().mk_packed_bytes(C.byref(desc)))
+
+
+def mk_static_bytes(desc: mk_model_desc, grid: int) -> tuple:
+    """(bytes needed, bytes held) of the allocation-free entry point's array
+    for this model on a device of `grid` SMs."""
+    need, cap = C.c_int64(), C.c_int64()
+    _check(load().mk_static_bytes(C.byref(desc), grid, C.byref(need), C.byref(cap)))
+    return need.value, cap.value
 
 
 def mk_pack_weights(desc: mk_model_desc, weights: mk_weights, dst_dev: int, dst_bytes: int, stream: int = 0):

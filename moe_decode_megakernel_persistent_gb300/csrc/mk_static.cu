@@ -51,6 +51,17 @@ size_t rope_bytes(int head_dim) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Layout of the static array for a launch of `grid` blocks: RoPE table |
+// layer table | kernel scratch.  Returns the bytes the model needs.
+size_t static_need(const mk_model_desc& d, int grid, size_t* off_layers, size_t* off_scratch) {
+  const int max_units = grid + d.n_kv_heads * kMaxBatch;
+  const size_t ol = align256(rope_bytes(d.head_dim));
+  const size_t os = align256(ol + sizeof(LayerW) * d.n_layers);
+  if (off_layers) *off_layers = ol;
+  if (off_scratch) *off_scratch = os;
+  return os + host_carve_scratch(d, grid, max_units, nullptr, nullptr);
+}
+
 // With device `dev` current: the first call resolves the array's device
 // address.  When the RoPE parameters or the layer table differ from what the
 // array holds, the device is first drained (an earlier call, on any stream,
@@ -167,12 +178,10 @@ extern "C" MK_API int mk_decode_step_static(
   if ((d->hidden / 4 + sms - 1) / sms * 4 > kMaxRowsPerBlock)
     return host_fail(MK_ERR_UNSUPPORTED, "too few SMs for the compiled per-block row budget");
 
-  // layout of the static array: RoPE table | layer table | kernel scratch
   const int grid = sms;
   const int max_units = grid + d->n_kv_heads * kMaxBatch;
-  const size_t off_layers = align256(rope_bytes(d->head_dim));
-  const size_t off_scratch = align256(off_layers + sizeof(LayerW) * d->n_layers);
-  const size_t need = off_scratch + host_carve_scratch(*d, grid, max_units, nullptr, nullptr);
+  size_t off_layers = 0, off_scratch = 0;
+  const size_t need = static_need(*d, grid, &off_layers, &off_scratch);
   if (need > kStaticBytes)
     return host_fail(MK_ERR_UNSUPPORTED,
                      ("model needs " + std::to_string(need) + " bytes of static scratch; the array holds " +
@@ -242,5 +251,19 @@ extern "C" MK_API int mk_decode_step_static(
     e = cudaMemcpyAsync(status_dev, a.sc.err, sizeof(int32_t), cudaMemcpyDeviceToDevice, st);
     if (e != cudaSuccess) return host_fail(MK_ERR_CUDA, cudaGetErrorString(e));
   }
+  return MK_OK;
+}
+
+extern "C" MK_API int mk_static_bytes(const mk_model_desc* d, int32_t grid, int64_t* need_out,
+                                      int64_t* capacity_out) {
+  host_clear_error();
+  if (!need_out || !capacity_out) return host_fail(MK_ERR_INVALID_ARG, "NULL argument");
+  int shape = -1;
+  if (int r = host_validate_desc(d, &shape)) return r;
+  if (grid < 1) return host_fail(MK_ERR_INVALID_ARG, "grid must be >= 1");
+  if (d->n_layers > kMaxStaticLayers)
+    return host_fail(MK_ERR_INVALID_ARG, "more layers than the static layer table holds (128)");
+  *need_out = (int64_t)static_need(*d, grid, nullptr, nullptr);
+  *capacity_out = (int64_t)kStaticBytes;
   return MK_OK;
 }

@@ -111,3 +111,26 @@ def test_trace_bytes_layout(lib):
     per_layer = m.hidden + m.n_heads * m.head_dim + m.n_experts + 2 * m.top_k
     assert L.mk_trace_bytes(d, 3) == 4 * (m.n_layers * 3 * per_layer + 3 * m.vocab)
     assert L.mk_trace_bytes(d, 0) == 0
+
+
+def test_static_array_holds_the_flint_models_on_152_sms(lib):
+    """The allocation-free entry point keeps the RoPE table (8192 positions x
+    head_dim / 2 cos/sin pairs of fp32), the layer table and the kernel scratch
+    in one 8 MiB array: every benchmarked Flint model fits it on GB300's 152
+    SMs, and a grid far above that (more blocks, more attention partials) is
+    one the entry point would reject."""
+    models = [c.model for c in synth.CONFIGS.values()] + [c.model for c in synth.EXTRA.values()]
+    for m in models:
+        d = make_desc(m)
+        need, cap = L.mk_static_bytes(d, 152)
+        assert cap == 8 << 20
+        assert 8192 * (m.head_dim // 2) * 8 < need <= cap, (m, need)
+        assert L.mk_static_bytes(d, 1)[0] <= need <= L.mk_static_bytes(d, 304)[0]
+    need, cap = L.mk_static_bytes(_desc(3), 1024)
+    assert need > cap
+    with pytest.raises(L.MKError) as e:
+        L.mk_static_bytes(_desc(3), 0)
+    assert e.value.code == L.MK_ERR_INVALID_ARG
+    with pytest.raises(L.MKError) as e:
+        L.mk_static_bytes(_desc(3, hidden=512), 152)
+    assert e.value.code == L.MK_ERR_UNSUPPORTED
