@@ -90,8 +90,8 @@ typedef struct mk_model_desc {
   int32_t wdtype;       /* MK_F32 | MK_BF16 | MK_INT4_G64: the linear layers */
   int32_t page_tokens;  /* must be 128 */
   int32_t max_batch;    /* rows per launch, 1..16 */
-  int32_t max_ctx;      /* largest position + 1 any sequence may reach */
-  int32_t max_seqs;     /* sequence ids are 0 .. max_seqs-1 */
+  int32_t max_ctx;      /* largest position + 1 any sequence may reach, 1..1048576 */
+  int32_t max_seqs;     /* sequence ids are 0 .. max_seqs-1; 1..65536 */
   int32_t expert_wdtype;  /* format of exp_gate / exp_up / exp_down: equal to wdtype, or
                              MK_INT3_G64 with wdtype MK_INT4_G64 (int3 experts, int4
                              elsewhere); anything else is MK_ERR_INVALID_ARG */

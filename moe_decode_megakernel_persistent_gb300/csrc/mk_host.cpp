@@ -46,6 +46,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Host tables sized by the description (the RoPE table, max_ctx x head_dim / 2
+// pairs; the sequence table) stay bounded: 512 MiB and 64 Ki entries at most.
+constexpr int32_t kMaxCtx = 1 << 20;
+constexpr int32_t kMaxSeqs = 1 << 16;
+
 }  // namespace
 
 struct mk_ctx {
@@ -94,7 +99,8 @@ int validate_desc(const mk_model_desc* d, int* shape) {
   if (d->page_tokens != kPageTokens) return fail(MK_ERR_UNSUPPORTED, "page_tokens must be 128");
   if (d->max_batch < 1 || d->max_batch > kMaxBatch)
     return fail(MK_ERR_INVALID_ARG, "max_batch must be in [1, 16]");
-  if (d->max_ctx < 1 || d->max_seqs < 1) return fail(MK_ERR_INVALID_ARG, "max_ctx / max_seqs must be >= 1");
+  if (d->max_ctx < 1 || d->max_ctx > kMaxCtx || d->max_seqs < 1 || d->max_seqs > kMaxSeqs)
+    return fail(MK_ERR_INVALID_ARG, "max_ctx must be in [1, 1048576] and max_seqs in [1, 65536]");
   if (d->wdtype != MK_F32 && d->wdtype != MK_BF16 && d->wdtype != MK_INT4_G64)
     return fail(MK_ERR_INVALID_ARG, "unknown wdtype");
   if (d->expert_wdtype != d->wdtype && !(d->wdtype == MK_INT4_G64 && d->expert_wdtype == MK_INT3_G64))
@@ -254,7 +260,10 @@ int launch(mk_ctx* c, const int32_t* slots, const int32_t* positions, int n,
       if (a.slot[j] == a.slot[i] && a.pos[j] < a.new0[i]) a.new0[i] = a.pos[j];
   }
   attention_split(c, positions, n, &a.chunk, &a.n_units);
-  if (a.n_units > kMaxOwnUnits * c->grid) return fail(MK_ERR_INVALID_ARG, "more attention units than the grid can merge");
+  if (a.n_units > kMaxOwnUnits * c->grid) {
+    rollback();
+    return fail(MK_ERR_INVALID_ARG, "more attention units than the grid can merge");
+  }
   if (a.n_units > c->max_units) {
     rollback();
     return fail(MK_ERR_INVALID_ARG, "attention split exceeds the partials buffer");
@@ -721,6 +730,15 @@ MK_API int mk_kv_write(mk_ctx* c, int32_t seq_id, int32_t start_pos, int32_t n, 
   // segments of at most kMaxUpd - 1 pages, so one launch carries every new page it touches
   const int seg = (kMaxUpd - 1) * kPageTokens;
   const uint16_t* src = static_cast<const uint16_t*>(src_dev);
+  // pages taken by a segment whose launch fails go back to the pool (the
+  // block-table entries they were given are rewritten when next handed out)
+  auto give_back = [&](const KvXfer& x) {
+    for (int i = x.n_upd - 1; i >= 0; --i) {
+      q.pages.pop_back();
+      c->page_ref[x.upd[i].page] = 0;
+      c->free_pages.push_back(x.upd[i].page);
+    }
+  };
   const size_t per_pos = (size_t)2 * c->d.n_kv_heads * c->d.head_dim;  // bf16 values of one position, one layer
   for (int off = 0; off < n; off += seg) {
     const int m = std::min(seg, n - off);
@@ -740,7 +758,10 @@ MK_API int mk_kv_write(mk_ctx* c, int32_t seq_id, int32_t start_pos, int32_t n, 
     // when the call is split, else in one launch
     if (m == n) {
       x.src = src;
-      if (int r = launch_kv_xfer(x, (cudaStream_t)stream)) return r;
+      if (int r = launch_kv_xfer(x, (cudaStream_t)stream)) {
+        give_back(x);
+        return r;
+      }
     } else {
       for (int l = 0; l < c->d.n_layers; ++l) {
         KvXfer y = x;
@@ -748,7 +769,10 @@ MK_API int mk_kv_write(mk_ctx* c, int32_t seq_id, int32_t start_pos, int32_t n, 
         y.src = src + ((size_t)l * n + off) * per_pos;
         y.kv = c->kv_dev + (size_t)l * c->n_pages * 2 * c->d.n_kv_heads * kPageTokens * c->d.head_dim;
         if (l > 0) y.n_upd = 0;  // the entries are set by the first launch; reads use the list
-        if (int r = launch_kv_xfer(y, (cudaStream_t)stream)) return r;
+        if (int r = launch_kv_xfer(y, (cudaStream_t)stream)) {
+          give_back(x);
+          return r;
+        }
       }
     }
     q.open = true;
@@ -815,8 +839,8 @@ MK_API int mk_sync(mk_ctx* c, void* stream) {
   if (err[0] != 0) {
     MK_CUDA(cudaMemset(c->sc.err, 0, sizeof(err)));
     static const char* sites[] = {"?", "grid barrier", "page table", "attention unit", "token id",
-                                  "weight ring", "shared-memory plan"};
-    const int site = err[1] >= 1 && err[1] <= 6 ? err[1] : 0;
+                                  "weight ring", "shared-memory plan", "flagged residual word"};
+    const int site = err[1] >= 1 && err[1] <= SITE_FLAG ? err[1] : 0;
     return fail(err[0], std::string("device reported error ") + std::to_string(err[0]) + " at " +
                             sites[site] + " (site " + std::to_string(err[1]) + ", detail " +
                             std::to_string(err[2]) + ", " + std::to_string(err[3]) + ")");

@@ -54,6 +54,10 @@ def test_create_rejects_bad_descriptions_without_cuda(lib):
     assert lib.mk_create(C.byref(_desc(max_batch=17)), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
     assert lib.mk_create(C.byref(_desc(wdtype=9)), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
     assert lib.mk_create(C.byref(_desc(n_dense=5)), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    # host tables sized by max_ctx and max_seqs are bounded
+    assert lib.mk_create(C.byref(_desc(max_ctx=(1 << 20) + 1)), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_create(C.byref(_desc(max_seqs=(1 << 16) + 1)), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
+    assert lib.mk_create(C.byref(_desc(max_ctx=2 ** 31 - 1)), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
     assert lib.mk_create(C.byref(_desc()), C.byref(w), C.byref(out)) == L.MK_ERR_INVALID_ARG
     assert "NULL" in L.mk_last_error()
     assert out.value is None
