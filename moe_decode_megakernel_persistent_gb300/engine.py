@@ -31,6 +31,13 @@ def _ptr(t) -> int:
     return 0 if t is None else int(t.data_ptr())
 
 
+def _i32(t, n: int, what: str):
+    """The library reads n int32 values at t's address on the GPU."""
+    if not (isinstance(t, torch.Tensor) and t.dtype == torch.int32 and t.is_cuda and t.is_contiguous()
+            and t.numel() >= n):
+        raise ValueError(f"{what} must be a contiguous int32 CUDA tensor of at least {n} elements")
+
+
 def _lin(x) -> L.mk_linear:
     if isinstance(x, tuple):
         return L.mk_linear(_ptr(x[0]), _ptr(x[1]))
@@ -94,8 +101,10 @@ class Engine:
         """Run prompt tokens (int32 CUDA tensor) in chunks of at most 4096;
         returns the device int32[1] next token after the last position."""
         n = tokens.numel()
+        _i32(tokens, n, "tokens")
         if out is None:
             out = torch.empty(1, dtype=torch.int32, device=tokens.device)
+        _i32(out, 1, "out")
         for off in range(0, n, MAX_PREFILL):
             m = min(MAX_PREFILL, n - off)
             last = off + m == n
@@ -104,6 +113,9 @@ class Engine:
         return out
 
     def decode_step(self, seq_ids, tokens: torch.Tensor, positions, out: torch.Tensor):
+        n = len(seq_ids)
+        _i32(tokens, n, "tokens")
+        _i32(out, n, "out")
         L.mk_decode_step(self.ctx, list(seq_ids), _ptr(tokens), list(positions), _ptr(out),
                          self.stream)
         return out
@@ -300,8 +312,9 @@ class Batcher:
     """Continuous batching: every step, requests whose arrival step has come
     are prefilled and join; the active set (up to max_batch) runs as ONE
     decode launch; finished requests leave and release their pages.  Tokens
-    stay on the device between steps; the host reads them back once per step
-    in one copy (needed to know the tokens; they are also the output)."""
+    stay on the device between steps (a step's inputs are the previous
+    step's outputs); with read_back the host copies all generated tokens
+    back in one transfer after the last step."""
 
     def __init__(self, engine: Engine):
         self.e = engine
@@ -354,8 +367,12 @@ class Batcher:
                 active = still
             step += 1
         if read_back:
+            flat = [t for r in requests for t in r.generated]
+            host = torch.cat(flat).cpu().tolist() if flat else []
+            k = 0
             for r in requests:
-                r.generated = [int(t.item()) for t in r.generated]
+                n = len(r.generated)
+                r.generated, k = host[k:k + n], k + n
         out = {"steps": step, "launches": steps_run, "finish_step": max(r.finish_step for r in requests)}
         if timed:
             torch.cuda.synchronize()
