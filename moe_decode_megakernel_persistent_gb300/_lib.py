@@ -126,7 +126,11 @@ def _check(code: int):
         raise MKError(code, (_lib.mk_last_error() or b"").decode())
 
 
-def _i32(xs):
+def _i32(xs, n: int | None = None):
+    """Host int32 array of xs; with n, xs must hold exactly n values (the
+    library reads n of them)."""
+    if n is not None and len(xs) != n:
+        raise ValueError(f"expected {n} values, got {len(xs)}")
     arr = (C.c_int32 * len(xs))(*[int(x) for x in xs])
     return arr
 
@@ -152,7 +156,7 @@ def mk_prefill_chunk(ctx: int, seq_id: int, tokens_dev: int, n: int, start_pos: 
 def mk_decode_step(ctx: int, seq_ids, tokens_dev: int, positions, out_tokens_dev: int,
                    stream: int = 0):
     n = len(seq_ids)
-    _check(load().mk_decode_step(ctx, _i32(seq_ids), tokens_dev, _i32(positions), n,
+    _check(load().mk_decode_step(ctx, _i32(seq_ids), tokens_dev, _i32(positions, n), n,
                                  out_tokens_dev, stream))
 
 
@@ -233,7 +237,7 @@ def mk_decode_step_static(desc: mk_model_desc, weights: mk_weights, packed_dev: 
     n = len(slots)
     _check(load().mk_decode_step_static(C.byref(desc), C.byref(weights), packed_dev, kv_dev, n_pages,
                                         block_table_dev, max_pages_per_seq, _i32(slots),
-                                        _i32(positions), _i32(pages), n, tokens_dev,
+                                        _i32(positions, n), _i32(pages, n), n, tokens_dev,
                                         out_tokens_dev, status_dev or None, stream))
 
 

@@ -138,3 +138,12 @@ def test_static_array_holds_the_flint_models_on_152_sms(lib):
     with pytest.raises(L.MKError) as e:
         L.mk_static_bytes(_desc(3, hidden=512), 152)
     assert e.value.code == L.MK_ERR_UNSUPPORTED
+
+
+def test_per_row_lists_must_match_the_row_count(lib):
+    """The binding refuses lists shorter or longer than the rows it passes
+    (the library reads n host values from each)."""
+    with pytest.raises(ValueError):
+        L.mk_decode_step(None, [0, 1], 0, [5], 0)
+    with pytest.raises(ValueError):
+        L.mk_decode_step_static(_desc(), L.mk_weights(), 0, 0, 1, 0, 1, [0], [3, 4], [0], 0, 0)
